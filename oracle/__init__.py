@@ -1,0 +1,141 @@
+"""fp64 CPU oracle for the gated delta rule prefill (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline /
+reference arm may import this package. The product path (the CUDA library and
+its binding) never does, and the two share no code.
+
+The arithmetic lives in ``gdn_oracle.c`` (plain C, double precision,
+pthreads over (sequence, value head) units); this module compiles it with gcc
+when the shared object is missing or older than the source, and marshals
+arrays. See the C file's header for the definition it follows and the
+readings it takes where the pages are silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_gdn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+EPS = 1e-6
+
+
+def build(force: bool = False) -> str:
+    """Compile gdn_oracle.c into _gdn_oracle.so (gcc -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            common = [ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                      P, P, P, P, P, P, ctypes.c_int, P, ctypes.c_double, ctypes.c_int,
+                      ctypes.c_double, P, P, P]
+            lib.gdn_oracle_recurrent.argtypes = common + [ctypes.c_int]
+            lib.gdn_oracle_recurrent.restype = ctypes.c_int
+            lib.gdn_oracle_chunked.argtypes = common + [ctypes.c_int, ctypes.c_int]
+            lib.gdn_oracle_chunked.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f32(x) -> Optional[np.ndarray]:
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: widen exactly to float32 on the host
+        import torch
+        x = x.detach().to("cpu", torch.float32).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _i64(x) -> Optional[np.ndarray]:
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _run(kind, q, k, v, g, beta, cu_seqlens, initial_state=None, state_index=None,
+         scale: float = 0.0, l2norm: bool = True, eps: float = EPS, unit_mask=None,
+         chunk: int = 64, n_threads: Optional[int] = None, want_out: bool = True
+         ) -> Tuple[Optional[np.ndarray], np.ndarray]:
+    lib = _load()
+    q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
+    cu = _i64(cu_seqlens)
+    s0 = _f32(initial_state)
+    sidx = _i64(state_index)
+    T, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    N = cu.size - 1
+    if k.shape != q.shape or v.shape[0] != T or g.shape != (T, h_v) or beta.shape != (T, h_v):
+        raise ValueError("inconsistent shapes")
+    if int(cu[-1]) != T or int(cu[0]) != 0:
+        raise ValueError("cu_seqlens must start at 0 and end at T")
+    if not scale:
+        scale = float(d_k) ** -0.5
+    n_slots = 0 if s0 is None else s0.shape[0]
+    mask = None
+    if unit_mask is not None:
+        mask = np.ascontiguousarray(np.asarray(unit_mask, dtype=np.uint8).reshape(N * h_v))
+    out = np.zeros((T, h_v, d_v), dtype=np.float64) if want_out else None
+    fs = np.zeros((N, h_v, d_k, d_v), dtype=np.float64)
+    nt = default_threads() if n_threads is None else int(n_threads)
+    args = [N, _ptr(cu), h_qk, h_v, d_k, d_v, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+            _ptr(s0), n_slots, _ptr(sidx), float(scale), int(bool(l2norm)), float(eps),
+            _ptr(mask), _ptr(out), _ptr(fs)]
+    if kind == "recurrent":
+        rc = lib.gdn_oracle_recurrent(*args, nt)
+    else:
+        rc = lib.gdn_oracle_chunked(*args, int(chunk), nt)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the input (code {rc})")
+    return out, fs
+
+
+def recurrent(q, k, v, g, beta, cu_seqlens, initial_state=None, state_index=None, **kw):
+    """Token-by-token fp64 recurrence. Returns (out [T,h_v,d_v], final [N,h_v,d_k,d_v])."""
+    return _run("recurrent", q, k, v, g, beta, cu_seqlens, initial_state, state_index, **kw)
+
+
+def chunked(q, k, v, g, beta, cu_seqlens, initial_state=None, state_index=None, chunk=64, **kw):
+    """Chunked (WY/UT) fp64 form, for cross-checking the recurrence."""
+    return _run("chunked", q, k, v, g, beta, cu_seqlens, initial_state, state_index,
+                chunk=chunk, **kw)
+
+
+def run_workload(w, kind: str = "recurrent", **kw):
+    """Run the oracle on a workloads.Workload (host tensors)."""
+    fn = recurrent if kind == "recurrent" else chunked
+    return fn(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state, w.state_index,
+              scale=w.scale, **kw)
