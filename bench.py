@@ -1,0 +1,404 @@
+"""Benchmark of the gated delta rule prefill on one GB300 (or N independent replicas).
+
+Workload: 74 packed prompts of 80..3,399 tokens (log-uniform), 16 q/k heads,
+32 v heads, head dim 128, bf16 q/k/v and output, fp32 g/beta and final state
+(the single-candidate workload shape of the System1-Omni validation page,
+"Raw HF Transformers comparison"). Synthetic, seeded inputs.
+
+One step = one gdn_prefill_varlen call over the whole batch (the prep kernel
+and the chunk kernel). Inputs (about 1.6 GB) are larger than the 129 MB L2, so
+no flush is needed between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+                  [--kernel tc|simt] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0). Under torchrun every rank runs its own replica
+batch (seed offset by rank; no collective on the data path) and the line
+reports the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "GDN prefill tokens/s at 1 GB300 and % of roofline (HBM vs bf16 TC)"
+UNIT = "tokens/s"
+CONFIG_INDEX = 2
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_COLS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+# ---------------------------------------------------------------- workload accounting
+def algorithmic_bytes(w) -> int:
+    """Bytes the method must move once: q, k, v, g, beta, cu_seqlens read; o and
+    the final state written; each distinct gathered initial-state slot read."""
+    b = 0
+    for t in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens):
+        b += t.numel() * t.element_size()
+    b += w.v.numel() * torch.empty((), dtype=w.out_dtype).element_size()
+    b += w.num_seqs * w.h_v * w.d_k * w.d_v * 4
+    if w.initial_state is not None:
+        if w.state_index is None:
+            slots = w.num_seqs
+        else:
+            si = w.state_index.numpy()
+            slots = len(set(int(x) for x in si if x >= 0))
+        b += slots * w.h_v * w.d_k * w.d_v * 4
+    return int(b)
+
+
+def chunked_tensor_flops(w, C=64) -> int:
+    """Tensor-core products of the chunked form per chunk of length l:
+    per q/k head 4 l^2 d_k (K K^T, Q K^T); per v head 2 l^2 d_k + 4 l^2 d_v
+    (W, U, intra-chunk output) + 6 l d_k d_v (W S, Q S, K^T U')."""
+    f = 0
+    G = w.h_v // w.h_qk
+    for L in w.lengths:
+        full, rem = divmod(int(L), C)
+        for l, cnt in ((C, full), (rem, 1 if rem else 0)):
+            if cnt == 0:
+                continue
+            per_qk = 4 * l * l * w.d_k
+            per_v = 2 * l * l * w.d_k + 4 * l * l * w.d_v + 6 * l * w.d_k * w.d_v
+            f += cnt * (w.h_qk * per_qk + w.h_v * per_v)
+    del G
+    return int(f)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def profiled_traffic(kernel_name: str, workload_name: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel source (the summary records the source hash)."""
+    import hashlib
+    src = os.path.join(ROOT, "gated_deltanet_linear_prefill_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(f.read())
+    digest = h.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"{kernel_name}_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k_, v_ = line[2:].split(":", 1)
+                vals[k_.strip()] = v_.strip().strip("`")
+    if vals.get("csrc_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (200 ms period)."""
+
+    def __init__(self, gpu_index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(REASON_COLS, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle timing (CPU)
+def _oracle_sample(w, target_tokens: int, seed: int = 0):
+    """A fixed subset of the workload's sequences with about target_tokens rows."""
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.num_seqs)
+    pick, tot = [], 0
+    for n in order:
+        if tot >= target_tokens:
+            break
+        pick.append(int(n))
+        tot += int(w.lengths[n])
+    return sorted(pick), tot
+
+
+def time_oracle(w, target_tokens: int, seed: int = 0):
+    import oracle
+    seqs, tokens = _oracle_sample(w, target_tokens, seed)
+    sub = workloads.subset_sequences(w, seqs)
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.run_workload(sub, n_threads=threads)
+    dt = time.perf_counter() - t0
+    return tokens / dt, dt, len(seqs), tokens, threads
+
+
+# ---------------------------------------------------------------- distributed helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(tokens_per_rank: int, times_ms, world: int, device):
+    """Whole-job throughput: all ranks' tokens over the slowest rank's time."""
+    total_ms = reduce_max(float(sum(times_ms)), world, device)
+    steps = len(times_ms)
+    total_tokens = tokens_per_rank * world * steps
+    return total_tokens / (total_ms / 1e3), total_ms / steps
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    """The oracle arm: the fp64 CPU oracle as it stands, on host cores, each step
+    a bounded sample (about 1/16 of the batch's tokens) of the same workload."""
+    if rank != 0:
+        return
+    w = workloads.config(CONFIG_INDEX)
+    target = max(1, w.total_tokens // 16)
+    for i in range(args.warmup):
+        time_oracle(w, target, seed=i)
+    rates, secs, toks = [], [], []
+    for i in range(args.steps):
+        r, dt, nseq, tok, threads = time_oracle(w, target, seed=1000 + i)
+        rates.append(r)
+        secs.append(dt)
+        toks.append(tok)
+    value = sum(toks) / sum(secs)
+    sample = (f"per step a fixed random subset of the batch's sequences with ~{target} of "
+              f"{w.total_tokens} tokens, all {w.h_v} heads; {args.steps} steps")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workloads.CONFIG_NAMES[CONFIG_INDEX], "num_seqs": w.num_seqs,
+                   "total_tokens": w.total_tokens, "h_qk": w.h_qk, "h_v": w.h_v, "d": w.d_k},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gdn(args, world, rank, local):
+    import gated_deltanet_linear_prefill_gb300 as gdn
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl gdn")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    gdn.load_library()
+    w = workloads.config(CONFIG_INDEX, seed_offset=rank)
+    flags = gdn.GDN_FLAG_SIMT if args.kernel == "simt" else 0
+    d = w.to(device)
+    out = torch.empty(d.v.shape, dtype=d.out_dtype, device=device)
+    fs = torch.empty((d.num_seqs, d.h_v, d.d_k, d.d_v), dtype=torch.float32, device=device)
+    desc = gdn.make_desc(d.q, d.v, d.g, d.cu_seqlens, out_dtype=d.out_dtype,
+                         max_seqlen=w.max_seqlen, flags=flags)
+    ws = torch.empty(max(256, gdn.gdn_workspace_bytes(desc)), dtype=torch.uint8, device=device)
+    desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
+    stream = torch.cuda.current_stream(device)
+    launches_per_step = 2  # prep kernel + chunk kernel
+
+    def step():
+        rc = gdn.gdn_prefill_varlen(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, None, None, out,
+                                    fs, desc, stream)
+        if rc != gdn.GDN_OK:
+            raise gdn.GdnError(rc, "gdn_prefill_varlen")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    rc = gdn.gdn_get_device_status(desc, stream)
+    if rc != gdn.GDN_OK:
+        raise gdn.GdnError(rc, "device status")
+    torch.cuda.synchronize(device)
+
+    # ---- device-resident timing, per-step events on the launching stream
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    barrier(world)
+    torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clk = clocks.stop()
+    times = [a.elapsed_time(b) for a, b in ev]
+    value, ms_per_step = aggregate(w.total_tokens, times, world, device)
+
+    # ---- end to end: pinned host inputs -> device, call, results -> pinned host
+    host_in = {n: getattr(w, n).pin_memory() for n in ("q", "k", "v", "g", "beta", "cu_seqlens")}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_fs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_fs.numel() * host_fs.element_size()
+
+    def e2e_step():
+        for n, t in host_in.items():
+            getattr(d, n).copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+        host_fs.copy_(fs, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    e2e_value, _ = aggregate(w.total_tokens, [e0.elapsed_time(e1)] * 1, world, device)
+    e2e_value *= e2e_steps
+
+    # ---- roofline of the dominant kernel (the chunk kernel; the step also holds
+    # the one-block prep kernel, so the figure is a slight underestimate)
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
+    B = algorithmic_bytes(w)
+    F = chunked_tensor_flops(w)
+    step_s = statistics.median(times) / 1e3
+    achieved = B / step_s / 1e9
+    kernel_name = "gdn_tc_kernel" if args.kernel == "tc" else "gdn_simt_kernel"
+    traffic = profiled_traffic(kernel_name, workloads.CONFIG_NAMES[CONFIG_INDEX])
+    roofline_time = max(B / (hbm_peak * 1e9), F / (tc_peak * 1e12))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workloads.CONFIG_NAMES[CONFIG_INDEX], "num_seqs": w.num_seqs,
+                   "total_tokens": w.total_tokens, "max_seqlen": w.max_seqlen, "h_qk": w.h_qk,
+                   "h_v": w.h_v, "d_k": w.d_k, "d_v": w.d_v, "chunk": 64,
+                   "gates": "fp32", "out": "bf16", "state": "fp32", "kernel": args.kernel,
+                   "l2_flush": "none needed: inputs (%.2f GB) exceed the 129 MB L2" % (
+                       (B - w.num_seqs * w.h_v * w.d_k * w.d_v * 4) / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": B, "tensor_flops_per_launch": F,
+                     "tensor_tflops_achieved": F / step_s / 1e12,
+                     "frac_of_roofline_time": roofline_time / step_s},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, dt, nseq, tok, threads = time_oracle(w, max(1, w.total_tokens // 4), seed=0)
+        line["cpu_baseline"] = {
+            "value": r, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{nseq} of {w.num_seqs} sequences ({tok} of {w.total_tokens} tokens), "
+                      f"all {w.h_v} heads, fp64 recurrence, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--kernel", choices=["tc", "simt"], default="tc")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_gdn(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

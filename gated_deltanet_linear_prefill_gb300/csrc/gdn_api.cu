@@ -1,0 +1,280 @@
+// C ABI of the gated delta rule prefill library (declared in include/gdn.h):
+// host-side validation, workspace layout, the prep kernel (device checks of
+// cu_seqlens / state_index and the longest-first sequence order) and dispatch
+// to the chunk kernels.
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+
+constexpr int kPrepThreads = 1024;
+constexpr int kBins = 4096;  // sequences are ordered by chunk count, capped here
+
+// One block. Resets the status word, checks what only the device can see, and
+// writes the sequence order (most chunks first) by a counting sort on the
+// chunk count. The order only steers scheduling; results do not depend on it.
+__global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_t* order) {
+  __shared__ int hist[kBins];
+  __shared__ int warp_tot[kPrepThreads / 32];
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    p.status->code = 0u;
+    p.status->detail = 0u;
+    p.status->units_done = 0u;
+  }
+  for (int b = tid; b < kBins; b += kPrepThreads) hist[b] = 0;
+  __syncthreads();
+
+  const int N = p.num_seqs;
+  for (int n = tid; n < N; n += kPrepThreads) {
+    const int64_t b = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
+    if ((n == 0 && b != 0) || e < b || (n == N - 1 && e != p.total_tokens) ||
+        (p.max_seqlen > 0 && e - b > p.max_seqlen))
+      report(p.status, GDN_ERR_SEQLENS, (uint32_t)n);
+    if (p.initial_state && p.state_index) {
+      const int32_t s = p.state_index[n];
+      if (s < -1 || s >= p.num_state_slots) report(p.status, GDN_ERR_STATE_INDEX, (uint32_t)n);
+    }
+    int64_t bos, eos;
+    seq_bounds(p, n, bos, eos);
+    int64_t nc = (eos - bos + kChunk - 1) / kChunk;
+    const int bin = (int)(nc < kBins - 1 ? nc : kBins - 1);
+    atomicAdd(&hist[bin], 1);
+  }
+  __syncthreads();
+
+  // Exclusive prefix sum over bins taken from the top: start[b] = #seqs in bins > b.
+  constexpr int per = kBins / kPrepThreads;
+  int local[per];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    local[j] = hist[kBins - 1 - (tid * per + j)];
+    sum += local[j];
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    warp_tot[lane] = wi - w;  // exclusive
+  }
+  __syncthreads();
+  int run = warp_tot[warp] + incl - sum;
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    hist[kBins - 1 - (tid * per + j)] = run;
+    run += local[j];
+  }
+  __syncthreads();
+  for (int n = tid; n < N; n += kPrepThreads) {
+    int64_t bos, eos;
+    seq_bounds(p, n, bos, eos);
+    int64_t nc = (eos - bos + kChunk - 1) / kChunk;
+    const int bin = (int)(nc < kBins - 1 ? nc : kBins - 1);
+    const int pos = atomicAdd(&hist[bin], 1);
+    order[pos] = n;
+  }
+}
+
+cudaError_t launch_prep(const Params& p, cudaStream_t stream) {
+  gdn_prep_kernel<<<1, kPrepThreads, 0, stream>>>(p, const_cast<int32_t*>(p.order));
+  return cudaGetLastError();
+}
+
+cudaError_t set_smem_once(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static const void* done_kernel[256];
+  static int done_dev[256];
+  static int n_done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done_kernel[i] == kernel && done_dev[i] == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (n_done < 256) {
+    done_kernel[n_done] = kernel;
+    done_dev[n_done] = dev;
+    ++n_done;
+  }
+  return cudaSuccess;
+}
+
+// ---------------------------------------------------------------- host checks
+
+static bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  if (!a || !b || an == 0 || bn == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// sm_103 check, cached per device.
+static gdn_status check_arch() {
+  static std::mutex mu;
+  static int cached[64];  // 0 unknown, 1 ok, 2 not sm_103
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return GDN_ERR_ARCH;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return cached[dev] == 1 ? GDN_OK : GDN_ERR_ARCH;
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" int gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+extern "C" size_t gdn_workspace_bytes(const gdn_desc* desc) {
+  if (!desc || desc->num_seqs < 0) return 0;
+  return gdn::workspace_bytes(desc->num_seqs);
+}
+
+extern "C" const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_NULL: return "GDN_ERR_NULL: a required pointer is NULL";
+    case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE: unsupported or inconsistent sizes";
+    case GDN_ERR_DTYPE: return "GDN_ERR_DTYPE: unsupported storage type";
+    case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: misaligned pointer";
+    case GDN_ERR_SEQLENS: return "GDN_ERR_SEQLENS: cu_seqlens inconsistent (device check)";
+    case GDN_ERR_STATE_INDEX: return "GDN_ERR_STATE_INDEX: state_index out of range (device check)";
+    case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: an output overlaps an input";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case GDN_ERR_ARCH: return "GDN_ERR_ARCH: the current device is not sm_103";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA runtime call failed";
+    case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+  }
+  return "unknown gdn_status";
+}
+
+// Host-side validation shared by every entry point that launches. Fills `p`.
+static gdn_status validate(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta, const int32_t* cu_seqlens,
+                           const float* initial_state, const int32_t* state_index, void* out,
+                           float* final_state, const gdn_desc* d, Params& p) {
+  if (!d) return GDN_ERR_NULL;
+  const int64_t T = d->total_tokens;
+  const int N = d->num_seqs;
+  if (N < 0 || T < 0 || d->max_seqlen < 0) return GDN_ERR_SHAPE;
+  if (d->h_qk < 1 || d->h_v < 1 || d->h_v % d->h_qk != 0) return GDN_ERR_SHAPE;
+  if (!((d->d_k == 64 || d->d_k == 128) && (d->d_v == 64 || d->d_v == 128))) return GDN_ERR_SHAPE;
+  if (d->qkv_dtype != GDN_BF16) return GDN_ERR_DTYPE;
+  if (d->gate_dtype != GDN_BF16 && d->gate_dtype != GDN_F32) return GDN_ERR_DTYPE;
+  if (d->out_dtype != GDN_BF16 && d->out_dtype != GDN_F32) return GDN_ERR_DTYPE;
+  if (!cu_seqlens) return GDN_ERR_NULL;
+  if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_NULL;
+  if (initial_state && d->num_state_slots < 1) return GDN_ERR_SHAPE;
+  if (initial_state && !state_index && d->num_state_slots < N) return GDN_ERR_SHAPE;
+  if (!d->workspace) return GDN_ERR_WORKSPACE;
+  if (!aligned(d->workspace, 256) || d->workspace_bytes < gdn::workspace_bytes(N))
+    return GDN_ERR_WORKSPACE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(initial_state, 16) || !aligned(final_state, 16) || !aligned(g, 4) ||
+      !aligned(beta, 4) || !aligned(cu_seqlens, 4) || !aligned(state_index, 4))
+    return GDN_ERR_ALIGN;
+
+  const size_t gsz = d->gate_dtype == GDN_F32 ? 4 : 2;
+  const size_t osz = d->out_dtype == GDN_F32 ? 4 : 2;
+  const size_t qb = (size_t)T * d->h_qk * d->d_k * 2, vb = (size_t)T * d->h_v * d->d_v * 2;
+  const size_t gb = (size_t)T * d->h_v * gsz, ob = (size_t)T * d->h_v * d->d_v * osz;
+  const size_t sb = (size_t)d->h_v * d->d_k * d->d_v * 4;
+  const size_t isb = initial_state ? sb * (size_t)d->num_state_slots : 0;
+  const size_t fsb = final_state ? sb * (size_t)N : 0;
+  const size_t cub = sizeof(int32_t) * (size_t)(N + 1);
+  const size_t sib = state_index ? sizeof(int32_t) * (size_t)N : 0;
+  const size_t wsb = d->workspace_bytes;
+  struct R { const void* p; size_t n; } ins[] = {{q, qb}, {k, qb}, {v, vb}, {g, gb}, {beta, gb},
+                                                 {cu_seqlens, cub}, {initial_state, isb},
+                                                 {state_index, sib}, {d->workspace, wsb}};
+  for (const R& r : ins) {
+    if (overlaps(out, ob, r.p, r.n)) return GDN_ERR_ALIAS;
+    if (overlaps(final_state, fsb, r.p, r.n)) return GDN_ERR_ALIAS;
+  }
+  if (overlaps(out, ob, final_state, fsb)) return GDN_ERR_ALIAS;
+
+  const gdn_status arch = check_arch();
+  if (arch != GDN_OK) return arch;
+
+  memset(&p, 0, sizeof(p));
+  p.q = (const __nv_bfloat16*)q;
+  p.k = (const __nv_bfloat16*)k;
+  p.v = (const __nv_bfloat16*)v;
+  p.g = g;
+  p.beta = beta;
+  p.cu_seqlens = cu_seqlens;
+  p.initial_state = initial_state;
+  p.state_index = state_index;
+  p.out = out;
+  p.final_state = final_state;
+  p.status = (Status*)d->workspace;
+  p.order = (const int32_t*)((char*)d->workspace + kOrderOffset);
+  p.total_tokens = T;
+  p.num_seqs = N;
+  p.max_seqlen = d->max_seqlen;
+  p.h_qk = d->h_qk;
+  p.h_v = d->h_v;
+  p.d_k = d->d_k;
+  p.d_v = d->d_v;
+  p.num_state_slots = initial_state ? d->num_state_slots : 0;
+  p.gate_f32 = d->gate_dtype == GDN_F32;
+  p.out_f32 = d->out_dtype == GDN_F32;
+  p.l2norm = (d->flags & GDN_FLAG_NO_L2NORM) ? 0 : 1;
+  p.scale = d->scale != 0.0f ? d->scale : 1.0f / sqrtf((float)d->d_k);
+  return GDN_OK;
+}
+
+extern "C" gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v,
+                                         const void* g, const void* beta,
+                                         const int32_t* cu_seqlens, const float* initial_state,
+                                         const int32_t* state_index, void* out,
+                                         float* final_state, const gdn_desc* desc, void* stream) {
+  Params p;
+  const gdn_status st = validate(q, k, v, g, beta, cu_seqlens, initial_state, state_index, out,
+                                 final_state, desc, p);
+  if (st != GDN_OK) return st;
+  if (p.num_seqs == 0) return GDN_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_prep(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (launch_simt(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+extern "C" gdn_status gdn_get_device_status(const gdn_desc* desc, void* stream) {
+  if (!desc || !desc->workspace) return GDN_ERR_NULL;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t code = 0;
+  if (cudaMemcpyAsync(&code, desc->workspace, sizeof(code), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  return (gdn_status)code;
+}

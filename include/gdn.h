@@ -1,0 +1,151 @@
+/*
+ * gdn.h - C ABI of the GB300 (sm_103a) gated delta rule prefill library.
+ *
+ * The operation: for every packed sequence n and value head h, run the
+ * gated delta rule
+ *
+ *     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * over the sequence's rows, starting from a gathered initial state, and
+ * write every o_t and the final S.
+ *
+ * Where it comes from: System1-Omni PR #186 ("Purpose and summary" and the
+ * review-map row on device operations) runs the model's linear-attention
+ * layers as one batched call in which every candidate sequence keeps its own
+ * recurrent state and short continuations start from a prefix's state. The
+ * recurrence itself is the gated delta rule of "Gated Delta Networks:
+ * Improving Mamba2 with Delta Rule" (ICLR 2025), the open-jev-fast README's
+ * reference [5]. The kernels evaluate it in the chunked form that README
+ * describes for its GDN kernel (Phase 3 item 1): 64-token chunks, with the
+ * gate cumulative sum, the K K^T product, the unit-lower-triangular solve,
+ * the u/w products, the chunk output and the state update. q and k are
+ * L2-normalised inside the kernel; the README puts that normalisation in its
+ * input-prep kernel (Phase 2 item 1). Handing a prefix's final state to each
+ * continuation (README Phase 2 item 2) is the initial_state + state_index
+ * gather.
+ *
+ * Conventions shared by every entry point
+ *  - All tensors are caller-owned, contiguous, row-major device memory. The
+ *    library allocates nothing, never synchronises inside gdn_prefill_varlen,
+ *    and launches only on the given stream (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream).
+ *  - Value head h reads q/k head h / (h_v / h_qk) (contiguous groups).
+ *  - L2 normalisation: x / sqrt(sum x^2 + 1e-6), in fp32, for q and k.
+ *  - scale == 0 selects d_k^-1/2.
+ *  - Errors found on the host are returned before anything is launched and
+ *    nothing is written. Inconsistencies only the device can see (cu_seqlens,
+ *    state_index) set a status word in the workspace and leave the outputs
+ *    unspecified; the kernels never trap. Read it with gdn_get_device_status.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+/* Storage types. */
+typedef enum { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
+
+/* Result codes (the value of the device status word uses the same codes). */
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_NULL = 1,           /* a required pointer is NULL */
+  GDN_ERR_SHAPE = 2,          /* unsupported or inconsistent sizes */
+  GDN_ERR_DTYPE = 3,          /* unsupported storage type */
+  GDN_ERR_ALIGN = 4,          /* a pointer is not 16-byte aligned */
+  GDN_ERR_SEQLENS = 5,        /* device: cu_seqlens[0] != 0, decreasing, cu[N] != total_tokens,
+                                 or a length above max_seqlen */
+  GDN_ERR_STATE_INDEX = 6,    /* device: state_index outside [-1, num_state_slots) */
+  GDN_ERR_ALIAS = 7,          /* an output overlaps an input */
+  GDN_ERR_WORKSPACE = 8,      /* workspace NULL, misaligned or smaller than gdn_workspace_bytes */
+  GDN_ERR_ARCH = 9,           /* the current device is not sm_103 */
+  GDN_ERR_CUDA = 10,          /* a CUDA runtime call failed (launch, query, copy) */
+  GDN_ERR_DEVICE_TIMEOUT = 11 /* device: a bounded wait gave up */
+} gdn_status;
+
+/* Flags. */
+#define GDN_FLAG_NO_L2NORM 0x1u /* use q and k as given (tests of closed forms) */
+#define GDN_FLAG_SIMT 0x2u      /* run the CUDA-core (SIMT) kernel instead of the tensor-core one */
+
+/*
+ * Problem descriptor. Every field is read on the host at call time; the
+ * struct is not retained.
+ */
+typedef struct {
+  int32_t num_seqs;        /* N >= 0 (N = 0 writes nothing) */
+  int64_t total_tokens;    /* T = cu_seqlens[N]: a host copy, so the call never syncs */
+  int32_t max_seqlen;      /* upper bound on any sequence length, or 0 if unknown */
+  int32_t h_qk, h_v;       /* h_qk >= 1, h_v a multiple of h_qk */
+  int32_t d_k, d_v;        /* each 64 or 128 */
+  gdn_dtype qkv_dtype;     /* GDN_BF16 */
+  gdn_dtype gate_dtype;    /* g and beta: GDN_BF16 or GDN_F32 */
+  gdn_dtype out_dtype;     /* GDN_BF16 or GDN_F32 */
+  int32_t num_state_slots; /* rows of initial_state (ignored when it is NULL) */
+  float scale;             /* 0 => d_k^-1/2 */
+  uint32_t flags;          /* GDN_FLAG_* */
+  void* workspace;         /* caller-owned device memory, 256-byte aligned */
+  size_t workspace_bytes;  /* >= gdn_workspace_bytes(desc) */
+} gdn_desc;
+
+/* GDN_ABI_VERSION of the loaded library. */
+int gdn_abi_version(void);
+
+/*
+ * Bytes of device workspace gdn_prefill_varlen needs for this descriptor
+ * (depends on num_seqs and the head counts only; 0 for a NULL desc). The
+ * workspace holds the device status word and the work list. Its contents need
+ * no initialisation and are rewritten by every call; size it once for the
+ * largest batch and reuse it (one call at a time per workspace).
+ */
+size_t gdn_workspace_bytes(const gdn_desc* desc);
+
+/*
+ * Gated delta rule prefill over N packed sequences.
+ *
+ *  q, k          [T, h_qk, d_k]  bf16
+ *  v             [T, h_v,  d_v]  bf16
+ *  g             [T, h_v] natural-log decay per token and value head (any finite value)
+ *  beta          [T, h_v] write strength (used as given)
+ *  cu_seqlens    [N+1] int32, device: sequence n owns rows cu[n] .. cu[n+1]-1
+ *  initial_state [num_state_slots, h_v, d_k, d_v] fp32, or NULL (all sequences start from 0)
+ *  state_index   [N] int32, device: sequence n starts from initial_state[state_index[n]];
+ *                -1 selects a zero state; several sequences may name one slot. NULL means
+ *                slot n for sequence n (then num_state_slots >= N, else GDN_ERR_SHAPE).
+ *                Ignored when initial_state is NULL.
+ *  out           [T, h_v, d_v] out_dtype: o_t for every row
+ *  final_state   [N, h_v, d_k, d_v] fp32: S after each sequence's last row (S_0 for an
+ *                empty sequence), or NULL to skip
+ *
+ * Pointers q, k, v, out, initial_state, final_state must be 16-byte aligned;
+ * g and beta 4-byte aligned. out must not overlap any input; final_state must
+ * not overlap initial_state (one slot can feed many sequences). Asynchronous on
+ * `stream`; safe to capture in a CUDA graph (fixed launch shapes for a fixed
+ * descriptor, no allocation, no host synchronisation).
+ */
+gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, const int32_t* cu_seqlens,
+                              const float* initial_state, const int32_t* state_index, void* out,
+                              float* final_state, const gdn_desc* desc, void* stream);
+
+/*
+ * Synchronises `stream`, then returns the device status word the last call on
+ * this workspace left (GDN_OK if the device found nothing), or GDN_ERR_CUDA if
+ * the synchronisation or the read failed.
+ */
+gdn_status gdn_get_device_status(const gdn_desc* desc, void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* gdn_status_string(gdn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

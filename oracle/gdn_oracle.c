@@ -12,11 +12,11 @@
  *   o_t = scale * S_t^T q_t
  *
  * the gated delta rule of "Gated Delta Networks: Improving Mamba2 with Delta
- * Rule" (Yang, Kautz, Hatamizadeh, ICLR 2025), which the pages cite as the
- * model's recurrent linear-attention computation (System1-Omni PR #186,
- * "Purpose and summary"; open-jev-fast README, reference [5]). k_t and q_t are
- * L2-normalised first (open-jev-fast README, Phase 2 item 1, "Gated DeltaNet
- * input prep ... L2 norm"), as x / sqrt(|x|^2 + eps).
+ * Rule" (Yang, Kautz, Hatamizadeh, ICLR 2025), the model's recurrent
+ * linear-attention layer in System1-Omni PR #186 ("Purpose and summary") and
+ * reference [5] of the open-jev-fast README. k_t and q_t are L2-normalised
+ * first, as x / sqrt(|x|^2 + eps); that README does the normalisation in its
+ * linear-attention input-prep kernel (Phase 2 item 1).
  *
  * Readings taken where the pages are silent:
  *  - the decay multiplies the whole (I - beta k k^T) S term, so the delta

@@ -1,0 +1,153 @@
+"""The C-ABI library loads, exports every entry point include/gdn.h declares,
+and rejects bad calls on the host before touching the GPU.
+
+No test here launches a kernel: every call made with fake (never dereferenced)
+device addresses fails host validation first. That ordering is part of the
+contract (host errors are returned before any launch and write nothing).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import gated_deltanet_linear_prefill_gb300 as gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+FAKE = 1 << 20  # an aligned address that is never dereferenced (validation fails first)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted([
+        "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_get_device_status",
+        "gdn_status_string"])
+
+
+def test_library_exports_every_declared_symbol():
+    lib = gdn.load_library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings():
+    assert gdn.gdn_abi_version() == 1
+    for code, name in enumerate(gdn.STATUS_NAMES):
+        assert gdn.gdn_status_string(code).startswith(name)
+    assert "unknown" in gdn.gdn_status_string(99)
+
+
+def test_desc_layout_matches_header():
+    # int32, (pad), int64, int32 x5, enum x3, int32, float, uint32, (pad), void*, size_t
+    assert ctypes.sizeof(gdn.GdnDesc) == 80
+    assert gdn.GdnDesc.workspace.offset == 64
+
+
+def base_desc(**kw):
+    d = gdn.GdnDesc()
+    d.num_seqs, d.total_tokens, d.max_seqlen = 2, 100, 0
+    d.h_qk, d.h_v, d.d_k, d.d_v = 16, 32, 128, 128
+    d.qkv_dtype, d.gate_dtype, d.out_dtype = gdn.GDN_BF16, gdn.GDN_F32, gdn.GDN_BF16
+    d.num_state_slots, d.scale, d.flags = 0, 0.0, 0
+    d.workspace = FAKE * 64
+    d.workspace_bytes = 1 << 16
+    for k_, v_ in kw.items():
+        setattr(d, k_, v_)
+    return d
+
+
+def call(desc, **ptrs):
+    # Fake addresses are only ever passed where no device exists, so that a
+    # validation slip can never turn into a launch on bogus memory.
+    if torch.cuda.is_available():
+        pytest.skip("fake-pointer validation calls run only without a device")
+    lib = gdn.load_library()
+    T = desc.total_tokens if desc else 100
+    qb = max(T, 1) * 16 * 128 * 2
+    base = dict(q=FAKE, k=FAKE + 4 * qb, v=FAKE + 8 * qb, g=FAKE + 16 * qb, beta=FAKE + 18 * qb,
+                cu=FAKE + 20 * qb, init=None, sidx=None, out=FAKE + 32 * qb, fs=None)
+    base.update(ptrs)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_prefill_varlen(P(base["q"]), P(base["k"]), P(base["v"]), P(base["g"]),
+                                  P(base["beta"]), P(base["cu"]), P(base["init"]),
+                                  P(base["sidx"]), P(base["out"]), P(base["fs"]),
+                                  ctypes.byref(desc) if desc is not None else None, None)
+
+
+E = {n: i for i, n in enumerate(gdn.STATUS_NAMES)}
+
+
+def test_null_desc_and_pointers():
+    lib = gdn.load_library()
+    assert lib.gdn_workspace_bytes(None) == 0
+    assert call(None) == E["GDN_ERR_NULL"]
+    assert call(base_desc(), q=None) == E["GDN_ERR_NULL"]
+    assert call(base_desc(), cu=None) == E["GDN_ERR_NULL"]
+    assert call(base_desc(), out=None) == E["GDN_ERR_NULL"]
+    assert lib.gdn_get_device_status(None, None) == E["GDN_ERR_NULL"]
+
+
+@pytest.mark.parametrize("field,value", [("h_qk", 0), ("h_v", 24), ("d_k", 96), ("d_v", 32),
+                                         ("num_seqs", -1), ("total_tokens", -5),
+                                         ("max_seqlen", -1)])
+def test_shape_errors(field, value):
+    d = base_desc(**{field: value})
+    if field == "h_v":
+        d.h_qk = 16  # 24 is not a multiple of 16
+    assert call(d) == E["GDN_ERR_SHAPE"]
+
+
+def test_initial_state_needs_slots():
+    assert call(base_desc(num_state_slots=0), init=FAKE * 200) == E["GDN_ERR_SHAPE"]
+    # NULL state_index means slot n for sequence n: fewer slots than sequences is an error
+    assert call(base_desc(num_state_slots=1), init=FAKE * 200) == E["GDN_ERR_SHAPE"]
+
+
+@pytest.mark.parametrize("field,value", [("qkv_dtype", gdn.GDN_F32), ("gate_dtype", 7),
+                                         ("out_dtype", 5)])
+def test_dtype_errors(field, value):
+    assert call(base_desc(**{field: value})) == E["GDN_ERR_DTYPE"]
+
+
+def test_workspace_errors():
+    need = gdn.gdn_workspace_bytes(base_desc())
+    assert need >= 256 + 4 * 2
+    assert call(base_desc(workspace=None)) == E["GDN_ERR_WORKSPACE"]
+    assert call(base_desc(workspace=FAKE * 64 + 16)) == E["GDN_ERR_WORKSPACE"]
+    assert call(base_desc(workspace_bytes=need - 1)) == E["GDN_ERR_WORKSPACE"]
+    big = base_desc(num_seqs=100000)
+    assert gdn.gdn_workspace_bytes(big) >= 256 + 4 * 100000
+
+
+def test_alignment_errors():
+    assert call(base_desc(), q=FAKE + 8) == E["GDN_ERR_ALIGN"]
+    assert call(base_desc(), out=FAKE * 40 + 2) == E["GDN_ERR_ALIGN"]
+    assert call(base_desc(), g=FAKE * 30 + 2) == E["GDN_ERR_ALIGN"]
+
+
+def test_alias_errors():
+    d = base_desc()
+    # out overlapping v
+    assert call(d, out=FAKE + 8 * 100 * 16 * 128 * 2 + 64) == E["GDN_ERR_ALIAS"]
+    # final_state overlapping initial_state (one slot may feed many sequences)
+    d = base_desc(num_state_slots=2)
+    assert call(d, init=FAKE * 400, fs=FAKE * 400 + 1024) == E["GDN_ERR_ALIAS"]
+    # final_state overlapping the workspace
+    d = base_desc()
+    assert call(d, fs=d.workspace) == E["GDN_ERR_ALIAS"]
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path only")
+def test_valid_call_without_a_device_reports_cuda_or_arch():
+    """With every host check passing and no GPU, the arch query fails cleanly."""
+    d = base_desc()
+    rc = call(d)
+    assert rc in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
