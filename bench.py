@@ -290,9 +290,16 @@ def run_gdn(args, world, rank, local):
         raise gdn.GdnError(rc, "device status")
     torch.cuda.synchronize(device)
 
-    # ---- device-resident timing, per-step events on the launching stream
+    # ---- device-resident timing, per-step events on the launching stream. The
+    # clock sampler starts one second of untimed steps before the timed region
+    # (its 200 ms period needs samples) and stops right after it.
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(8):
+            step()
+        torch.cuda.synchronize(device)
     barrier(world)
     torch.cuda.synchronize(device)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -307,34 +314,38 @@ def run_gdn(args, world, rank, local):
     times = [a.elapsed_time(b) for a, b in ev]
     value, ms_per_step = aggregate(w.total_tokens, times, world, device)
 
+    e2e_line = None
     # ---- end to end: pinned host inputs -> device, call, results -> pinned host
-    host_in = {n: getattr(w, n).pin_memory() for n in ("q", "k", "v", "g", "beta", "cu_seqlens")}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    host_fs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * host_out.element_size() + host_fs.numel() * host_fs.element_size()
+    if not args.no_e2e:
+        host_in = {n: getattr(w, n).pin_memory() for n in ("q", "k", "v", "g", "beta", "cu_seqlens")}
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        host_fs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = host_out.numel() * host_out.element_size() + host_fs.numel() * host_fs.element_size()
 
-    def e2e_step():
-        for n, t in host_in.items():
-            getattr(d, n).copy_(t, non_blocking=True)
-        step()
-        host_out.copy_(out, non_blocking=True)
-        host_fs.copy_(fs, non_blocking=True)
+        def e2e_step():
+            for n, t in host_in.items():
+                getattr(d, n).copy_(t, non_blocking=True)
+            step()
+            host_out.copy_(out, non_blocking=True)
+            host_fs.copy_(fs, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(device)
-    e2e_steps = max(3, min(args.steps, 10))
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    barrier(world)
-    e2e_value, _ = aggregate(w.total_tokens, [e0.elapsed_time(e1)] * 1, world, device)
-    e2e_value *= e2e_steps
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        e2e_steps = max(3, min(args.steps, 10))
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e2e_value, _ = aggregate(w.total_tokens, [e0.elapsed_time(e1)] * 1, world, device)
+        e2e_value *= e2e_steps
+        e2e_line = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)}
 
     # ---- roofline of the dominant kernel (the chunk kernel; the step also holds
     # the one-block prep kernel, so the figure is a slight underestimate)
@@ -363,17 +374,22 @@ def run_gdn(args, world, rank, local):
                      "algorithmic_bytes_per_launch": B, "tensor_flops_per_launch": F,
                      "tensor_tflops_achieved": F / step_s / 1e12,
                      "frac_of_roofline_time": roofline_time / step_s},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+        "e2e": e2e_line,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, dt, nseq, tok, threads = time_oracle(w, max(1, w.total_tokens // 4), seed=0)
+        # the whole batch through the fp64 oracle, repeated until at least 10 s of CPU work
+        tot_tok, tot_s, passes = 0, 0.0, 0
+        while tot_s < 10.0 and passes < 20:
+            r, dt, nseq, tok, threads = time_oracle(w, w.total_tokens, seed=0)
+            tot_tok += tok
+            tot_s += dt
+            passes += 1
         line["cpu_baseline"] = {
-            "value": r, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{nseq} of {w.num_seqs} sequences ({tok} of {w.total_tokens} tokens), "
-                      f"all {w.h_v} heads, fp64 recurrence, {dt:.1f} s"}
+            "value": tot_tok / tot_s, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the whole batch ({w.num_seqs} sequences, {w.total_tokens} tokens, "
+                      f"{w.h_v} heads), fp64 recurrence, {passes} passes in {tot_s:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -386,6 +402,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--kernel", choices=["tc", "simt"], default="tc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer timing")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="seconds of untimed steps while the clock sampler warms up")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     try:

@@ -264,7 +264,8 @@ extern "C" gdn_status gdn_prefill_varlen(const void* q, const void* k, const voi
   if (p.num_seqs == 0) return GDN_OK;
   cudaStream_t s = (cudaStream_t)stream;
   if (launch_prep(p, s) != cudaSuccess) return GDN_ERR_CUDA;
-  if (launch_simt(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+  const cudaError_t e = (desc->flags & GDN_FLAG_SIMT) ? launch_simt(p, s) : launch_tc(p, s);
+  if (e != cudaSuccess) return GDN_ERR_CUDA;
   return GDN_OK;
 }
 

@@ -92,5 +92,6 @@ cudaError_t set_smem_once(const void* kernel, int bytes);
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_prep(const Params& p, cudaStream_t stream);
 cudaError_t launch_simt(const Params& p, cudaStream_t stream);
+cudaError_t launch_tc(const Params& p, cudaStream_t stream);
 
 }  // namespace gdn
