@@ -18,18 +18,23 @@
 //   [K;Q] K^T          -> KK^T (lanes 0-63), QK^T (lanes 64-127)       (per chunk)
 //   W^T  = K^T T_w^T    (T_w = T diag(beta e^G r^k), bf16)
 //   U'^T = V^T T_b^T (T_b = T diag(beta) as bf16 hi + lo) - S^T W^T
-//   O^T  = S^T Qh^T + U'^T P^T      (Qh_i = e^{G_i} q_i, P_ij = e^{G_i-G_j} r^k_j q_i.k_j)
+//   QS^T = -S^T Q^T                 (the inter-chunk term, weighted by e^{G_i} at the end)
+//   O^T  = U'^T P^T                 (P_ij = e^{G_i-G_j} r^k_j q_i.k_j, j <= i)
 //   S^T += (U' diag(s))^T K         (s_j = e^{G_m-G_j} r^k_j; U' diag(s) as bf16 hi + lo,
 //                                    read by the MMA straight from TMEM)
 // Operand precision: the products feeding the fp32 state carry T and U' as
 // bf16 hi + lo pairs (about 16 significant bits); S and W enter as bf16; every
-// accumulation is fp32 in TMEM. The triangular solve, decays and norms run on
-// CUDA cores in fp32.
+// accumulation is fp32 in TMEM. Decays and norms run on CUDA cores in fp32.
+// The 64x64 unit-lower-triangular inverse inverts its 16x16 diagonal blocks
+// by fp32 substitution and merges them with small tf32 mma.sync products in a
+// three-pass hi/lo split (fp32-level accuracy); the open-jev-fast README's GDN
+// kernel also builds its inverse with tf32 MMAs in blocks (Phase 3 item 1).
 //
-// Warp roles (384 threads): warp 0 loads K/Q/V tiles by TMA (128-byte swizzle)
-// and the gates; warp 1 allocates TMEM and issues the state-independent MMAs;
+// Warp roles (384 threads): warp 0 loads K/Q/V tiles by TMA (128-byte swizzle),
+// clears rows past the sequence end, scans the gates and takes the q norms
+// (r^k comes from the diagonal of K K^T); warp 1 allocates TMEM and issues the state-independent MMAs;
 // warp 2 issues the state-dependent MMAs; warps 4-7 (WG-A) prepare chunk c+1
-// (norms, A and P, the solve, T_b / T_w / Qh, W^T) while warps 8-11 (WG-B) run
+// (A and P, the solve, T_b / T_w, W^T) while warps 8-11 (WG-B) run
 // chunk c's state step (S -> bf16 operand, U' split, output epilogue). Every
 // mbarrier wait is bounded: on timeout the CTA reports GDN_ERR_DEVICE_TIMEOUT
 // and unwinds.
@@ -55,21 +60,38 @@ constexpr uint32_t TM_KQ = 256;  // [K;Q] K^T, then W^T                     (64)
 constexpr uint32_t TM_UH = 320;  // (U' diag(s))^T hi, packed bf16 pairs    (32)
 constexpr uint32_t TM_UL = 352;  // (U' diag(s))^T lo                       (32)
 constexpr uint32_t TM_UU = 384;  // U'^T as bf16                            (32)
+constexpr uint32_t TM_QS = 448;  // -S^T Q^T: lanes d_v, columns i          (64)
 constexpr uint32_t kTmemCols = 512;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMaxDecaySpan = 80.0f;  // chunks whose log-decay spans more use exact exps
 
 // Barrier indices
 enum {
-  B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_KQ_READY, B_KQ_DONE, B_P1_MID, B_W_DONE,
-  B_P1_DONE0, B_P1_DONE1, B_BUF_FREE0, B_BUF_FREE1, B_S_READY, B_UP_DONE, B_UOPS_READY,
-  B_O_DONE, B_DRAIN1, B_DRAIN2, kNumBars
+  B_TMA0 = 0, B_TMA1, B_READY0, B_READY1, B_EMPTY0, B_EMPTY1, B_KQ_DONE, B_P1_MID, B_W_DONE,
+  B_KQ_FREE, B_P1_DONE0, B_P1_DONE1, B_BUF_FREE0, B_BUF_FREE1, B_S_READY, B_UP_DONE,
+  B_UOPS_READY, B_O_DONE, B_DRAIN1, B_DRAIN2, kNumBars
 };
 
-// Per-chunk scalars shared by WG-A (writer) and WG-B (reader).
+// Per-chunk values WG-A hands to WG-B (double-buffered by chunk parity).
 struct ChunkScalars {
-  float rk[64], rq[64], G[64], beta[64], eG[64], s[64], tw[64];
-  float eGC;
-  int pad[15];
+  float cq[64];  // -scale r^q_i e^{G_i}: weight of the (-S^T q_i) column
+  float co[64];  // scale r^q_i: weight of the intra-chunk column
+  float s[64];   // e^{G_m - G_j} r^k_j: state-update weight of row j
+  float eGC;     // e^{G_m}: decay of the whole chunk
+  int pad[31];
 };
+// WG-A private per-chunk values.
+struct PrepScalars {
+  float d[64];     // r^k_j e^{Gmax - G_j}
+  float r[64];     // r^k_j
+  float tw[64];    // beta_j e^{G_j} r^k_j: column scale of T_w
+  float beta[64];
+};
+// Stage scalars written by the producer: G[64], beta[64], rq[64], Gmax, Gmin.
+constexpr int SC_G = 0, SC_B = 64, SC_RQ = 128, SC_GMAX = 192, SC_GMIN = 193;
+
+constexpr int LDF = 68;  // row stride (floats) of the fp32 64x64 scratch of the solve
 
 // Shared-memory layout, byte offsets from a 1024-aligned base.
 template <int DK, int DV>
@@ -78,19 +100,22 @@ struct TcLayout {
   static constexpr int NVA = DV / 64;
   static constexpr uint32_t KQ_BYTES = NKA * 16384u;  // [K ac][Q ac] per atom column
   static constexpr uint32_t V_BYTES = NVA * 8192u;
-  static constexpr uint32_t GATE_BYTES = 1024u;  // G[64], beta[64] fp32
-  static constexpr uint32_t STAGE_BYTES = KQ_BYTES + V_BYTES + GATE_BYTES;
+  static constexpr uint32_t SCAL_BYTES = 1024u;
+  static constexpr uint32_t STAGE_BYTES = KQ_BYTES + V_BYTES + SCAL_BYTES;
   static constexpr uint32_t STAGE0 = 0;
+  static constexpr uint32_t SCR_BYTES = 17408u;           // 64 x 68 fp32, 1024-aligned size
   static constexpr uint32_t P0 = 2 * STAGE_BYTES;         // P (bf16 64x64) x2
   static constexpr uint32_t TB0 = P0 + 2 * 8192u;         // T_b hi/lo (or fp32 T) x2
-  static constexpr uint32_t TW = TB0 + 2 * 16384u;        // T_w bf16
+  static constexpr uint32_t TW = TB0 + 2 * SCR_BYTES;     // T_w bf16
   static constexpr uint32_t WT0 = TW + 8192u;             // W^T bf16 128x64 (or fp32 A) x2
-  static constexpr uint32_t SOP = WT0 + 2 * 16384u;       // -S^T bf16 [128][DK]
-  static constexpr uint32_t SOP_BYTES = NKA * 16384u;
+  static constexpr uint32_t SOP = WT0 + 2 * SCR_BYTES;    // -S^T bf16 [128][DK]; output staging
+  static constexpr uint32_t SOP_BYTES =
+      (NKA * 16384u > 64u * DV * 4u) ? NKA * 16384u : 64u * DV * 4u;
   static constexpr bool NEED_ZERO = (DK == 64) || (DV == 64);
   static constexpr uint32_t ZERO = SOP + SOP_BYTES;       // 8 KB of zeros (M padding)
-  static constexpr uint32_t SC0 = ZERO + (NEED_ZERO ? 8192u : 0u);
-  static constexpr uint32_t BARS = SC0 + 2 * (uint32_t)sizeof(ChunkScalars);
+  static constexpr uint32_t CS0 = ZERO + (NEED_ZERO ? 8192u : 0u);
+  static constexpr uint32_t PS = CS0 + 2 * (uint32_t)sizeof(ChunkScalars);
+  static constexpr uint32_t BARS = PS + (uint32_t)sizeof(PrepScalars);
   static constexpr uint32_t MISC = BARS + kNumBars * 8u;  // tmem base, abort flag
   static constexpr uint32_t TOTAL = MISC + 64u;
   static constexpr uint32_t DYN_SMEM = TOTAL + 1024u;     // alignment slack
@@ -102,124 +127,118 @@ struct Tmaps {
   CUtensorMap q, k, v;
 };
 
-// Swizzled fp32 64x64 scratch (A and T of the solve): element (r, c).
-__device__ __forceinline__ int fidx(int r, int c) { return r * 64 + (c ^ (r & 31)); }
-
 // ---------------------------------------------------------------- the solve
-// T = (I + A)^-1 for the 64x64 strictly-lower A, by 16x16 blocks: invert the
-// diagonal blocks by forward substitution, then T_ij = -D_i sum_{k=j}^{i-1}
-// A_ik T_kj level by level. 128 threads (4 warps).
+// mma.sync m16n8k8 (tf32) with a three-pass hi/lo split, which carries the
+// products at about fp32 accuracy. Fragments follow the PTX m16n8k8 layouts:
+// a0..a3 = (g, t), (g+8, t), (g, t+4), (g+8, t+4); b0, b1 = (t, g), (t+4, g);
+// c0..c3 = (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1), g = lane/4, t = lane%4.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// C[16x16] += X[16x16 block at (xr, xc)] * Y[16x16 block at (yr, yc)], fp32 smem, stride LDF.
+__device__ __forceinline__ void gemm16(const float* X, int xr, int xc, const float* Y, int yr, int yc,
+                                       float (&c)[2][4], int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    const int k0 = ks * 8;
+    const float af[4] = {X[(xr + g) * LDF + xc + k0 + t], X[(xr + g + 8) * LDF + xc + k0 + t],
+                         X[(xr + g) * LDF + xc + k0 + t + 4],
+                         X[(xr + g + 8) * LDF + xc + k0 + t + 4]};
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ah[e] = to_tf32(af[e]);
+      al[e] = to_tf32(af[e] - __uint_as_float(ah[e]));
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float b0 = Y[(yr + k0 + t) * LDF + yc + nt * 8 + g];
+      const float b1 = Y[(yr + k0 + t + 4) * LDF + yc + nt * 8 + g];
+      const uint32_t bh0 = to_tf32(b0), bh1 = to_tf32(b1);
+      const uint32_t bl0 = to_tf32(b0 - __uint_as_float(bh0)),
+                     bl1 = to_tf32(b1 - __uint_as_float(bh1));
+      mma_tf32(c[nt], al, bh0, bh1);
+      mma_tf32(c[nt], ah, bl0, bl1);
+      mma_tf32(c[nt], ah, bh0, bh1);
+    }
+  }
+}
+__device__ __forceinline__ void store16(float* M, int r0, int c0, const float (&c)[2][4], float sgn,
+                                        int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    M[(r0 + g) * LDF + c0 + nt * 8 + 2 * t] = sgn * c[nt][0];
+    M[(r0 + g) * LDF + c0 + nt * 8 + 2 * t + 1] = sgn * c[nt][1];
+    M[(r0 + g + 8) * LDF + c0 + nt * 8 + 2 * t] = sgn * c[nt][2];
+    M[(r0 + g + 8) * LDF + c0 + nt * 8 + 2 * t + 1] = sgn * c[nt][3];
+  }
+}
+
+// T = (I + A)^-1 for the strictly-lower 64x64 A (fp32, stride LDF), by 16x16
+// blocks: the four diagonal blocks D_b by forward substitution in fp32, the
+// two 16-row merges T_{b+1,b} = -D_{b+1} A_{b+1,b} D_b inside each 32x32
+// diagonal block, then T_21 = -T_22 (A_21 T_11) for the lower-left 32x32
+// block. Blocks above the diagonal are not written. 128 threads (4 warps).
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ T,
                                                  int wa) {
   const int wq = wa >> 5, ln = wa & 31;
-  // diagonal blocks: warp wq owns block wq, lane l < 16 owns column l
   {
-    const int b = wq * 16;
-    if (ln < 16) {
-      const int l = ln;
-      float t[16];
+    // lanes l and l + 16 both own column l and split each row's sum by parity
+    const int b = wq * 16, l = ln & 15, hp = ln >> 4;
+    float t[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) t[i] = (i == l) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) t[i] = (i == l) ? 1.f : 0.f;
 #pragma unroll
-      for (int i = 1; i < 16; ++i) {
-        float s = 0.f;
+    for (int i = 1; i < 16; ++i) {
+      float sacc = 0.f;
 #pragma unroll
-        for (int x = 0; x < i; ++x) s = fmaf(A[fidx(b + i, b + x)], t[x], s);
-        if (i > l) t[i] = -s;
+      for (int x = 0; x < i; x += 2) {
+        const float tx = hp == 0 ? t[x] : ((x + 1 < i) ? t[x + 1] : 0.f);
+        sacc = fmaf(A[(b + i) * LDF + b + x + hp], tx, sacc);
       }
+      sacc += __shfl_xor_sync(0xffffffffu, sacc, 16);
+      if (i > l) t[i] = -sacc;
+    }
+    if (hp == 0) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) T[fidx(b + i, b + l)] = t[i];
+      for (int i = 0; i < 16; ++i) T[(b + i) * LDF + b + l] = t[i];
     }
   }
   named_bar_sync(1, 128);
-  // level 1: T_{i,i-1}, warp wq -> block (wq+1, wq)
-  if (wq < 3) {
-    const int bi = (wq + 1) * 16, bj = wq * 16;
-    const int r = ln >> 1, c0 = (ln & 1) * 8;
-    float x[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float a = A[fidx(bi + r, bj + k)];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = fmaf(a, T[fidx(bj + k, bj + c0 + e)], x[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) T[fidx(bi + r, bj + c0 + e)] = x[e];
+  if (wq < 2) {
+    const int bi = 16 * (2 * wq + 1), bj = 16 * (2 * wq);
+    float c[2][4] = {};
+    gemm16(A, bi, bj, T, bj, bj, c, ln);  // X = A_ij D_j
+    store16(T, bi, bj, c, 1.f, ln);
     __syncwarp();
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) y[e] = 0.f;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float d = T[fidx(bi + r, bi + k)];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = fmaf(d, T[fidx(bi + k, bj + c0 + e)], y[e]);
-    }
+    float y[2][4] = {};
+    gemm16(T, bi, bi, T, bi, bj, y, ln);  // D_i X
     __syncwarp();
-#pragma unroll
-    for (int e = 0; e < 8; ++e) T[fidx(bi + r, bj + c0 + e)] = -y[e];
+    store16(T, bi, bj, y, -1.f, ln);
   }
   named_bar_sync(1, 128);
-  // level 2: T_20 (warps 0, 1) and T_31 (warps 2, 3), 8 columns per warp
   {
-    const int bi = (wq < 2 ? 2 : 3) * 16, bj = (wq < 2 ? 0 : 1) * 16;
-    const int r = ln >> 1, c0 = (wq & 1) * 8 + (ln & 1) * 4;
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      const int bk = bj + kb * 16;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float a = A[fidx(bi + r, bk + k)];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = fmaf(a, T[fidx(bk + k, bj + c0 + e)], x[e]);
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) T[fidx(bi + r, bj + c0 + e)] = x[e];
-    __syncwarp();
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float d = T[fidx(bi + r, bi + k)];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) y[e] = fmaf(d, T[fidx(bi + k, bj + c0 + e)], y[e]);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int e = 0; e < 4; ++e) T[fidx(bi + r, bj + c0 + e)] = -y[e];
-  }
-  named_bar_sync(1, 128);
-  // level 3: T_30, 4 columns per warp
-  {
-    const int bi = 48;
-    const int r = ln >> 1, c0 = wq * 4 + (ln & 1) * 2;
-    float x[2] = {0.f, 0.f};
-#pragma unroll
-    for (int kb = 0; kb < 3; ++kb) {
-      const int bk = kb * 16;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float a = A[fidx(bi + r, bk + k)];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) x[e] = fmaf(a, T[fidx(bk + k, c0 + e)], x[e]);
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 2; ++e) T[fidx(bi + r, c0 + e)] = x[e];
-    __syncwarp();
-    float y[2] = {0.f, 0.f};
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float d = T[fidx(bi + r, bi + k)];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) y[e] = fmaf(d, T[fidx(bi + k, c0 + e)], y[e]);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int e = 0; e < 2; ++e) T[fidx(bi + r, c0 + e)] = -y[e];
+    const int rb = 2 + (wq >> 1), cb = wq & 1;
+    float c[2][4] = {};
+    for (int kb = cb; kb < 2; ++kb) gemm16(A, 16 * rb, 16 * kb, T, 16 * kb, 16 * cb, c, ln);
+    store16(T, 16 * rb, 16 * cb, c, 1.f, ln);  // X_{rb,cb} = sum_kb A_{rb,kb} T_{kb,cb}
+    named_bar_sync(1, 128);
+    float y[2][4] = {};
+    for (int kb = 2; kb <= rb; ++kb) gemm16(T, 16 * rb, 16 * kb, T, 16 * kb, 16 * cb, y, ln);
+    named_bar_sync(1, 128);
+    store16(T, 16 * rb, 16 * cb, y, -1.f, ln);
   }
   named_bar_sync(1, 128);
 }
@@ -236,7 +255,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
   uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(sm + L::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
-  ChunkScalars* scal = reinterpret_cast<ChunkScalars*>(sm + L::SC0);
+  ChunkScalars* cscal = reinterpret_cast<ChunkScalars*>(sm + L::CS0);
+  PrepScalars* ps = reinterpret_cast<PrepScalars*>(sm + L::PS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int unit = blockIdx.x;
@@ -253,11 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // ---- setup
   if (tid == 0) {
-    for (int b = 0; b < kNumBars; ++b) {
-      uint32_t cnt = 1;
-      if (b == B_FULL0 || b == B_FULL1) cnt = 32;
-      mbar_init(&bars[b], cnt);
-    }
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], (b == B_READY0 || b == B_READY1) ? 32u : 1u);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -282,39 +298,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       report(p.status, GDN_ERR_DEVICE_TIMEOUT, (uint32_t)(unit * 16 + where));
     }
   };
-
   auto stage_kq = [&](int s) { return sbase + L::STAGE0 + (uint32_t)s * L::STAGE_BYTES; };
   auto stage_v = [&](int s) { return stage_kq(s) + L::KQ_BYTES; };
-  auto stage_gates = [&](int s) {
+  auto stage_scal = [&](int s) {
     return reinterpret_cast<float*>(sm + L::STAGE0 + (uint32_t)s * L::STAGE_BYTES + L::KQ_BYTES +
                                     L::V_BYTES);
+  };
+  auto chunk_rows = [&](int c) {
+    const int64_t t0 = bos + (int64_t)c * kChunk;
+    return (int)((eos - t0) < kChunk ? (eos - t0) : kChunk);
   };
 
   if (warp == 0) {
     // ================================================================ producer
+    // TMA tiles for chunk c+1 are requested before chunk c is finished here;
+    // then chunk c's tail rows are cleared, its gates scanned and its q norms
+    // taken, and the stage is published to WG-A and the MMA issuer.
     const uint32_t tx_bytes = (uint32_t)(2 * L::NKA + L::NVA) * 8192u;
-    int issued[2] = {-1, -1};  // last chunk whose tiles were requested into each stage
-    for (int c = 0; c < nchunks; ++c) {
+    int issued[2] = {-1, -1};
+    auto issue = [&](int c) {
       const int s = c & 1;
-      if (c >= 2 && !mbar_wait(&bars[B_EMPTY0 + s], ((c >> 1) + 1) & 1, abort_flag, kWaitLimitNs)) {
-        fail(0);
-        break;
+      const int t0 = (int)(bos + (int64_t)c * kChunk);
+      uint8_t* kq = sm + L::STAGE0 + s * L::STAGE_BYTES;
+      mbar_arrive_expect_tx(&bars[B_TMA0 + s], tx_bytes);
+      for (int a = 0; a < L::NKA; ++a) {
+        tma_load_3d(kq + a * 16384, &tm.k, &bars[B_TMA0 + s], 64 * a, hq, t0);
+        tma_load_3d(kq + a * 16384 + 8192, &tm.q, &bars[B_TMA0 + s], 64 * a, hq, t0);
       }
+      for (int a = 0; a < L::NVA; ++a)
+        tma_load_3d(kq + L::KQ_BYTES + a * 8192, &tm.v, &bars[B_TMA0 + s], 64 * a, h, t0);
+    };
+    auto load_gates = [&](int c, float& g0, float& g1, float& b0, float& b1) {
       const int64_t t0 = bos + (int64_t)c * kChunk;
-      const int m = (int)((eos - t0) < kChunk ? (eos - t0) : kChunk);
-      if (lane == 0) {
-        mbar_expect_tx(&bars[B_FULL0 + s], tx_bytes);
-        uint8_t* kq = sm + L::STAGE0 + s * L::STAGE_BYTES;
-        for (int a = 0; a < L::NKA; ++a) {
-          tma_load_3d(kq + a * 16384, &tm.k, &bars[B_FULL0 + s], 64 * a, hq, (int)t0);
-          tma_load_3d(kq + a * 16384 + 8192, &tm.q, &bars[B_FULL0 + s], 64 * a, hq, (int)t0);
-        }
-        for (int a = 0; a < L::NVA; ++a)
-          tma_load_3d(kq + L::KQ_BYTES + a * 8192, &tm.v, &bars[B_FULL0 + s], 64 * a, h, (int)t0);
-      }
-      issued[s] = c;
-      // gates: rows lane and lane + 32, masked past the sequence end
-      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+      const int m = chunk_rows(c);
+      g0 = g1 = b0 = b1 = 0.f;
       if (lane < m) {
         g0 = load_gate(p.g, (t0 + lane) * p.h_v + h, p.gate_f32);
         b0 = load_gate(p.beta, (t0 + lane) * p.h_v + h, p.gate_f32);
@@ -323,6 +340,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         g1 = load_gate(p.g, (t0 + lane + 32) * p.h_v + h, p.gate_f32);
         b1 = load_gate(p.beta, (t0 + lane + 32) * p.h_v + h, p.gate_f32);
       }
+    };
+    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+    if (nchunks > 0) {
+      if (lane == 0) issue(0);
+      issued[0] = 0;
+      load_gates(0, g0, g1, b0, b1);
+    }
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c & 1;
+      if (!mbar_wait(&bars[B_TMA0 + s], (c >> 1) & 1, abort_flag, kWaitLimitNs)) {
+        fail(1);
+        break;
+      }
+      const int m = chunk_rows(c);
+      const uint32_t kq = stage_kq(s), vv = stage_v(s);
+      if (m < kChunk) {  // rows of the next sequence (or TMA zero fill): clear them
+        const int rows = kChunk - m, nreg = 2 * L::NKA + L::NVA;
+        for (int idx = lane; idx < rows * 8 * nreg; idx += 32) {
+          const int reg = idx / (rows * 8), rem = idx % (rows * 8);
+          const int r = m + (rem >> 3), ch = rem & 7;
+          const uint32_t base = reg < 2 * L::NKA ? kq + (reg >> 1) * 16384u + (reg & 1) * 8192u
+                                                 : vv + (reg - 2 * L::NKA) * 8192u;
+          st_shared_v4(base + r * 128u + ch * 16u, 0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // gate cumsum over the chunk and its span
       float c0v = g0, c1v = g1;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -334,19 +379,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       c1v += __shfl_sync(0xffffffffu, c0v, 31);
-      float* gt = stage_gates(s);
-      gt[lane] = c0v;
-      gt[lane + 32] = c1v;
-      gt[64 + lane] = b0;
-      gt[64 + lane + 32] = b1;
-      mbar_arrive(&bars[B_FULL0 + s]);
+      float gmax = fmaxf(c0v, c1v), gmin = fminf(c0v, c1v);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+        gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
+      }
+      // q norms: rows lane and lane + 32
+      float rq0 = 1.f, rq1 = 1.f;
+      if (p.l2norm) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t rbase = kq + 8192u + (lane + 32 * hh) * 128u;
+          float ss = 0.f;
+#pragma unroll
+          for (int a = 0; a < L::NKA; ++a)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              uint32_t x[4];
+              ld_shared_v4(rbase + a * 16384u + ch * 16u, x[0], x[1], x[2], x[3]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float lo = bf16_lo_f(x[e]), hi = bf16_hi_f(x[e]);
+                ss = fmaf(lo, lo, ss);
+                ss = fmaf(hi, hi, ss);
+              }
+            }
+          const float r = 1.0f / sqrtf(ss + 1e-6f);
+          if (hh == 0)
+            rq0 = r;
+          else
+            rq1 = r;
+        }
+      }
+      float* sc = stage_scal(s);
+      sc[SC_G + lane] = c0v;
+      sc[SC_G + lane + 32] = c1v;
+      sc[SC_B + lane] = b0;
+      sc[SC_B + lane + 32] = b1;
+      sc[SC_RQ + lane] = rq0;
+      sc[SC_RQ + lane + 32] = rq1;
+      if (lane == 0) {
+        sc[SC_GMAX] = gmax;
+        sc[SC_GMIN] = gmin;
+      }
+      mbar_arrive(&bars[B_READY0 + s]);
+      // next chunk: gates into registers, then its tiles once the stage is free
+      if (c + 1 < nchunks) {
+        load_gates(c + 1, g0, g1, b0, b1);
+        const int s1 = (c + 1) & 1;
+        if (c + 1 >= 2 &&
+            !mbar_wait(&bars[B_EMPTY0 + s1], (((c + 1) >> 1) + 1) & 1, abort_flag, kWaitLimitNs)) {
+          fail(0);
+          break;
+        }
+        if (lane == 0) issue(c + 1);
+        issued[s1] = c + 1;
+      }
     }
     // on abort, let the loads already issued land before the CTA can exit
-    // (in the normal path their stages were consumed and these return at once)
-    if (*abort_flag) {
-      for (int s = 0; s < 2; ++s)
-        if (issued[s] >= 0) mbar_wait(&bars[B_FULL0 + s], (issued[s] >> 1) & 1, nullptr, 100000000ull);
-    }
+    // (in the normal path they were all consumed and these return at once)
+    for (int s = 0; s < 2; ++s)
+      if (issued[s] >= 0)
+        mbar_wait(&bars[B_TMA0 + s], (issued[s] >> 1) & 1, nullptr, 100000000ull);
   } else if (warp == 1) {
     // ================================================================ state-independent MMAs
     if (lane == 0) {
@@ -354,8 +449,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
       for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1;
-        if (!mbar_wait(&bars[B_KQ_READY], c & 1, abort_flag, kWaitLimitNs)) {
-          fail(1);
+        if (!mbar_wait(&bars[B_READY0 + s], (c >> 1) & 1, abort_flag, kWaitLimitNs) ||
+            (c >= 1 && !mbar_wait(&bars[B_KQ_FREE], (c - 1) & 1, abort_flag, kWaitLimitNs))) {
+          fail(2);
           break;
         }
         tc_fence_after();
@@ -371,7 +467,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         mma_commit(&bars[B_KQ_DONE]);
         if (!mbar_wait(&bars[B_P1_MID], c & 1, abort_flag, kWaitLimitNs)) {
-          fail(2);
+          fail(3);
           break;
         }
         tc_fence_after();
@@ -398,13 +494,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = c & 1, par = c & 1;
         if (!mbar_wait(&bars[B_P1_DONE0 + par], (c >> 1) & 1, abort_flag, kWaitLimitNs) ||
             !mbar_wait(&bars[B_S_READY], c & 1, abort_flag, kWaitLimitNs)) {
-          fail(3);
+          fail(4);
           break;
         }
         tc_fence_after();
         const uint32_t kq = stage_kq(s), vv = stage_v(s);
-        const uint32_t tb = sbase + L::TB0 + par * 16384u;
-        const uint32_t wt = sbase + L::WT0 + par * 16384u;
+        const uint32_t tb = sbase + L::TB0 + par * L::SCR_BYTES;
+        const uint32_t wt = sbase + L::WT0 + par * L::SCR_BYTES;
         const uint32_t sop = sbase + L::SOP;
         // U^T = V^T (T_b hi + lo)^T : A = V^T MN-major (d_v atoms 8 KB apart or the zero page)
         const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
@@ -421,16 +517,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_R, sdesc(sop + a * 16384u + k * 32u, 16, 1024),
                    sdesc(wt + (a * 4 + k) * 2048u, 16, 1024), id_sw, 1);
-        // O^T = (-S^T) (-Qh)^T : B = Qh in place of Q (K-major)
+        // QS^T = (-S^T) Q^T : B = the raw q tile (K-major)
 #pragma unroll
         for (int a = 0; a < L::NKA; ++a)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_O, sdesc(sop + a * 16384u + k * 32u, 16, 1024),
+            mma_ss(tmem + TM_QS, sdesc(sop + a * 16384u + k * 32u, 16, 1024),
                    sdesc(kq + a * 16384u + 8192u + k * 32u, 16, 1024), id_qs, (a | k) != 0);
         mma_commit(&bars[B_UP_DONE]);
         if (!mbar_wait(&bars[B_UOPS_READY], c & 1, abort_flag, kWaitLimitNs)) {
-          fail(4);
+          fail(5);
           break;
         }
         tc_fence_after();
@@ -446,7 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t pp = sbase + L::P0 + par * 8192u;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + TM_O, tmem + TM_UU + k * 8u, sdesc(pp + k * 32u, 16, 1024), id_pu, 1);
+          mma_ts(tmem + TM_O, tmem + TM_UU + k * 8u, sdesc(pp + k * 32u, 16, 1024), id_pu, k != 0);
         mma_commit(&bars[B_O_DONE]);
         mma_commit(&bars[B_EMPTY0 + s]);
       }
@@ -457,118 +553,104 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ================================================================ WG-A: chunk preparation
     const int wa = tid - 128;  // == TMEM lane
     const uint32_t lane_off = (uint32_t)((wa & ~31) << 16);
+    const bool krow = wa < 64;
+    const int i = wa & 63;
     for (int c = 0; c < nchunks; ++c) {
       const int s = c & 1, par = c & 1;
-      bool ok = mbar_wait(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+      bool ok = mbar_wait(&bars[B_READY0 + s], (c >> 1) & 1, abort_flag, kWaitLimitNs);
       if (ok && c >= 2)
         ok = mbar_wait(&bars[B_BUF_FREE0 + par], ((c >> 1) + 1) & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(5);
-      named_bar_sync(1, 128);
-      if (*abort_flag) break;
-      const int64_t t0 = bos + (int64_t)c * kChunk;
-      const int m = (int)((eos - t0) < kChunk ? (eos - t0) : kChunk);
-      const uint32_t kq = stage_kq(s), vv = stage_v(s);
-      const float* gt = stage_gates(s);
-      ChunkScalars& sc = scal[par];
-      // rows past the sequence end belong to another sequence (or are TMA zero
-      // fill): clear them so that only exact zeros enter the products
-      if (m < kChunk) {
-        const int rows = kChunk - m;
-        const int per_row = 8;  // 16-byte chunks in a 128-byte row
-        const int nreg = 2 * L::NKA + L::NVA;
-        for (int idx = wa; idx < rows * per_row * nreg; idx += 128) {
-          const int reg = idx / (rows * per_row), rem = idx % (rows * per_row);
-          const int r = m + rem / per_row, ch = rem % per_row;
-          uint32_t base;
-          if (reg < 2 * L::NKA)
-            base = kq + (reg >> 1) * 16384u + (reg & 1) * 8192u;
-          else
-            base = vv + (reg - 2 * L::NKA) * 8192u;
-          st_shared_v4(base + r * 128u + ch * 16u, 0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-      }
-      // L2-norm scales: thread wa < 64 -> k row wa, else q row wa - 64
-      {
-        const int row = wa & 63;
-        const uint32_t rbase = kq + (wa >= 64 ? 8192u : 0u) + row * 128u;
-        float ss = 0.f;
-#pragma unroll
-        for (int a = 0; a < L::NKA; ++a)
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t x0, x1, x2, x3;
-            ld_shared_v4(rbase + a * 16384u + ch * 16u, x0, x1, x2, x3);
-            const uint32_t xs[4] = {x0, x1, x2, x3};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = bf16_lo_f(xs[e]), hi = bf16_hi_f(xs[e]);
-              ss = fmaf(lo, lo, ss);
-              ss = fmaf(hi, hi, ss);
-            }
-          }
-        const float r = p.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-        if (wa < 64)
-          sc.rk[row] = r;
-        else
-          sc.rq[row] = r;
-      }
-      named_bar_sync(1, 128);
-      if (wa < 64) {
-        const int j = wa;
-        const float G = gt[j], GC = gt[63], bj = gt[64 + j];
-        const float eg = expf(G);
-        sc.G[j] = G;
-        sc.beta[j] = bj;
-        sc.eG[j] = eg;
-        sc.s[j] = expf(GC - G) * sc.rk[j];
-        sc.tw[j] = bj * eg * sc.rk[j];
-        if (j == 0) sc.eGC = expf(GC);
-      }
-      named_bar_sync(1, 128);
-      if (wa == 0) mbar_arrive(&bars[B_KQ_READY]);
-      // ---- A and P from [K;Q] K^T
-      ok = mbar_wait(&bars[B_KQ_DONE], c & 1, abort_flag, kWaitLimitNs);
       if (!ok) fail(6);
       named_bar_sync(1, 128);
       if (*abort_flag) break;
+      const uint32_t kq = stage_kq(s);
+      const float* sc = stage_scal(s);
+      ChunkScalars& cs = cscal[par];
+      const float gmax = sc[SC_GMAX];
+      const bool exact = (gmax - sc[SC_GMIN]) > kMaxDecaySpan;
+      const float Gi = sc[SC_G + i], Gl2i = Gi * kLog2e, GCl2 = sc[SC_G + 63] * kLog2e;
+      const float ai = exp2f((Gi - gmax) * kLog2e);
+      ok = mbar_wait(&bars[B_KQ_DONE], c & 1, abort_flag, kWaitLimitNs);
+      if (!ok) fail(7);
+      named_bar_sync(1, 128);
+      if (*abort_flag) break;
       tc_fence_after();
-      float* Abuf = reinterpret_cast<float*>(sm + L::WT0 + par * 16384u);
-      float* Tbuf = reinterpret_cast<float*>(sm + L::TB0 + par * 16384u);
-      {
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tmem + lane_off + TM_KQ, v0);
-        tmem_ld32(tmem + lane_off + TM_KQ + 32, v1);
-        tmem_ld_wait();
-        if (wa < 64) {
-          const int i = wa;
-          const float ci = sc.beta[i] * sc.rk[i], Gi = sc.G[i];
+      uint32_t v0[32], v1[32];
+      tmem_ld32(tmem + lane_off + TM_KQ, v0);
+      tmem_ld32(tmem + lane_off + TM_KQ + 32, v1);
+      tmem_ld_wait();
+      float* Abuf = reinterpret_cast<float*>(sm + L::WT0 + par * L::SCR_BYTES);
+      float* Tbuf = reinterpret_cast<float*>(sm + L::TB0 + par * L::SCR_BYTES);
+      float ri = 1.f;
+      if (krow) {
+        // r^k_i from the diagonal of K K^T (fp32 sum of exact bf16 products)
+        float diag = 0.f;
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
+        for (int j = 0; j < 64; ++j)
+          if (j == i) diag = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
+        ri = p.l2norm ? 1.0f / sqrtf(diag + 1e-6f) : 1.f;
+        const float bi = sc[SC_B + i];
+        ps->d[i] = ri * exp2f((gmax - Gi) * kLog2e);
+        ps->r[i] = ri;
+        ps->beta[i] = bi;
+        ps->tw[i] = bi * exp2f(Gl2i) * ri;
+        cs.s[i] = exp2f(GCl2 - Gl2i) * ri;
+      } else {
+        const float co = p.scale * sc[SC_RQ + i];
+        cs.co[i] = co;
+        cs.cq[i] = -co * exp2f(Gl2i);
+        if (i == 0) cs.eGC = exp2f(GCl2);
+      }
+      named_bar_sync(1, 128);
+      if (krow) {
+        // A_ij = beta_i r_i r_j e^{G_i - G_j} k_i.k_j  (j < i), fp32 into the scratch
+        const float ci = ps->beta[i] * ri;
+        const float cia = ci * ai;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          float a4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = q * 4 + e;
             const float kk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
-            Abuf[fidx(i, j)] = (j < i) ? ci * sc.rk[j] * expf(Gi - sc.G[j]) * kk : 0.f;
+            a4[e] = (cia * kk) * ps->d[j];
           }
-        } else {
-          const int i = wa - 64;
-          const float Gi = sc.G[i];
-          const uint32_t prow = sbase + L::P0 + par * 8192u;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t w4[4];
+          if (exact) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              float pv[2];
-#pragma unroll
-              for (int q = 0; q < 2; ++q) {
-                const int j = ch * 8 + e * 2 + q;
-                const float qk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
-                pv[q] = (j <= i) ? expf(Gi - sc.G[j]) * sc.rk[j] * qk : 0.f;
-              }
-              w4[e] = pack_bf16(pv[0], pv[1]);
+              const int j = q * 4 + e;
+              const float kk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
+              a4[e] = ci * ps->r[j] * exp2f(Gl2i - sc[SC_G + j] * kLog2e) * kk;
             }
-            st_shared_v4(prow + sw128(i, ch), w4[0], w4[1], w4[2], w4[3]);
           }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a4[e] = (q * 4 + e < i) ? a4[e] : 0.f;
+          *reinterpret_cast<float4*>(&Abuf[i * LDF + q * 4]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        }
+      } else {
+        // P_ij = e^{G_i - G_j} r^k_j q_i.k_j  (j <= i), bf16 K-major [i][j]
+        const uint32_t prow = sbase + L::P0 + par * 8192u;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          float pv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = ch * 8 + e;
+            const float qk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
+            pv[e] = (ai * qk) * ps->d[j];
+          }
+          if (exact) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int j = ch * 8 + e;
+              const float qk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
+              pv[e] = ps->r[j] * exp2f(Gl2i - sc[SC_G + j] * kLog2e) * qk;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pv[e] = (ch * 8 + e <= i) ? pv[e] : 0.f;
+          st_shared_v4(prow + sw128(i, ch), pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
+                       pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
         }
       }
       fence_proxy_async_smem();
@@ -578,45 +660,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       solve_unit_lower(Abuf, Tbuf, wa);
       // ---- T_b = T diag(beta) as bf16 hi + lo; T_w = T diag(beta e^G r^k)
       {
-        const int i = wa >> 1, hh = wa & 1;
+        const int ti = wa & 63, hh = wa >> 6;
         float t[32];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = hh * 32 + jj;
-          t[jj] = ((j >> 4) > (i >> 4)) ? 0.f : Tbuf[fidx(i, j)];
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = *reinterpret_cast<const float4*>(&Tbuf[ti * LDF + hh * 32 + q * 4]);
+          const bool zero = ((hh * 32 + q * 4) >> 4) > (ti >> 4);  // block above the diagonal
+          t[q * 4 + 0] = zero ? 0.f : x.x;
+          t[q * 4 + 1] = zero ? 0.f : x.y;
+          t[q * 4 + 2] = zero ? 0.f : x.z;
+          t[q * 4 + 3] = zero ? 0.f : x.w;
         }
         named_bar_sync(1, 128);  // every thread has read T before it is overwritten
-        const uint32_t tb = sbase + L::TB0 + par * 16384u;
+        const uint32_t tb = sbase + L::TB0 + par * L::SCR_BYTES;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t hi4[4], lo4[4], w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j0 = hh * 32 + q * 8 + e * 2;
-            const float x0 = t[q * 8 + e * 2] * sc.beta[j0];
-            const float x1 = t[q * 8 + e * 2 + 1] * sc.beta[j0 + 1];
+            const float x0 = t[q * 8 + e * 2] * ps->beta[j0];
+            const float x1 = t[q * 8 + e * 2 + 1] * ps->beta[j0 + 1];
             hi4[e] = pack_bf16(x0, x1);
             lo4[e] = pack_bf16(x0 - bf16_lo_f(hi4[e]), x1 - bf16_hi_f(hi4[e]));
-            w4[e] = pack_bf16(t[q * 8 + e * 2] * sc.tw[j0], t[q * 8 + e * 2 + 1] * sc.tw[j0 + 1]);
+            w4[e] = pack_bf16(t[q * 8 + e * 2] * ps->tw[j0], t[q * 8 + e * 2 + 1] * ps->tw[j0 + 1]);
           }
-          const uint32_t off = sw128(i, hh * 4 + q);
+          const uint32_t off = sw128(ti, hh * 4 + q);
           st_shared_v4(tb + off, hi4[0], hi4[1], hi4[2], hi4[3]);
           st_shared_v4(tb + 8192u + off, lo4[0], lo4[1], lo4[2], lo4[3]);
           st_shared_v4(sbase + L::TW + off, w4[0], w4[1], w4[2], w4[3]);
-        }
-      }
-      // ---- Qh = -e^{G_i} q_i, in place over the q tile (row-wise scale ignores the swizzle)
-      {
-        const int row = wa >> 1;
-        const float f = -sc.eG[row];
-        for (int idx = (wa & 1); idx < 8 * L::NKA; idx += 2) {
-          const int a = idx >> 3, ch = idx & 7;
-          const uint32_t addr = kq + a * 16384u + 8192u + row * 128u + ch * 16u;
-          uint32_t x[4];
-          ld_shared_v4(addr, x[0], x[1], x[2], x[3]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] = pack_bf16(bf16_lo_f(x[e]) * f, bf16_hi_f(x[e]) * f);
-          st_shared_v4(addr, x[0], x[1], x[2], x[3]);
         }
       }
       fence_proxy_async_smem();
@@ -624,25 +696,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (wa == 0) mbar_arrive(&bars[B_P1_MID]);
       // ---- W^T: TMEM -> bf16 MN-major [d_k][j]
       ok = mbar_wait(&bars[B_W_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(7);
+      if (!ok) fail(8);
       named_bar_sync(1, 128);
       if (*abort_flag) break;
       tc_fence_after();
       {
-        uint32_t v0[32], v1[32];
         tmem_ld32(tmem + lane_off + TM_KQ, v0);
         tmem_ld32(tmem + lane_off + TM_KQ + 32, v1);
         tmem_ld_wait();
-        const uint32_t wt = sbase + L::WT0 + par * 16384u;
+        const uint32_t wt = sbase + L::WT0 + par * L::SCR_BYTES;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           uint32_t w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = ch * 8 + e * 2;
-            const float a0 = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
-            const float a1 = __uint_as_float(j + 1 < 32 ? v0[j + 1] : v1[j + 1 - 32]);
-            w4[e] = pack_bf16(a0, a1);
+            w4[e] = pack_bf16(__uint_as_float(j < 32 ? v0[j] : v1[j - 32]),
+                              __uint_as_float(j + 1 < 32 ? v0[j + 1] : v1[j + 1 - 32]));
           }
           st_shared_v4(wt + sw128(wa, ch), w4[0], w4[1], w4[2], w4[3]);
         }
@@ -650,7 +720,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(1, 128);
-      if (wa == 0) mbar_arrive(&bars[B_P1_DONE0 + par]);
+      if (wa == 0) {
+        mbar_arrive(&bars[B_P1_DONE0 + par]);
+        mbar_arrive(&bars[B_KQ_FREE]);
+      }
     }
   } else if (warp >= 8) {
     // ================================================================ WG-B: state step + epilogue
@@ -661,7 +734,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     {
       const int64_t slot = state_slot(p, n);
       const float* s0 = slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + h) * DK * DV : nullptr;
-#pragma unroll
+#pragma unroll 1
       for (int xb = 0; xb < DK / 32; ++xb) {
         uint32_t v[32];
 #pragma unroll
@@ -675,29 +748,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int par = c & 1;
       // ---- S -> -S^T (bf16 operand); S *= e^{G_m}
       bool ok = mbar_wait(&bars[B_P1_DONE0 + par], (c >> 1) & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(8);
+      if (!ok) fail(9);
       named_bar_sync(2, 128);
       if (*abort_flag) break;
       tc_fence_after();
-      const ChunkScalars& sc = scal[par];
-      const float eGC = sc.eGC;
-#pragma unroll
-      for (int xb = 0; xb < DK / 32; ++xb) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + TM_S + xb * 32, v);
+      const ChunkScalars& cs = cscal[par];
+      const float eGC = cs.eGC;
+#pragma unroll 1
+      for (int xp = 0; xp < DK / 64; ++xp) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(tmem + lane_off + TM_S + xp * 64, va);
+        tmem_ld32(tmem + lane_off + TM_S + xp * 64 + 32, vb);
         tmem_ld_wait();
-        const uint32_t row = sbase + L::SOP + (xb >> 1) * 16384u;
+        const uint32_t row = sbase + L::SOP + xp * 16384u;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
           uint32_t w4[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w4[e] = pack_bf16(-__uint_as_float(v[q * 8 + e * 2]), -__uint_as_float(v[q * 8 + e * 2 + 1]));
-          st_shared_v4(row + sw128(wb, (xb & 1) * 4 + q), w4[0], w4[1], w4[2], w4[3]);
+          for (int e = 0; e < 4; ++e) {
+            const int x = q * 8 + e * 2;
+            w4[e] = pack_bf16(-__uint_as_float(x < 32 ? va[x] : vb[x - 32]),
+                              -__uint_as_float(x + 1 < 32 ? va[x + 1] : vb[x + 1 - 32]));
+          }
+          st_shared_v4(row + sw128(wb, q), w4[0], w4[1], w4[2], w4[3]);
         }
 #pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * eGC);
-        tmem_st32(tmem + lane_off + TM_S + xb * 32, v);
+        for (int x = 0; x < 32; ++x) {
+          va[x] = __float_as_uint(__uint_as_float(va[x]) * eGC);
+          vb[x] = __float_as_uint(__uint_as_float(vb[x]) * eGC);
+        }
+        tmem_st32(tmem + lane_off + TM_S + xp * 64, va);
+        tmem_st32(tmem + lane_off + TM_S + xp * 64 + 32, vb);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -706,7 +787,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (wb == 0) mbar_arrive(&bars[B_S_READY]);
       // ---- U' -> (U' s) hi / lo and U' as bf16, into TMEM A operands
       ok = mbar_wait(&bars[B_UP_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(9);
+      if (!ok) fail(10);
       named_bar_sync(2, 128);
       if (*abort_flag) break;
       tc_fence_after();
@@ -726,7 +807,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (pass == 2) {
               w[cc] = pack_bf16(a0, a1);
             } else {
-              const float x0 = a0 * sc.s[j], x1 = a1 * sc.s[j + 1];
+              const float x0 = a0 * cs.s[j], x1 = a1 * cs.s[j + 1];
               const uint32_t hi = pack_bf16(x0, x1);
               w[cc] = pass == 0 ? hi : pack_bf16(x0 - bf16_lo_f(hi), x1 - bf16_hi_f(hi));
             }
@@ -738,29 +819,70 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       named_bar_sync(2, 128);
       if (wb == 0) mbar_arrive(&bars[B_UOPS_READY]);
-      // ---- epilogue: o_i = scale r^q_i O^T[:, i]
+      // ---- epilogue: o_i = scale r^q_i O^T[:, i], staged through shared memory
       ok = mbar_wait(&bars[B_O_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(10);
+      if (!ok) fail(11);
       named_bar_sync(2, 128);
       if (*abort_flag) break;
       tc_fence_after();
       {
         const int64_t t0 = bos + (int64_t)c * kChunk;
-        const int m = (int)((eos - t0) < kChunk ? (eos - t0) : kChunk);
-        uint32_t o0[32], o1[32];
-        tmem_ld32(tmem + lane_off + TM_O, o0);
-        tmem_ld32(tmem + lane_off + TM_O + 32, o1);
-        tmem_ld_wait();
-        if (live) {
+        const int m = chunk_rows(c);
+        uint8_t* stg = sm + L::SOP;
+#pragma unroll 1
+        for (int hb = 0; hb < 2; ++hb) {  // token halves [32 hb, 32 hb + 32)
+          uint32_t oq[32], oi[32];
+          tmem_ld32(tmem + lane_off + TM_QS + hb * 32, oq);
+          tmem_ld32(tmem + lane_off + TM_O + hb * 32, oi);
+          tmem_ld_wait();
+          if (p.out_f32) {
+            float* st = reinterpret_cast<float*>(stg);
+            if (live) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            if (i < m) {
-              const float o = p.scale * sc.rq[i] * __uint_as_float(i < 32 ? o0[i] : o1[i - 32]);
-              const size_t idx = ((size_t)(t0 + i) * p.h_v + h) * DV + wb;
-              if (p.out_f32)
-                reinterpret_cast<float*>(p.out)[idx] = o;
-              else
-                reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(o);
+              for (int ii = 0; ii < 32; ++ii) {
+                const int i2 = hb * 32 + ii;
+                st[i2 * DV + wb] = fmaf(cs.cq[i2], __uint_as_float(oq[ii]), cs.co[i2] * __uint_as_float(oi[ii]));
+              }
+            }
+          } else {
+            // lanes 2k and 2k+1 swap values so each writes a bf16 pair (d_v 2k, 2k+1)
+            // of one token; odd rows flip word bit 4 against bank conflicts
+            uint32_t* st = reinterpret_cast<uint32_t*>(stg);
+            const bool odd = wb & 1;
+#pragma unroll
+            for (int tp = 0; tp < 16; ++tp) {
+              const int i0 = hb * 32 + 2 * tp, i1 = i0 + 1;
+              const float x0 = fmaf(cs.cq[i0], __uint_as_float(oq[2 * tp]), cs.co[i0] * __uint_as_float(oi[2 * tp]));
+              const float x1 = fmaf(cs.cq[i1], __uint_as_float(oq[2 * tp + 1]), cs.co[i1] * __uint_as_float(oi[2 * tp + 1]));
+              const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+              const int row = odd ? i1 : i0;
+              const uint32_t word = odd ? pack_bf16(got, x1) : pack_bf16(x0, got);
+              if (live) st[row * (DV / 2) + ((wb >> 1) ^ ((row & 1) << 4))] = word;
+            }
+          }
+        }
+        named_bar_sync(2, 128);
+        // coalesced copy-out of rows < m, 16 bytes at a time
+        if (p.out_f32) {
+          constexpr int cpr = DV * 4 / 16;
+          for (int q = wb; q < 64 * cpr; q += 128) {
+            const int row = q / cpr, ch = q % cpr;
+            if (row < m) {
+              uint32_t x[4];
+              ld_shared_v4(sbase + L::SOP + row * (DV * 4) + ch * 16, x[0], x[1], x[2], x[3]);
+              float* dst = reinterpret_cast<float*>(p.out) + ((size_t)(t0 + row) * p.h_v + h) * DV + ch * 4;
+              *reinterpret_cast<uint4*>(dst) = make_uint4(x[0], x[1], x[2], x[3]);
+            }
+          }
+        } else {
+          constexpr int cpr = DV * 2 / 16;
+          for (int q = wb; q < 64 * cpr; q += 128) {
+            const int row = q / cpr, ch = q % cpr;
+            if (row < m) {
+              uint32_t x[4];
+              ld_shared_v4(sbase + L::SOP + row * (DV * 2) + ((ch ^ ((row & 1) << 2)) * 16), x[0], x[1], x[2], x[3]);
+              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)(t0 + row) * p.h_v + h) * DV + ch * 8;
+              *reinterpret_cast<uint4*>(dst) = make_uint4(x[0], x[1], x[2], x[3]);
             }
           }
         }
@@ -773,7 +895,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!*abort_flag && p.final_state) {
       tc_fence_after();
       float* fs = p.final_state + ((size_t)n * p.h_v + h) * DK * DV;
-#pragma unroll
+#pragma unroll 1
       for (int xb = 0; xb < DK / 32; ++xb) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + TM_S + xb * 32, v);
