@@ -24,17 +24,14 @@
 //                                    read by the MMA straight from TMEM)
 // Operand precision: the products feeding the fp32 state carry T and U' as
 // bf16 hi + lo pairs (about 16 significant bits); S and W enter as bf16; every
-// accumulation is fp32 in TMEM. Decays and norms run on CUDA cores in fp32.
-// The 64x64 unit-lower-triangular inverse inverts its 16x16 diagonal blocks
-// by fp32 substitution and merges them with small tf32 mma.sync products in a
-// three-pass hi/lo split (fp32-level accuracy); the open-jev-fast README's GDN
-// kernel also builds its inverse with tf32 MMAs in blocks (Phase 3 item 1).
+// accumulation is fp32 in TMEM. Decays, norms and the 64x64 unit-lower-
+// triangular inverse (16x16 blocks merged level by level, the blocked order
+// the open-jev-fast README's GDN kernel also uses) run on CUDA cores in fp32.
 //
-// Warp roles (384 threads): warp 0 loads K/Q/V tiles by TMA (128-byte swizzle),
-// clears rows past the sequence end, scans the gates and takes the q norms
-// (r^k comes from the diagonal of K K^T); warp 1 allocates TMEM and issues the state-independent MMAs;
-// warp 2 issues the state-dependent MMAs; warps 4-7 (WG-A) prepare chunk c+1
-// (A and P, the solve, T_b / T_w, W^T) while warps 8-11 (WG-B) run
+// Warp roles (512 threads): warp 0 loads K/Q/V tiles by TMA (128-byte swizzle),
+// clears rows past the sequence end and scans the gates; warp 1 allocates TMEM and issues the state-independent MMAs;
+// warp 2 issues the state-dependent MMAs; warps 4-11 (WG-A) prepare chunk c+1
+// (norms, A and P, the solve, T_b / T_w, W^T) while warps 12-15 (WG-B) run
 // chunk c's state step (S -> bf16 operand, U' split, output epilogue). Every
 // mbarrier wait is bounded: on timeout the CTA reports GDN_ERR_DEVICE_TIMEOUT
 // and unwinds.
@@ -49,7 +46,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kTcThreads = 384;
+constexpr int kTcThreads = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait: far above any legal wait
 
 // TMEM columns (fp32 unless noted)
@@ -69,11 +66,11 @@ constexpr float kMaxDecaySpan = 80.0f;  // chunks whose log-decay spans more use
 // Barrier indices
 enum {
   B_TMA0 = 0, B_TMA1, B_READY0, B_READY1, B_EMPTY0, B_EMPTY1, B_KQ_DONE, B_P1_MID, B_W_DONE,
-  B_KQ_FREE, B_P1_DONE0, B_P1_DONE1, B_BUF_FREE0, B_BUF_FREE1, B_S_READY, B_UP_DONE,
-  B_UOPS_READY, B_O_DONE, B_DRAIN1, B_DRAIN2, kNumBars
+  B_KQ_FREE, B_P1_DONE0, B_P1_DONE1, B_CS_FREE0, B_CS_FREE1, B_CS_FREE2, B_S_READY, B_UP_DONE,
+  B_UOPS_READY, B_O_DONE, B_STATE_DONE, B_EPI_DONE, B_DRAIN1, B_DRAIN2, kNumBars
 };
 
-// Per-chunk values WG-A hands to WG-B (double-buffered by chunk parity).
+// Per-chunk values WG-A hands to WG-B (three buffers, indexed by chunk % 3).
 struct ChunkScalars {
   float cq[64];  // -scale r^q_i e^{G_i}: weight of the (-S^T q_i) column
   float co[64];  // scale r^q_i: weight of the intra-chunk column
@@ -88,8 +85,9 @@ struct PrepScalars {
   float tw[64];    // beta_j e^{G_j} r^k_j: column scale of T_w
   float beta[64];
 };
-// Stage scalars written by the producer: G[64], beta[64], rq[64], Gmax, Gmin.
-constexpr int SC_G = 0, SC_B = 64, SC_RQ = 128, SC_GMAX = 192, SC_GMIN = 193;
+// Stage scalars: G[64], beta[64], Gmax, Gmin written by the producer; WG-A
+// parks half-row partial sums of |q_i|^2 in [SC_QSS, SC_QSS + 64).
+constexpr int SC_G = 0, SC_B = 64, SC_QSS = 128, SC_GMAX = 192, SC_GMIN = 193;
 
 constexpr int LDF = 68;  // row stride (floats) of the fp32 64x64 scratch of the solve
 
@@ -114,7 +112,7 @@ struct TcLayout {
   static constexpr bool NEED_ZERO = (DK == 64) || (DV == 64);
   static constexpr uint32_t ZERO = SOP + SOP_BYTES;       // 8 KB of zeros (M padding)
   static constexpr uint32_t CS0 = ZERO + (NEED_ZERO ? 8192u : 0u);
-  static constexpr uint32_t PS = CS0 + 2 * (uint32_t)sizeof(ChunkScalars);
+  static constexpr uint32_t PS = CS0 + 3 * (uint32_t)sizeof(ChunkScalars);
   static constexpr uint32_t BARS = PS + (uint32_t)sizeof(PrepScalars);
   static constexpr uint32_t MISC = BARS + kNumBars * 8u;  // tmem base, abort flag
   static constexpr uint32_t TOTAL = MISC + 64u;
@@ -128,119 +126,96 @@ struct Tmaps {
 };
 
 // ---------------------------------------------------------------- the solve
-// mma.sync m16n8k8 (tf32) with a three-pass hi/lo split, which carries the
-// products at about fp32 accuracy. Fragments follow the PTX m16n8k8 layouts:
-// a0..a3 = (g, t), (g+8, t), (g, t+4), (g+8, t+4); b0, b1 = (t, g), (t+4, g);
-// c0..c3 = (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1), g = lane/4, t = lane%4.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// C[16x16] += X[16x16 block at (xr, xc)] * Y[16x16 block at (yr, yc)], fp32 smem, stride LDF.
-__device__ __forceinline__ void gemm16(const float* X, int xr, int xc, const float* Y, int yr, int yc,
-                                       float (&c)[2][4], int lane) {
+// C[16 x 8] (+)= X[16 x K block at (xr, xc)] * Y[K x 8 block at (yr, yc)] in
+// fp32 FMA, fp32 smem with row stride LDF. Lane (g, t) = (lane / 4, lane % 4)
+// owns rows g, g + 8 and columns 2t, 2t + 1; all operand loads are issued up
+// front so the four accumulation chains run back to back.
+template <int K>
+__device__ __forceinline__ void fma_tile(const float* X, int xr, int xc, const float* Y, int yr, int yc,
+                                         float (&c)[4], int lane) {
   const int g = lane >> 2, t = lane & 3;
+  float xa[K], xb[K];
+  float2 yv[K];
 #pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    const int k0 = ks * 8;
-    const float af[4] = {X[(xr + g) * LDF + xc + k0 + t], X[(xr + g + 8) * LDF + xc + k0 + t],
-                         X[(xr + g) * LDF + xc + k0 + t + 4],
-                         X[(xr + g + 8) * LDF + xc + k0 + t + 4]};
-    uint32_t ah[4], al[4];
+  for (int k = 0; k < K; ++k) {
+    xa[k] = X[(xr + g) * LDF + xc + k];
+    xb[k] = X[(xr + g + 8) * LDF + xc + k];
+    yv[k] = *reinterpret_cast<const float2*>(&Y[(yr + k) * LDF + yc + 2 * t]);
+  }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      ah[e] = to_tf32(af[e]);
-      al[e] = to_tf32(af[e] - __uint_as_float(ah[e]));
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const float b0 = Y[(yr + k0 + t) * LDF + yc + nt * 8 + g];
-      const float b1 = Y[(yr + k0 + t + 4) * LDF + yc + nt * 8 + g];
-      const uint32_t bh0 = to_tf32(b0), bh1 = to_tf32(b1);
-      const uint32_t bl0 = to_tf32(b0 - __uint_as_float(bh0)),
-                     bl1 = to_tf32(b1 - __uint_as_float(bh1));
-      mma_tf32(c[nt], al, bh0, bh1);
-      mma_tf32(c[nt], ah, bl0, bl1);
-      mma_tf32(c[nt], ah, bh0, bh1);
-    }
+  for (int k = 0; k < K; ++k) {
+    c[0] = fmaf(xa[k], yv[k].x, c[0]);
+    c[1] = fmaf(xa[k], yv[k].y, c[1]);
+    c[2] = fmaf(xb[k], yv[k].x, c[2]);
+    c[3] = fmaf(xb[k], yv[k].y, c[3]);
   }
 }
-__device__ __forceinline__ void store16(float* M, int r0, int c0, const float (&c)[2][4], float sgn,
-                                        int lane) {
+__device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float (&c)[4], float sgn,
+                                           int lane) {
   const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    M[(r0 + g) * LDF + c0 + nt * 8 + 2 * t] = sgn * c[nt][0];
-    M[(r0 + g) * LDF + c0 + nt * 8 + 2 * t + 1] = sgn * c[nt][1];
-    M[(r0 + g + 8) * LDF + c0 + nt * 8 + 2 * t] = sgn * c[nt][2];
-    M[(r0 + g + 8) * LDF + c0 + nt * 8 + 2 * t + 1] = sgn * c[nt][3];
-  }
+  *reinterpret_cast<float2*>(&M[(r0 + g) * LDF + c0 + 2 * t]) = make_float2(sgn * c[0], sgn * c[1]);
+  *reinterpret_cast<float2*>(&M[(r0 + g + 8) * LDF + c0 + 2 * t]) = make_float2(sgn * c[2], sgn * c[3]);
 }
 
 // T = (I + A)^-1 for the strictly-lower 64x64 A (fp32, stride LDF), by 16x16
-// blocks: the four diagonal blocks D_b by forward substitution in fp32, the
-// two 16-row merges T_{b+1,b} = -D_{b+1} A_{b+1,b} D_b inside each 32x32
-// diagonal block, then T_21 = -T_22 (A_21 T_11) for the lower-left 32x32
-// block. Blocks above the diagonal are not written. 128 threads (4 warps).
+// blocks: the four diagonal blocks D_b by right-looking elimination (once
+// t_x is final, every later row of the column is updated at once), the two
+// 16-row merges T_{b+1,b} = -D_{b+1} A_{b+1,b} D_b inside each 32x32 diagonal
+// block, then T_21 = -T_22 (A_21 T_11) for the lower-left 32x32 block. All in
+// fp32. Blocks above the diagonal are not written. 256 threads (8 warps);
+// every merge product is split into 8-column halves.
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ T,
                                                  int wa) {
   const int wq = wa >> 5, ln = wa & 31;
-  {
-    // lanes l and l + 16 both own column l and split each row's sum by parity
-    const int b = wq * 16, l = ln & 15, hp = ln >> 4;
+  if (wq < 4 && ln < 16) {
+    const int b = wq * 16, l = ln;  // lane l owns column l of D_wq
     float t[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) t[i] = (i == l) ? 1.f : 0.f;
 #pragma unroll
-    for (int i = 1; i < 16; ++i) {
-      float sacc = 0.f;
+    for (int x = 0; x < 15; ++x) {
+      const float tx = t[x];
 #pragma unroll
-      for (int x = 0; x < i; x += 2) {
-        const float tx = hp == 0 ? t[x] : ((x + 1 < i) ? t[x + 1] : 0.f);
-        sacc = fmaf(A[(b + i) * LDF + b + x + hp], tx, sacc);
-      }
-      sacc += __shfl_xor_sync(0xffffffffu, sacc, 16);
-      if (i > l) t[i] = -sacc;
+      for (int i = x + 1; i < 16; ++i) t[i] = fmaf(-A[(b + i) * LDF + b + x], tx, t[i]);
     }
-    if (hp == 0) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) T[(b + i) * LDF + b + l] = t[i];
-    }
+    for (int i = 0; i < 16; ++i) T[(b + i) * LDF + b + l] = t[i];
   }
-  named_bar_sync(1, 128);
-  if (wq < 2) {
-    const int bi = 16 * (2 * wq + 1), bj = 16 * (2 * wq);
-    float c[2][4] = {};
-    gemm16(A, bi, bj, T, bj, bj, c, ln);  // X = A_ij D_j
-    store16(T, bi, bj, c, 1.f, ln);
+  named_bar_sync(1, 256);
+  if (wq < 4) {
+    // T_{2k+1, 2k} = -D_{2k+1} (A_{2k+1, 2k} D_{2k}); warp pair k, 8 columns each
+    const int k = wq >> 1, cc = 8 * (wq & 1);
+    const int bi = 16 * (2 * k + 1), bj = 16 * (2 * k);
+    float c[4] = {};
+    fma_tile<16>(A, bi, bj, T, bj, bj + cc, c, ln);
+    store_tile(T, bi, bj + cc, c, 1.f, ln);
     __syncwarp();
-    float y[2][4] = {};
-    gemm16(T, bi, bi, T, bi, bj, y, ln);  // D_i X
+    float y[4] = {};
+    fma_tile<16>(T, bi, bi, T, bi, bj + cc, y, ln);
     __syncwarp();
-    store16(T, bi, bj, y, -1.f, ln);
+    store_tile(T, bi, bj + cc, y, -1.f, ln);
   }
-  named_bar_sync(1, 128);
+  named_bar_sync(1, 256);
   {
-    const int rb = 2 + (wq >> 1), cb = wq & 1;
-    float c[2][4] = {};
-    for (int kb = cb; kb < 2; ++kb) gemm16(A, 16 * rb, 16 * kb, T, 16 * kb, 16 * cb, c, ln);
-    store16(T, 16 * rb, 16 * cb, c, 1.f, ln);  // X_{rb,cb} = sum_kb A_{rb,kb} T_{kb,cb}
-    named_bar_sync(1, 128);
-    float y[2][4] = {};
-    for (int kb = 2; kb <= rb; ++kb) gemm16(T, 16 * rb, 16 * kb, T, 16 * kb, 16 * cb, y, ln);
-    named_bar_sync(1, 128);
-    store16(T, 16 * rb, 16 * cb, y, -1.f, ln);
+    // T_21 = -T_22 X, X = A_21 T_11: warp -> output block (rb, cb), 8 columns
+    const int blk = wq >> 1, cc = 8 * (wq & 1);
+    const int rb = 2 + (blk >> 1), cb = blk & 1;
+    float c[4] = {};
+    if (cb == 0)
+      fma_tile<32>(A, 16 * rb, 0, T, 0, cc, c, ln);  // T_11 column block 0: rows 0..31
+    else
+      fma_tile<16>(A, 16 * rb, 16, T, 16, 16 + cc, c, ln);  // column block 1: rows 16..31
+    store_tile(T, 16 * rb, 16 * cb + cc, c, 1.f, ln);
+    named_bar_sync(1, 256);
+    float y[4] = {};
+    if (rb == 3)
+      fma_tile<32>(T, 48, 32, T, 32, 16 * cb + cc, y, ln);  // T_22 row block 1: columns 32..63
+    else
+      fma_tile<16>(T, 32, 32, T, 32, 16 * cb + cc, y, ln);  // row block 0: D_2 only
+    named_bar_sync(1, 256);
+    store_tile(T, 16 * rb, 16 * cb + cc, y, -1.f, ln);
   }
-  named_bar_sync(1, 128);
+  named_bar_sync(1, 256);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -248,6 +223,7 @@ template <int DK, int DV>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gdn_tc_kernel(const Params p, const __grid_constant__ Tmaps tm) {
   using L = TcLayout<DK, DV>;
+  using L_ = L;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -385,40 +361,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
         gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
       }
-      // q norms: rows lane and lane + 32
-      float rq0 = 1.f, rq1 = 1.f;
-      if (p.l2norm) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t rbase = kq + 8192u + (lane + 32 * hh) * 128u;
-          float ss = 0.f;
-#pragma unroll
-          for (int a = 0; a < L::NKA; ++a)
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-              uint32_t x[4];
-              ld_shared_v4(rbase + a * 16384u + ch * 16u, x[0], x[1], x[2], x[3]);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float lo = bf16_lo_f(x[e]), hi = bf16_hi_f(x[e]);
-                ss = fmaf(lo, lo, ss);
-                ss = fmaf(hi, hi, ss);
-              }
-            }
-          const float r = 1.0f / sqrtf(ss + 1e-6f);
-          if (hh == 0)
-            rq0 = r;
-          else
-            rq1 = r;
-        }
-      }
       float* sc = stage_scal(s);
       sc[SC_G + lane] = c0v;
       sc[SC_G + lane + 32] = c1v;
       sc[SC_B + lane] = b0;
       sc[SC_B + lane + 32] = b1;
-      sc[SC_RQ + lane] = rq0;
-      sc[SC_RQ + lane + 32] = rq1;
       if (lane == 0) {
         sc[SC_GMAX] = gmax;
         sc[SC_GMIN] = gmin;
@@ -492,8 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t id_pu = idesc_bf16(128, 64, 0, 0);
       for (int c = 0; c < nchunks; ++c) {
         const int s = c & 1, par = c & 1;
-        if (!mbar_wait(&bars[B_P1_DONE0 + par], (c >> 1) & 1, abort_flag, kWaitLimitNs) ||
-            !mbar_wait(&bars[B_S_READY], c & 1, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait(&bars[B_P1_DONE0 + par], (c >> 1) & 1, abort_flag, kWaitLimitNs)) {
           fail(4);
           break;
         }
@@ -502,7 +448,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t tb = sbase + L::TB0 + par * L::SCR_BYTES;
         const uint32_t wt = sbase + L::WT0 + par * L::SCR_BYTES;
         const uint32_t sop = sbase + L::SOP;
-        // U^T = V^T (T_b hi + lo)^T : A = V^T MN-major (d_v atoms 8 KB apart or the zero page)
+        // U^T = V^T (T_b hi + lo)^T : A = V^T MN-major (d_v atoms 8 KB apart or the zero page).
+        // State-independent: issued as soon as the chunk is prepared.
         const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
 #pragma unroll
         for (int half = 0; half < 2; ++half)
@@ -510,6 +457,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_R, sdesc(vv + k * 2048u, lbo_v, 1024),
                    sdesc(tb + half * 8192u + k * 32u, 16, 1024), id_u, (half | k) != 0);
+        if (!mbar_wait(&bars[B_S_READY], c & 1, abort_flag, kWaitLimitNs)) {
+          fail(5);
+          break;
+        }
+        tc_fence_after();
         // U'^T += (-S^T) W^T : A = -S^T K-major, B = W^T MN-major [d_k][j]
 #pragma unroll
         for (int a = 0; a < L::NKA; ++a)
@@ -517,16 +469,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_R, sdesc(sop + a * 16384u + k * 32u, 16, 1024),
                    sdesc(wt + (a * 4 + k) * 2048u, 16, 1024), id_sw, 1);
-        // QS^T = (-S^T) Q^T : B = the raw q tile (K-major)
+        mma_commit(&bars[B_UP_DONE]);
+        // QS^T = (-S^T) Q^T (raw q tile, K-major), once the last epilogue has read its block
+        if (c >= 1 && !mbar_wait(&bars[B_EPI_DONE], (c - 1) & 1, abort_flag, kWaitLimitNs)) {
+          fail(6);
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int a = 0; a < L::NKA; ++a)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + TM_QS, sdesc(sop + a * 16384u + k * 32u, 16, 1024),
                    sdesc(kq + a * 16384u + 8192u + k * 32u, 16, 1024), id_qs, (a | k) != 0);
-        mma_commit(&bars[B_UP_DONE]);
         if (!mbar_wait(&bars[B_UOPS_READY], c & 1, abort_flag, kWaitLimitNs)) {
-          fail(5);
+          fail(7);
           break;
         }
         tc_fence_after();
@@ -538,7 +495,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < 4; ++k)
             mma_ts(tmem + TM_S, tmem + (half ? TM_UL : TM_UH) + k * 8u,
                    sdesc(kq + k * 2048u, lbo_kn, 1024), id_st, 1);
-        // O^T += U'^T P^T : A from TMEM (bf16 U'), B = P K-major [i][j]
+        mma_commit(&bars[B_STATE_DONE]);
+        // O^T = U'^T P^T : A from TMEM (bf16 U'), B = P K-major [i][j]
         const uint32_t pp = sbase + L::P0 + par * 8192u;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -549,185 +507,204 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mma_commit(&bars[B_DRAIN2]);
       mbar_wait(&bars[B_DRAIN2], 0, nullptr, 100000000ull);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ================================================================ WG-A: chunk preparation
-    const int wa = tid - 128;  // == TMEM lane
-    const uint32_t lane_off = (uint32_t)((wa & ~31) << 16);
-    const bool krow = wa < 64;
-    const int i = wa & 63;
+    const int wa = tid - 128;         // 0..255
+    const int L = wa & 127;           // TMEM lane
+    const int hf = wa >> 7;           // which 32-column half of a 64-wide block
+    const uint32_t lane_off = (uint32_t)((L & ~31) << 16);
+    const bool krow = L < 64;
+    const int i = L & 63;
     for (int c = 0; c < nchunks; ++c) {
       const int s = c & 1, par = c & 1;
       bool ok = mbar_wait(&bars[B_READY0 + s], (c >> 1) & 1, abort_flag, kWaitLimitNs);
+      // P, T_b and W^T of this parity were last read by chunk c-2's MMAs
       if (ok && c >= 2)
-        ok = mbar_wait(&bars[B_BUF_FREE0 + par], ((c >> 1) + 1) & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(6);
-      named_bar_sync(1, 128);
+        ok = mbar_wait(&bars[B_EMPTY0 + s], ((c >> 1) + 1) & 1, abort_flag, kWaitLimitNs);
+      // chunk scalars c % 3 were last read by chunk c-3's epilogue
+      if (ok && c >= 3)
+        ok = mbar_wait(&bars[B_CS_FREE0 + c % 3], ((c / 3) + 1) & 1, abort_flag, kWaitLimitNs);
+      if (!ok) fail(8);
+      named_bar_sync(1, 256);
       if (*abort_flag) break;
-      const uint32_t kq = stage_kq(s);
       const float* sc = stage_scal(s);
-      ChunkScalars& cs = cscal[par];
+      ChunkScalars& cs = cscal[c % 3];
       const float gmax = sc[SC_GMAX];
       const bool exact = (gmax - sc[SC_GMIN]) > kMaxDecaySpan;
       const float Gi = sc[SC_G + i], Gl2i = Gi * kLog2e, GCl2 = sc[SC_G + 63] * kLog2e;
       const float ai = exp2f((Gi - gmax) * kLog2e);
       ok = mbar_wait(&bars[B_KQ_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(7);
-      named_bar_sync(1, 128);
+      if (!ok) fail(9);
+      named_bar_sync(1, 256);
       if (*abort_flag) break;
       tc_fence_after();
-      uint32_t v0[32], v1[32];
-      tmem_ld32(tmem + lane_off + TM_KQ, v0);
-      tmem_ld32(tmem + lane_off + TM_KQ + 32, v1);
+      float qss_own = 0.f;
+      uint32_t v[32];  // row L of [K;Q] K^T, columns [32 hf, 32 hf + 32)
+      tmem_ld32(tmem + lane_off + TM_KQ + 32 * hf, v);
       tmem_ld_wait();
-      float* Abuf = reinterpret_cast<float*>(sm + L::WT0 + par * L::SCR_BYTES);
-      float* Tbuf = reinterpret_cast<float*>(sm + L::TB0 + par * L::SCR_BYTES);
-      float ri = 1.f;
-      if (krow) {
+      float* Abuf = reinterpret_cast<float*>(sm + L_::WT0 + par * L_::SCR_BYTES);
+      float* Tbuf = reinterpret_cast<float*>(sm + L_::TB0 + par * L_::SCR_BYTES);
+      if (krow && (i >> 5) == hf) {
         // r^k_i from the diagonal of K K^T (fp32 sum of exact bf16 products)
         float diag = 0.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-          if (j == i) diag = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
-        ri = p.l2norm ? 1.0f / sqrtf(diag + 1e-6f) : 1.f;
+        for (int j = 0; j < 32; ++j)
+          if (j == (i & 31)) diag = __uint_as_float(v[j]);
+        const float ri = p.l2norm ? 1.0f / sqrtf(diag + 1e-6f) : 1.f;
         const float bi = sc[SC_B + i];
         ps->d[i] = ri * exp2f((gmax - Gi) * kLog2e);
         ps->r[i] = ri;
         ps->beta[i] = bi;
         ps->tw[i] = bi * exp2f(Gl2i) * ri;
         cs.s[i] = exp2f(GCl2 - Gl2i) * ri;
-      } else {
-        const float co = p.scale * sc[SC_RQ + i];
+      } else if (!krow) {
+        // |q_i|^2 over this thread's half of the raw q row (r^q only scales the output)
+        float ss0 = 0.f, ss1 = 0.f;
+        const uint32_t rbase = stage_kq(s) + 8192u + i * 128u;
+#pragma unroll
+        for (int k = 0; k < 4 * L_::NKA; ++k) {
+          const int idx = hf * 4 * L_::NKA + k;
+          uint32_t x[4];
+          ld_shared_v4(rbase + (idx >> 3) * 16384u + (idx & 7) * 16u, x[0], x[1], x[2], x[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = bf16_lo_f(x[e]), hi = bf16_hi_f(x[e]);
+            ss0 = fmaf(lo, lo, ss0);
+            ss1 = fmaf(hi, hi, ss1);
+          }
+        }
+        if (hf == 1) const_cast<float*>(sc)[SC_QSS + i] = ss0 + ss1;
+        else qss_own = ss0 + ss1;
+      }
+      named_bar_sync(1, 256);
+      if (!krow && hf == 0) {
+        const float rq = p.l2norm ? 1.0f / sqrtf(qss_own + sc[SC_QSS + i] + 1e-6f) : 1.f;
+        const float co = p.scale * rq;
         cs.co[i] = co;
         cs.cq[i] = -co * exp2f(Gl2i);
         if (i == 0) cs.eGC = exp2f(GCl2);
       }
-      named_bar_sync(1, 128);
       if (krow) {
         // A_ij = beta_i r_i r_j e^{G_i - G_j} k_i.k_j  (j < i), fp32 into the scratch
-        const float ci = ps->beta[i] * ri;
+        const float ci = ps->beta[i] * ps->r[i];
         const float cia = ci * ai;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < 8; ++q) {
+          const int j0 = 32 * hf + 4 * q;
+          const float4 d4 = *reinterpret_cast<const float4*>(&ps->d[j0]);
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
           float a4[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = q * 4 + e;
-            const float kk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
-            a4[e] = (cia * kk) * ps->d[j];
-          }
+          for (int e = 0; e < 4; ++e) a4[e] = (cia * __uint_as_float(v[4 * q + e])) * dd[e];
           if (exact) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = q * 4 + e;
-              const float kk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
-              a4[e] = ci * ps->r[j] * exp2f(Gl2i - sc[SC_G + j] * kLog2e) * kk;
-            }
+            for (int e = 0; e < 4; ++e)
+              a4[e] = ci * ps->r[j0 + e] * exp2f(Gl2i - sc[SC_G + j0 + e] * kLog2e) *
+                      __uint_as_float(v[4 * q + e]);
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) a4[e] = (q * 4 + e < i) ? a4[e] : 0.f;
-          *reinterpret_cast<float4*>(&Abuf[i * LDF + q * 4]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+          for (int e = 0; e < 4; ++e) a4[e] = (j0 + e < i) ? a4[e] : 0.f;
+          *reinterpret_cast<float4*>(&Abuf[i * LDF + j0]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
         }
       } else {
         // P_ij = e^{G_i - G_j} r^k_j q_i.k_j  (j <= i), bf16 K-major [i][j]
-        const uint32_t prow = sbase + L::P0 + par * 8192u;
+        const uint32_t prow = sbase + L_::P0 + par * 8192u;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int q = 0; q < 4; ++q) {
+          const int j0 = 32 * hf + 8 * q;
+          const float4 da = *reinterpret_cast<const float4*>(&ps->d[j0]);
+          const float4 db = *reinterpret_cast<const float4*>(&ps->d[j0 + 4]);
+          const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
           float pv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = ch * 8 + e;
-            const float qk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
-            pv[e] = (ai * qk) * ps->d[j];
-          }
+          for (int e = 0; e < 8; ++e) pv[e] = (ai * __uint_as_float(v[8 * q + e])) * dd[e];
           if (exact) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int j = ch * 8 + e;
-              const float qk = __uint_as_float(j < 32 ? v0[j] : v1[j - 32]);
-              pv[e] = ps->r[j] * exp2f(Gl2i - sc[SC_G + j] * kLog2e) * qk;
-            }
+            for (int e = 0; e < 8; ++e)
+              pv[e] = ps->r[j0 + e] * exp2f(Gl2i - sc[SC_G + j0 + e] * kLog2e) *
+                      __uint_as_float(v[8 * q + e]);
           }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pv[e] = (ch * 8 + e <= i) ? pv[e] : 0.f;
-          st_shared_v4(prow + sw128(i, ch), pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
+          for (int e = 0; e < 8; ++e) pv[e] = (j0 + e <= i) ? pv[e] : 0.f;
+          st_shared_v4(prow + sw128(i, 4 * hf + q), pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
                        pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       // ---- T = (I + A)^-1
       solve_unit_lower(Abuf, Tbuf, wa);
       // ---- T_b = T diag(beta) as bf16 hi + lo; T_w = T diag(beta e^G r^k)
       {
-        const int ti = wa & 63, hh = wa >> 6;
-        float t[32];
+        const int ti = wa & 63, qq = wa >> 6;  // row ti, columns [16 qq, 16 qq + 16)
+        float t[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 x = *reinterpret_cast<const float4*>(&Tbuf[ti * LDF + hh * 32 + q * 4]);
-          const bool zero = ((hh * 32 + q * 4) >> 4) > (ti >> 4);  // block above the diagonal
-          t[q * 4 + 0] = zero ? 0.f : x.x;
-          t[q * 4 + 1] = zero ? 0.f : x.y;
-          t[q * 4 + 2] = zero ? 0.f : x.z;
-          t[q * 4 + 3] = zero ? 0.f : x.w;
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float4 x = *reinterpret_cast<const float4*>(&Tbuf[ti * LDF + 16 * qq + 4 * k4]);
+          const bool zero = qq > (ti >> 4);  // block above the diagonal
+          t[4 * k4 + 0] = zero ? 0.f : x.x;
+          t[4 * k4 + 1] = zero ? 0.f : x.y;
+          t[4 * k4 + 2] = zero ? 0.f : x.z;
+          t[4 * k4 + 3] = zero ? 0.f : x.w;
         }
-        named_bar_sync(1, 128);  // every thread has read T before it is overwritten
-        const uint32_t tb = sbase + L::TB0 + par * L::SCR_BYTES;
+        named_bar_sync(1, 256);  // every thread has read T before it is overwritten
+        const uint32_t tb = sbase + L_::TB0 + par * L_::SCR_BYTES;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
+          const int j0 = 16 * qq + 8 * q;
+          const float4 ba = *reinterpret_cast<const float4*>(&ps->beta[j0]);
+          const float4 bb = *reinterpret_cast<const float4*>(&ps->beta[j0 + 4]);
+          const float4 wa4 = *reinterpret_cast<const float4*>(&ps->tw[j0]);
+          const float4 wb4 = *reinterpret_cast<const float4*>(&ps->tw[j0 + 4]);
+          const float bt[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+          const float wt8[8] = {wa4.x, wa4.y, wa4.z, wa4.w, wb4.x, wb4.y, wb4.z, wb4.w};
           uint32_t hi4[4], lo4[4], w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int j0 = hh * 32 + q * 8 + e * 2;
-            const float x0 = t[q * 8 + e * 2] * ps->beta[j0];
-            const float x1 = t[q * 8 + e * 2 + 1] * ps->beta[j0 + 1];
+            const float x0 = t[8 * q + 2 * e] * bt[2 * e], x1 = t[8 * q + 2 * e + 1] * bt[2 * e + 1];
             hi4[e] = pack_bf16(x0, x1);
             lo4[e] = pack_bf16(x0 - bf16_lo_f(hi4[e]), x1 - bf16_hi_f(hi4[e]));
-            w4[e] = pack_bf16(t[q * 8 + e * 2] * ps->tw[j0], t[q * 8 + e * 2 + 1] * ps->tw[j0 + 1]);
+            w4[e] = pack_bf16(t[8 * q + 2 * e] * wt8[2 * e], t[8 * q + 2 * e + 1] * wt8[2 * e + 1]);
           }
-          const uint32_t off = sw128(ti, hh * 4 + q);
+          const uint32_t off = sw128(ti, 2 * qq + q);
           st_shared_v4(tb + off, hi4[0], hi4[1], hi4[2], hi4[3]);
           st_shared_v4(tb + 8192u + off, lo4[0], lo4[1], lo4[2], lo4[3]);
-          st_shared_v4(sbase + L::TW + off, w4[0], w4[1], w4[2], w4[3]);
+          st_shared_v4(sbase + L_::TW + off, w4[0], w4[1], w4[2], w4[3]);
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       if (wa == 0) mbar_arrive(&bars[B_P1_MID]);
       // ---- W^T: TMEM -> bf16 MN-major [d_k][j]
       ok = mbar_wait(&bars[B_W_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(8);
-      named_bar_sync(1, 128);
+      if (!ok) fail(10);
+      named_bar_sync(1, 256);
       if (*abort_flag) break;
       tc_fence_after();
       {
-        tmem_ld32(tmem + lane_off + TM_KQ, v0);
-        tmem_ld32(tmem + lane_off + TM_KQ + 32, v1);
+        tmem_ld32(tmem + lane_off + TM_KQ + 32 * hf, v);
         tmem_ld_wait();
-        const uint32_t wt = sbase + L::WT0 + par * L::SCR_BYTES;
+        const uint32_t wt = sbase + L_::WT0 + par * L_::SCR_BYTES;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = ch * 8 + e * 2;
-            w4[e] = pack_bf16(__uint_as_float(j < 32 ? v0[j] : v1[j - 32]),
-                              __uint_as_float(j + 1 < 32 ? v0[j + 1] : v1[j + 1 - 32]));
-          }
-          st_shared_v4(wt + sw128(wa, ch), w4[0], w4[1], w4[2], w4[3]);
-        }
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(wt + sw128(L, 4 * hf + q),
+                       pack_bf16(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                       pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                       pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                       pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       if (wa == 0) {
         mbar_arrive(&bars[B_P1_DONE0 + par]);
         mbar_arrive(&bars[B_KQ_FREE]);
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ================================================================ WG-B: state step + epilogue
-    const int wb = tid - 256;  // == TMEM lane == d_v index
+    const int wb = tid - 384;  // == TMEM lane == d_v index
     const uint32_t lane_off = (uint32_t)((wb & ~31) << 16);
     const bool live = wb < DV;
     // initial state -> S^T in TMEM (lane d_v, column d_k)
@@ -744,152 +721,134 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tmem_st_wait();
     }
-    for (int c = 0; c < nchunks; ++c) {
+    // S -> -S^T (bf16 operand of chunk c's MMAs); S *= e^{G_m} of chunk c
+    auto s_convert = [&](int c) -> bool {
       const int par = c & 1;
-      // ---- S -> -S^T (bf16 operand); S *= e^{G_m}
       bool ok = mbar_wait(&bars[B_P1_DONE0 + par], (c >> 1) & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(9);
+      if (ok && c >= 1) ok = mbar_wait(&bars[B_STATE_DONE], (c - 1) & 1, abort_flag, kWaitLimitNs);
+      if (!ok) fail(11);
       named_bar_sync(2, 128);
-      if (*abort_flag) break;
+      if (*abort_flag) return false;
       tc_fence_after();
-      const ChunkScalars& cs = cscal[par];
-      const float eGC = cs.eGC;
+      const float eGC = cscal[c % 3].eGC;
 #pragma unroll 1
-      for (int xp = 0; xp < DK / 64; ++xp) {
-        uint32_t va[32], vb[32];
-        tmem_ld32(tmem + lane_off + TM_S + xp * 64, va);
-        tmem_ld32(tmem + lane_off + TM_S + xp * 64 + 32, vb);
+      for (int xb = 0; xb < DK / 32; ++xb) {
+        uint32_t va[32];
+        tmem_ld32(tmem + lane_off + TM_S + xb * 32, va);
         tmem_ld_wait();
-        const uint32_t row = sbase + L::SOP + xp * 16384u;
+        const uint32_t row = sbase + L_::SOP + (xb >> 1) * 16384u;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint32_t w4[4];
+        for (int q = 0; q < 4; ++q)
+          st_shared_v4(row + sw128(wb, (xb & 1) * 4 + q),
+                       pack_bf16(-__uint_as_float(va[8 * q + 0]), -__uint_as_float(va[8 * q + 1])),
+                       pack_bf16(-__uint_as_float(va[8 * q + 2]), -__uint_as_float(va[8 * q + 3])),
+                       pack_bf16(-__uint_as_float(va[8 * q + 4]), -__uint_as_float(va[8 * q + 5])),
+                       pack_bf16(-__uint_as_float(va[8 * q + 6]), -__uint_as_float(va[8 * q + 7])));
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int x = q * 8 + e * 2;
-            w4[e] = pack_bf16(-__uint_as_float(x < 32 ? va[x] : vb[x - 32]),
-                              -__uint_as_float(x + 1 < 32 ? va[x + 1] : vb[x + 1 - 32]));
-          }
-          st_shared_v4(row + sw128(wb, q), w4[0], w4[1], w4[2], w4[3]);
-        }
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          va[x] = __float_as_uint(__uint_as_float(va[x]) * eGC);
-          vb[x] = __float_as_uint(__uint_as_float(vb[x]) * eGC);
-        }
-        tmem_st32(tmem + lane_off + TM_S + xp * 64, va);
-        tmem_st32(tmem + lane_off + TM_S + xp * 64 + 32, vb);
+        for (int x = 0; x < 32; ++x) va[x] = __float_as_uint(__uint_as_float(va[x]) * eGC);
+        tmem_st32(tmem + lane_off + TM_S + xb * 32, va);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(2, 128);
       if (wb == 0) mbar_arrive(&bars[B_S_READY]);
+      return true;
+    };
+    bool run = nchunks == 0 || s_convert(0);
+    for (int c = 0; run && c < nchunks; ++c) {
+      const ChunkScalars& cs = cscal[c % 3];
       // ---- U' -> (U' s) hi / lo and U' as bf16, into TMEM A operands
-      ok = mbar_wait(&bars[B_UP_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(10);
+      bool ok = mbar_wait(&bars[B_UP_DONE], c & 1, abort_flag, kWaitLimitNs);
+      if (!ok) fail(12);
       named_bar_sync(2, 128);
       if (*abort_flag) break;
       tc_fence_after();
-      {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tmem + lane_off + TM_R, u0);
-        tmem_ld32(tmem + lane_off + TM_R + 32, u1);
+#pragma unroll 1
+      for (int hb = 0; hb < 2; ++hb) {  // tokens [32 hb, 32 hb + 32)
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_off + TM_R + hb * 32, u);
         tmem_ld_wait();
-        uint32_t w[32];
+        uint32_t hi[16], lo[16], uu[16];
 #pragma unroll
-        for (int pass = 0; pass < 3; ++pass) {
+        for (int q = 0; q < 8; ++q) {
+          const float4 s4 = *reinterpret_cast<const float4*>(&cs.s[hb * 32 + q * 4]);
+          const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            const int j = 2 * cc;
-            const float a0 = __uint_as_float(j < 32 ? u0[j] : u1[j - 32]);
-            const float a1 = __uint_as_float(j + 1 < 32 ? u0[j + 1] : u1[j + 1 - 32]);
-            if (pass == 2) {
-              w[cc] = pack_bf16(a0, a1);
-            } else {
-              const float x0 = a0 * cs.s[j], x1 = a1 * cs.s[j + 1];
-              const uint32_t hi = pack_bf16(x0, x1);
-              w[cc] = pass == 0 ? hi : pack_bf16(x0 - bf16_lo_f(hi), x1 - bf16_hi_f(hi));
-            }
+          for (int e = 0; e < 2; ++e) {
+            const float a0 = __uint_as_float(u[q * 4 + 2 * e]), a1 = __uint_as_float(u[q * 4 + 2 * e + 1]);
+            const float x0 = a0 * sv[2 * e], x1 = a1 * sv[2 * e + 1];
+            const uint32_t hh = pack_bf16(x0, x1);
+            hi[q * 2 + e] = hh;
+            lo[q * 2 + e] = pack_bf16(x0 - bf16_lo_f(hh), x1 - bf16_hi_f(hh));
+            uu[q * 2 + e] = pack_bf16(a0, a1);
           }
-          tmem_st32(tmem + lane_off + (pass == 0 ? TM_UH : pass == 1 ? TM_UL : TM_UU), w);
         }
-        tmem_st_wait();
+        tmem_st16(tmem + lane_off + TM_UH + hb * 16, hi);
+        tmem_st16(tmem + lane_off + TM_UL + hb * 16, lo);
+        tmem_st16(tmem + lane_off + TM_UU + hb * 16, uu);
       }
+      tmem_st_wait();
       tc_fence_before();
       named_bar_sync(2, 128);
       if (wb == 0) mbar_arrive(&bars[B_UOPS_READY]);
-      // ---- epilogue: o_i = scale r^q_i O^T[:, i], staged through shared memory
+      // ---- the next chunk's state operand first: it is on the serial path
+      if (c + 1 < nchunks && !s_convert(c + 1)) break;
+      // ---- epilogue: o_i = cq_i (-S^T q_i) + co_i (U'^T P^T)_i, stored straight to out
       ok = mbar_wait(&bars[B_O_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(11);
+      if (!ok) fail(13);
       named_bar_sync(2, 128);
       if (*abort_flag) break;
       tc_fence_after();
       {
         const int64_t t0 = bos + (int64_t)c * kChunk;
         const int m = chunk_rows(c);
-        uint8_t* stg = sm + L::SOP;
+        const bool odd = wb & 1;
 #pragma unroll 1
-        for (int hb = 0; hb < 2; ++hb) {  // token halves [32 hb, 32 hb + 32)
+        for (int hb = 0; hb < 2; ++hb) {  // tokens [32 hb, 32 hb + 32)
           uint32_t oq[32], oi[32];
           tmem_ld32(tmem + lane_off + TM_QS + hb * 32, oq);
           tmem_ld32(tmem + lane_off + TM_O + hb * 32, oi);
           tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&cs.cq[hb * 32 + q * 4]);
+            const float4 b4 = *reinterpret_cast<const float4*>(&cs.co[hb * 32 + q * 4]);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              oq[q * 4 + e] = __float_as_uint(fmaf(av[e], __uint_as_float(oq[q * 4 + e]),
+                                                   bv[e] * __uint_as_float(oi[q * 4 + e])));
+          }
           if (p.out_f32) {
-            float* st = reinterpret_cast<float*>(stg);
             if (live) {
 #pragma unroll
-              for (int ii = 0; ii < 32; ++ii) {
-                const int i2 = hb * 32 + ii;
-                st[i2 * DV + wb] = fmaf(cs.cq[i2], __uint_as_float(oq[ii]), cs.co[i2] * __uint_as_float(oi[ii]));
-              }
+              for (int ii = 0; ii < 32; ++ii)
+                if (hb * 32 + ii < m)
+                  reinterpret_cast<float*>(p.out)[((size_t)(t0 + hb * 32 + ii) * p.h_v + h) * DV + wb] =
+                      __uint_as_float(oq[ii]);
             }
           } else {
-            // lanes 2k and 2k+1 swap values so each writes a bf16 pair (d_v 2k, 2k+1)
-            // of one token; odd rows flip word bit 4 against bank conflicts
-            uint32_t* st = reinterpret_cast<uint32_t*>(stg);
-            const bool odd = wb & 1;
+            // lanes 2k and 2k+1 swap values so each stores a bf16 pair (d_v 2k, 2k+1)
+            // of one token: a warp writes two 64-byte row segments per store
 #pragma unroll
             for (int tp = 0; tp < 16; ++tp) {
-              const int i0 = hb * 32 + 2 * tp, i1 = i0 + 1;
-              const float x0 = fmaf(cs.cq[i0], __uint_as_float(oq[2 * tp]), cs.co[i0] * __uint_as_float(oi[2 * tp]));
-              const float x1 = fmaf(cs.cq[i1], __uint_as_float(oq[2 * tp + 1]), cs.co[i1] * __uint_as_float(oi[2 * tp + 1]));
+              const float x0 = __uint_as_float(oq[2 * tp]), x1 = __uint_as_float(oq[2 * tp + 1]);
               const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
-              const int row = odd ? i1 : i0;
+              const int row = hb * 32 + 2 * tp + (odd ? 1 : 0);
               const uint32_t word = odd ? pack_bf16(got, x1) : pack_bf16(x0, got);
-              if (live) st[row * (DV / 2) + ((wb >> 1) ^ ((row & 1) << 4))] = word;
-            }
-          }
-        }
-        named_bar_sync(2, 128);
-        // coalesced copy-out of rows < m, 16 bytes at a time
-        if (p.out_f32) {
-          constexpr int cpr = DV * 4 / 16;
-          for (int q = wb; q < 64 * cpr; q += 128) {
-            const int row = q / cpr, ch = q % cpr;
-            if (row < m) {
-              uint32_t x[4];
-              ld_shared_v4(sbase + L::SOP + row * (DV * 4) + ch * 16, x[0], x[1], x[2], x[3]);
-              float* dst = reinterpret_cast<float*>(p.out) + ((size_t)(t0 + row) * p.h_v + h) * DV + ch * 4;
-              *reinterpret_cast<uint4*>(dst) = make_uint4(x[0], x[1], x[2], x[3]);
-            }
-          }
-        } else {
-          constexpr int cpr = DV * 2 / 16;
-          for (int q = wb; q < 64 * cpr; q += 128) {
-            const int row = q / cpr, ch = q % cpr;
-            if (row < m) {
-              uint32_t x[4];
-              ld_shared_v4(sbase + L::SOP + row * (DV * 2) + ((ch ^ ((row & 1) << 2)) * 16), x[0], x[1], x[2], x[3]);
-              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + ((size_t)(t0 + row) * p.h_v + h) * DV + ch * 8;
-              *reinterpret_cast<uint4*>(dst) = make_uint4(x[0], x[1], x[2], x[3]);
+              if (live && row < m)
+                reinterpret_cast<uint32_t*>(p.out)[(((size_t)(t0 + row) * p.h_v + h) * DV + (wb & ~1)) >> 1] = word;
             }
           }
         }
       }
       tc_fence_before();
       named_bar_sync(2, 128);
-      if (wb == 0) mbar_arrive(&bars[B_BUF_FREE0 + par]);
+      if (wb == 0) {
+        mbar_arrive(&bars[B_EPI_DONE]);
+        mbar_arrive(&bars[B_CS_FREE0 + c % 3]);
+      }
     }
     // final state
     if (!*abort_flag && p.final_state) {
