@@ -125,29 +125,38 @@ struct Tmaps {
   CUtensorMap q, k, v;
 };
 
+// Exact-decay fallback for a chunk whose log-decay spans more than
+// kMaxDecaySpan (the factorised e^{G_i - G_j} = a_i b_j could leave fp32
+// range): 32 entries of one A row (krow) or P row, each decay by its own exp.
+// Kept out of line: it is rare and its code would crowd the hot loop.
+__device__ __noinline__ void exact_row(float* out, const uint32_t* v, const float* r, const float* G,
+                                       float Gl2i, float ci, int j0, int i, int krow) {
+  for (int e = 0; e < 32; ++e) {
+    const int j = j0 + e;
+    const float x = r[j] * exp2f(Gl2i - G[j] * 1.4426950408889634f) * __uint_as_float(v[e]);
+    out[e] = krow ? ((j < i) ? ci * x : 0.f) : ((j <= i) ? x : 0.f);
+  }
+}
+
 // ---------------------------------------------------------------- the solve
-// C[16 x 8] (+)= X[16 x K block at (xr, xc)] * Y[K x 8 block at (yr, yc)] in
+// C[16 x 8] += X[16 x 16 block at (xr, xc)] * Y[16 x 8 block at (yr, yc)] in
 // fp32 FMA, fp32 smem with row stride LDF. Lane (g, t) = (lane / 4, lane % 4)
 // owns rows g, g + 8 and columns 2t, 2t + 1; all operand loads are issued up
 // front so the four accumulation chains run back to back.
-template <int K>
-__device__ __forceinline__ void fma_tile(const float* X, int xr, int xc, const float* Y, int yr, int yc,
-                                         float (&c)[4], int lane) {
+__device__ __forceinline__ void fma_tile16(const float* X, int xr, int xc, const float* Y, int yr, int yc,
+                                           float (&c)[4], int lane) {
   const int g = lane >> 2, t = lane & 3;
-  float xa[K], xb[K];
-  float2 yv[K];
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    xa[k] = X[(xr + g) * LDF + xc + k];
-    xb[k] = X[(xr + g + 8) * LDF + xc + k];
-    yv[k] = *reinterpret_cast<const float2*>(&Y[(yr + k) * LDF + yc + 2 * t]);
-  }
-#pragma unroll
-  for (int k = 0; k < K; ++k) {
-    c[0] = fmaf(xa[k], yv[k].x, c[0]);
-    c[1] = fmaf(xa[k], yv[k].y, c[1]);
-    c[2] = fmaf(xb[k], yv[k].x, c[2]);
-    c[3] = fmaf(xb[k], yv[k].y, c[3]);
+  const float* xr0 = X + (xr + g) * LDF + xc;
+  const float* xr1 = xr0 + 8 * LDF;
+  const float* yr0 = Y + yr * LDF + yc + 2 * t;
+#pragma unroll 4
+  for (int k = 0; k < 16; ++k) {
+    const float a0 = xr0[k], a1 = xr1[k];
+    const float2 b = *reinterpret_cast<const float2*>(yr0 + k * LDF);
+    c[0] = fmaf(a0, b.x, c[0]);
+    c[1] = fmaf(a0, b.y, c[1]);
+    c[2] = fmaf(a1, b.x, c[2]);
+    c[3] = fmaf(a1, b.y, c[3]);
   }
 }
 __device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float (&c)[4], float sgn,
@@ -182,40 +191,38 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, fl
     for (int i = 0; i < 16; ++i) T[(b + i) * LDF + b + l] = t[i];
   }
   named_bar_sync(1, 256);
-  if (wq < 4) {
-    // T_{2k+1, 2k} = -D_{2k+1} (A_{2k+1, 2k} D_{2k}); warp pair k, 8 columns each
-    const int k = wq >> 1, cc = 8 * (wq & 1);
-    const int bi = 16 * (2 * k + 1), bj = 16 * (2 * k);
+  // Both merge levels as "C = X * Y over a run of 16-wide k blocks, then
+  // store" steps; a warp computes 8 columns of one 16x16 output block. One
+  // tile routine serves all of them through short runtime loops.
+  for (int lvl = 0; lvl < 2; ++lvl) {
+    // level 0: T_{2k+1,2k} = -D_{2k+1} (A_{2k+1,2k} D_{2k}), warps 0-3
+    // level 1: T_{rb,cb} = -T_22 (A_21 T_11) blocks, all 8 warps
+    const bool active = lvl == 1 || wq < 4;
+    int rb, cb, cc;
+    if (lvl == 0) {
+      rb = 2 * (wq >> 1) + 1;
+      cb = 2 * (wq >> 1);
+    } else {
+      rb = 2 + (wq >> 2);
+      cb = (wq >> 1) & 1;
+    }
+    cc = 8 * (wq & 1);
+    // X = A[rb, k0..k1) T[k0..k1, cb]; level 0: k = cb only; level 1: k = cb..1
+    const int xk0 = cb, xk1 = lvl == 0 ? cb + 1 : 2;
     float c[4] = {};
-    fma_tile<16>(A, bi, bj, T, bj, bj + cc, c, ln);
-    store_tile(T, bi, bj + cc, c, 1.f, ln);
-    __syncwarp();
-    float y[4] = {};
-    fma_tile<16>(T, bi, bi, T, bi, bj + cc, y, ln);
-    __syncwarp();
-    store_tile(T, bi, bj + cc, y, -1.f, ln);
-  }
-  named_bar_sync(1, 256);
-  {
-    // T_21 = -T_22 X, X = A_21 T_11: warp -> output block (rb, cb), 8 columns
-    const int blk = wq >> 1, cc = 8 * (wq & 1);
-    const int rb = 2 + (blk >> 1), cb = blk & 1;
-    float c[4] = {};
-    if (cb == 0)
-      fma_tile<32>(A, 16 * rb, 0, T, 0, cc, c, ln);  // T_11 column block 0: rows 0..31
-    else
-      fma_tile<16>(A, 16 * rb, 16, T, 16, 16 + cc, c, ln);  // column block 1: rows 16..31
-    store_tile(T, 16 * rb, 16 * cb + cc, c, 1.f, ln);
+    if (active)
+      for (int kb = xk0; kb < xk1; ++kb) fma_tile16(A, 16 * rb, 16 * kb, T, 16 * kb, 16 * cb + cc, c, ln);
+    if (active) store_tile(T, 16 * rb, 16 * cb + cc, c, 1.f, ln);
     named_bar_sync(1, 256);
+    // Y = T[rb, k0..k1) X[k0..k1, cb]; level 0: k = rb (D_rb); level 1: k = 2..rb (T_22)
+    const int yk0 = lvl == 0 ? rb : 2, yk1 = rb + 1;
     float y[4] = {};
-    if (rb == 3)
-      fma_tile<32>(T, 48, 32, T, 32, 16 * cb + cc, y, ln);  // T_22 row block 1: columns 32..63
-    else
-      fma_tile<16>(T, 32, 32, T, 32, 16 * cb + cc, y, ln);  // row block 0: D_2 only
+    if (active)
+      for (int kb = yk0; kb < yk1; ++kb) fma_tile16(T, 16 * rb, 16 * kb, T, 16 * kb, 16 * cb + cc, y, ln);
     named_bar_sync(1, 256);
-    store_tile(T, 16 * rb, 16 * cb + cc, y, -1.f, ln);
+    if (active) store_tile(T, 16 * rb, 16 * cb + cc, y, -1.f, ln);
+    named_bar_sync(1, 256);
   }
-  named_bar_sync(1, 256);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -404,13 +411,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t kq = stage_kq(s);
         // [K;Q] K^T : A = rows of K then Q (K-major), B = K (K-major, N = 64)
+        const uint64_t dkq = sdesc(kq, 16, 1024);
 #pragma unroll
         for (int a = 0; a < L::NKA; ++a)
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const uint32_t off = a * 16384u + k * 32u;
-            mma_ss(tmem + TM_KQ, sdesc(kq + off, 16, 1024), sdesc(kq + off, 16, 1024), id_kq,
-                   (a | k) != 0);
+            const uint64_t d = sdesc_add(dkq, a * 16384u + k * 32u);
+            mma_ss(tmem + TM_KQ, d, d, id_kq, (a | k) != 0);
           }
         mma_commit(&bars[B_KQ_DONE]);
         if (!mbar_wait(&bars[B_P1_MID], c & 1, abort_flag, kWaitLimitNs)) {
@@ -420,10 +427,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         // W^T = K^T T_w^T : A = K^T (MN-major, d_k atoms 16 KB apart or the zero page)
         const uint32_t lbo_k = (L::NKA == 2) ? 16384u : (sbase + L::ZERO - kq);
+        const uint64_t dka = sdesc(kq, lbo_k, 1024), dtw = sdesc(sbase + L::TW, 16, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + TM_KQ, sdesc(kq + k * 2048u, lbo_k, 1024),
-                 sdesc(sbase + L::TW + k * 32u, 16, 1024), id_w, k != 0);
+          mma_ss(tmem + TM_KQ, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
         mma_commit(&bars[B_W_DONE]);
       }
       mma_commit(&bars[B_DRAIN1]);  // every MMA this thread issued has finished before exit
@@ -451,24 +458,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // U^T = V^T (T_b hi + lo)^T : A = V^T MN-major (d_v atoms 8 KB apart or the zero page).
         // State-independent: issued as soon as the chunk is prepared.
         const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
+        const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(tb, 16, 1024);
 #pragma unroll
         for (int half = 0; half < 2; ++half)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_R, sdesc(vv + k * 2048u, lbo_v, 1024),
-                   sdesc(tb + half * 8192u + k * 32u, 16, 1024), id_u, (half | k) != 0);
+            mma_ss(tmem + TM_R, sdesc_add(dva, k * 2048u), sdesc_add(dtb, half * 8192u + k * 32u), id_u,
+                   (half | k) != 0);
         if (!mbar_wait(&bars[B_S_READY], c & 1, abort_flag, kWaitLimitNs)) {
           fail(5);
           break;
         }
         tc_fence_after();
         // U'^T += (-S^T) W^T : A = -S^T K-major, B = W^T MN-major [d_k][j]
+        const uint64_t dsop = sdesc(sop, 16, 1024), dwt = sdesc(wt, 16, 1024);
 #pragma unroll
         for (int a = 0; a < L::NKA; ++a)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_R, sdesc(sop + a * 16384u + k * 32u, 16, 1024),
-                   sdesc(wt + (a * 4 + k) * 2048u, 16, 1024), id_sw, 1);
+            mma_ss(tmem + TM_R, sdesc_add(dsop, a * 16384u + k * 32u), sdesc_add(dwt, (a * 4 + k) * 2048u),
+                   id_sw, 1);
         mma_commit(&bars[B_UP_DONE]);
         // QS^T = (-S^T) Q^T (raw q tile, K-major), once the last epilogue has read its block
         if (c >= 1 && !mbar_wait(&bars[B_EPI_DONE], (c - 1) & 1, abort_flag, kWaitLimitNs)) {
@@ -476,12 +485,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
+        const uint64_t dq = sdesc(kq + 8192u, 16, 1024);
 #pragma unroll
         for (int a = 0; a < L::NKA; ++a)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_QS, sdesc(sop + a * 16384u + k * 32u, 16, 1024),
-                   sdesc(kq + a * 16384u + 8192u + k * 32u, 16, 1024), id_qs, (a | k) != 0);
+            mma_ss(tmem + TM_QS, sdesc_add(dsop, a * 16384u + k * 32u), sdesc_add(dq, a * 16384u + k * 32u),
+                   id_qs, (a | k) != 0);
         if (!mbar_wait(&bars[B_UOPS_READY], c & 1, abort_flag, kWaitLimitNs)) {
           fail(7);
           break;
@@ -489,18 +499,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         // S^T += (U' diag(s))^T K : A from TMEM (hi, then lo), B = K MN-major (N = d_k)
         const uint32_t lbo_kn = (L::NKA == 2) ? 16384u : 16u;
+        const uint64_t dkn = sdesc(kq, lbo_kn, 1024);
 #pragma unroll
         for (int half = 0; half < 2; ++half)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_S, tmem + (half ? TM_UL : TM_UH) + k * 8u,
-                   sdesc(kq + k * 2048u, lbo_kn, 1024), id_st, 1);
+            mma_ts(tmem + TM_S, tmem + (half ? TM_UL : TM_UH) + k * 8u, sdesc_add(dkn, k * 2048u), id_st, 1);
         mma_commit(&bars[B_STATE_DONE]);
         // O^T = U'^T P^T : A from TMEM (bf16 U'), B = P K-major [i][j]
-        const uint32_t pp = sbase + L::P0 + par * 8192u;
+        const uint64_t dpp = sdesc(sbase + L::P0 + par * 8192u, 16, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + TM_O, tmem + TM_UU + k * 8u, sdesc(pp + k * 32u, 16, 1024), id_pu, k != 0);
+          mma_ts(tmem + TM_O, tmem + TM_UU + k * 8u, sdesc_add(dpp, k * 32u), id_pu, k != 0);
         mma_commit(&bars[B_O_DONE]);
         mma_commit(&bars[B_EMPTY0 + s]);
       }
@@ -584,10 +594,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cs.cq[i] = -co * exp2f(Gl2i);
         if (i == 0) cs.eGC = exp2f(GCl2);
       }
-      if (krow) {
+      if (exact) {
+        // rare: every decay by its own exp (A and P rows into registers first)
+        float row[32];
+        exact_row(row, v, ps->r, sc + SC_G, Gl2i, ps->beta[i] * ps->r[i], 32 * hf, i, krow);
+        if (krow) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(&Abuf[i * LDF + 32 * hf + 4 * q]) =
+                make_float4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
+        } else {
+          const uint32_t prow = sbase + L_::P0 + par * 8192u;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_shared_v4(prow + sw128(i, 4 * hf + q), pack_bf16(row[8 * q], row[8 * q + 1]),
+                         pack_bf16(row[8 * q + 2], row[8 * q + 3]), pack_bf16(row[8 * q + 4], row[8 * q + 5]),
+                         pack_bf16(row[8 * q + 6], row[8 * q + 7]));
+        }
+      } else if (krow) {
         // A_ij = beta_i r_i r_j e^{G_i - G_j} k_i.k_j  (j < i), fp32 into the scratch
-        const float ci = ps->beta[i] * ps->r[i];
-        const float cia = ci * ai;
+        const float cia = ps->beta[i] * ps->r[i] * ai;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int j0 = 32 * hf + 4 * q;
@@ -595,15 +621,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
           float a4[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) a4[e] = (cia * __uint_as_float(v[4 * q + e])) * dd[e];
-          if (exact) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              a4[e] = ci * ps->r[j0 + e] * exp2f(Gl2i - sc[SC_G + j0 + e] * kLog2e) *
-                      __uint_as_float(v[4 * q + e]);
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) a4[e] = (j0 + e < i) ? a4[e] : 0.f;
+          for (int e = 0; e < 4; ++e)
+            a4[e] = (j0 + e < i) ? (cia * __uint_as_float(v[4 * q + e])) * dd[e] : 0.f;
           *reinterpret_cast<float4*>(&Abuf[i * LDF + j0]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
         }
       } else {
@@ -617,15 +636,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
           float pv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pv[e] = (ai * __uint_as_float(v[8 * q + e])) * dd[e];
-          if (exact) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              pv[e] = ps->r[j0 + e] * exp2f(Gl2i - sc[SC_G + j0 + e] * kLog2e) *
-                      __uint_as_float(v[8 * q + e]);
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) pv[e] = (j0 + e <= i) ? pv[e] : 0.f;
+          for (int e = 0; e < 8; ++e)
+            pv[e] = (j0 + e <= i) ? (ai * __uint_as_float(v[8 * q + e])) * dd[e] : 0.f;
           st_shared_v4(prow + sw128(i, 4 * hf + q), pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
                        pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
         }

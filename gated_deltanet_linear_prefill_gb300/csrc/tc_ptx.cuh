@@ -54,13 +54,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One bounded probe of the phase. The suspend-time hint lets the hardware park
+// the thread until the phase completes (or the hint runs out) instead of
+// returning at once, so waiting warps do not spin on the barrier.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t suspend_ns = 20000u) {
   uint32_t ok;
   asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
@@ -69,17 +73,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // *abort becomes non-zero (abort may be null: drain waits ignore it) or after
 // `limit_ns` of global time; returns false then (the caller reports the
 // timeout and unwinds).
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                          volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (abort && *abort) return false;
-      if (globaltimer() - t0 > limit_ns) return false;
-    }
-  }
+  return mbar_wait_slow(bar, parity, abort, limit_ns);
 }
 
 // ---------------------------------------------------------------- proxies / fences
@@ -130,6 +136,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   d |= 1ull << 46;
   d |= 2ull << 61;
   return d;
+}
+
+// A descriptor moved by `bytes` (a multiple of 16) along its start address; the
+// 14-bit address field cannot carry for shared-memory offsets below 256 KB.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) {
+  return d + (uint64_t)(bytes >> 4);
 }
 
 // kind::f16 instruction descriptor: bf16 x bf16 -> f32, M x N, majors
