@@ -31,6 +31,7 @@ GDN_BF16, GDN_F32 = 0, 1
 GDN_OK = 0
 GDN_FLAG_NO_L2NORM = 0x1
 GDN_FLAG_SIMT = 0x2
+GDN_NOALLOC_MAX_SEQS = 16384  # include/gdn.h
 STATUS_NAMES = ["GDN_OK", "GDN_ERR_NULL", "GDN_ERR_SHAPE", "GDN_ERR_DTYPE", "GDN_ERR_ALIGN",
                 "GDN_ERR_SEQLENS", "GDN_ERR_STATE_INDEX", "GDN_ERR_ALIAS", "GDN_ERR_WORKSPACE",
                 "GDN_ERR_ARCH", "GDN_ERR_CUDA", "GDN_ERR_DEVICE_TIMEOUT"]
@@ -94,6 +95,8 @@ def load_library(build_if_missing: bool = True):
         lib.gdn_workspace_bytes.restype = ctypes.c_size_t
         lib.gdn_prefill_varlen.argtypes = [P] * 10 + [ctypes.POINTER(GdnDesc), P]
         lib.gdn_prefill_varlen.restype = ctypes.c_int
+        lib.gdn_prefill_varlen_noalloc.argtypes = [P] * 10 + [ctypes.POINTER(GdnDesc), P]
+        lib.gdn_prefill_varlen_noalloc.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.POINTER(GdnDesc), P]
         lib.gdn_get_device_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -150,6 +153,17 @@ def gdn_prefill_varlen(q, k, v, g, beta, cu_seqlens, initial_state, state_index,
                                       _ptr(cu_seqlens), _ptr(initial_state), _ptr(state_index),
                                       _ptr(out), _ptr(final_state), ctypes.byref(desc),
                                       _stream_handle(stream)))
+
+
+def gdn_prefill_varlen_noalloc(q, k, v, g, beta, cu_seqlens, initial_state, state_index, out,
+                               final_state, desc: GdnDesc, stream=None) -> int:
+    """The C entry point that uses the library's static workspace (no
+    allocation; desc.workspace is ignored); returns the gdn_status code."""
+    lib = load_library()
+    return int(lib.gdn_prefill_varlen_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                              _ptr(cu_seqlens), _ptr(initial_state),
+                                              _ptr(state_index), _ptr(out), _ptr(final_state),
+                                              ctypes.byref(desc), _stream_handle(stream)))
 
 
 def gdn_get_device_status(desc: GdnDesc, stream=None) -> int:

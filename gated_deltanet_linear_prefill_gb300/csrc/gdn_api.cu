@@ -279,3 +279,57 @@ extern "C" gdn_status gdn_get_device_status(const gdn_desc* desc, void* stream) 
   if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
   return (gdn_status)code;
 }
+
+// ------------------------------------------------ variant without a workspace
+//
+// The workspace of gdn_prefill_varlen_noalloc: a status block and a work list
+// for GDN_NOALLOC_MAX_SEQS sequences, compiled in as static device memory (one
+// copy per device). The prep kernel of every call resets the status word and
+// rewrites the work list, so nothing here needs clearing between calls.
+namespace gdn {
+
+constexpr size_t kNoallocBytes = kOrderOffset + sizeof(int32_t) * (size_t)GDN_NOALLOC_MAX_SEQS;
+static_assert(kNoallocBytes % 256 == 0, "the work list ends on a 256-byte boundary");
+
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoallocBytes];
+
+// The device address of g_noalloc_workspace on the current device, looked up
+// once per device and kept.
+static gdn_status noalloc_workspace(void** addr) {
+  static std::mutex mu;
+  static void* cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return GDN_ERR_ARCH;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_noalloc_workspace) != cudaSuccess || !a) return GDN_ERR_CUDA;
+    cached[dev] = a;
+  }
+  *addr = cached[dev];
+  return GDN_OK;
+}
+
+}  // namespace gdn
+
+extern "C" gdn_status gdn_prefill_varlen_noalloc(const void* q, const void* k, const void* v,
+                                                 const void* g, const void* beta,
+                                                 const int32_t* cu_seqlens,
+                                                 const float* initial_state,
+                                                 const int32_t* state_index, void* out,
+                                                 float* final_state, const gdn_desc* desc,
+                                                 void* stream) {
+  if (!desc) return GDN_ERR_NULL;
+  if (desc->num_seqs > GDN_NOALLOC_MAX_SEQS) return GDN_ERR_WORKSPACE;
+  const gdn_status arch = check_arch();
+  if (arch != GDN_OK) return arch;
+  void* ws = nullptr;
+  const gdn_status st = noalloc_workspace(&ws);
+  if (st != GDN_OK) return st;
+  gdn_desc d = *desc;
+  d.workspace = ws;
+  d.workspace_bytes = kNoallocBytes;
+  return gdn_prefill_varlen(q, k, v, g, beta, cu_seqlens, initial_state, state_index, out,
+                            final_state, &d, stream);
+}

@@ -135,6 +135,59 @@ gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const
                               float* final_state, const gdn_desc* desc, void* stream);
 
 /*
+ * Largest num_seqs gdn_prefill_varlen_noalloc accepts. Its built-in scratch
+ * (the status word and the work list for this many sequences) takes
+ * 256 + 4 * GDN_NOALLOC_MAX_SEQS = 65,792 bytes of static device memory on
+ * each device the library is loaded on.
+ */
+#define GDN_NOALLOC_MAX_SEQS 16384
+
+/*
+ * gdn_prefill_varlen without a caller-supplied workspace. The method itself
+ * has no counterpart to this call: it is a convenience of this library.
+ *
+ * Who needs it: callers that cannot hand the library a device buffer, for
+ * example
+ *  - an operator or plug-in interface that passes only the operation's own
+ *    tensors and gives the operator no allocator and no state kept between
+ *    calls, so there is nowhere to keep a workspace;
+ *  - a serving process that reserves its device memory up front (states,
+ *    caches) and owns every later allocation through its own arena;
+ *  - code that must not call cudaMalloc or cudaFree on its critical path,
+ *    since those calls can synchronise the device and stall other streams.
+ *
+ * Arguments, layouts, results and host-side errors are those of
+ * gdn_prefill_varlen; desc->workspace and desc->workspace_bytes are ignored.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * call): the workspace is a fixed array compiled into the library as static
+ * device memory, one per device.
+ *
+ *  - Set-up: the first call on each device looks up that array's device
+ *    address (cudaGetSymbolAddress) and keeps it; GDN_ERR_CUDA if the lookup
+ *    fails. Make that first call on a device before any stream capture
+ *    starts. The kept address belongs to the device's primary context: after
+ *    cudaDeviceReset the call must not be used again in that process.
+ *  - Limit: num_seqs > GDN_NOALLOC_MAX_SEQS returns GDN_ERR_WORKSPACE before
+ *    anything is launched or written.
+ *  - Nothing to clear: every call's first kernel resets the status word and
+ *    rewrites the whole work list before the chunk kernel reads them.
+ *  - One array per device, shared by every call on it: calls whose work can
+ *    overlap on the device (different streams, or host threads whose streams
+ *    are not ordered by events) race on it, and their outputs are then
+ *    unspecified. Issue such calls on one stream, or order them.
+ *  - The device status word of this call lives in that array, and no entry
+ *    point reads it back: device-detected errors (GDN_ERR_SEQLENS,
+ *    GDN_ERR_STATE_INDEX, GDN_ERR_DEVICE_TIMEOUT) leave the outputs
+ *    unspecified without being reported. Callers that need them should use
+ *    gdn_prefill_varlen with their own workspace.
+ */
+gdn_status gdn_prefill_varlen_noalloc(const void* q, const void* k, const void* v,
+                                      const void* g, const void* beta,
+                                      const int32_t* cu_seqlens, const float* initial_state,
+                                      const int32_t* state_index, void* out, float* final_state,
+                                      const gdn_desc* desc, void* stream);
+
+/*
  * Synchronises `stream`, then returns the device status word the last call on
  * this workspace left (GDN_OK if the device found nothing), or GDN_ERR_CUDA if
  * the synchronisation or the read failed.

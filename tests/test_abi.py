@@ -28,8 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
-        "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_get_device_status",
-        "gdn_status_string"])
+        "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_prefill_varlen_noalloc",
+        "gdn_get_device_status", "gdn_status_string"])
 
 
 def test_library_exports_every_declared_symbol():
