@@ -266,6 +266,11 @@ def run_gdn(args, world, rank, local):
     torch.cuda.set_device(device)
     gdn.load_library()
     w = workloads.config(CONFIG_INDEX, seed_offset=rank)
+    workload_name = workloads.CONFIG_NAMES[CONFIG_INDEX]
+    if args.subset_seqs > 0:
+        # a smaller case of the same batch (profiling captures): its first K sequences
+        w = workloads.subset_sequences(w, range(min(args.subset_seqs, w.num_seqs)))
+        workload_name += f"_first{args.subset_seqs}"
     flags = gdn.GDN_FLAG_SIMT if args.kernel == "simt" else 0
     d = w.to(device)
     out = torch.empty(d.v.shape, dtype=d.out_dtype, device=device)
@@ -352,16 +357,16 @@ def run_gdn(args, world, rank, local):
     hbm_peak, tc_peak, peak_kind = measured_peaks()
     B = algorithmic_bytes(w)
     F = chunked_tensor_flops(w)
-    step_s = statistics.median(times) / 1e3
+    step_s = sum(times) / len(times) / 1e3  # mean launch duration over the timed region
     achieved = B / step_s / 1e9
     kernel_name = "gdn_tc_kernel" if args.kernel == "tc" else "gdn_simt_kernel"
-    traffic = profiled_traffic(kernel_name, workloads.CONFIG_NAMES[CONFIG_INDEX])
+    traffic = profiled_traffic(kernel_name, workload_name)
     roofline_time = max(B / (hbm_peak * 1e9), F / (tc_peak * 1e12))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workloads.CONFIG_NAMES[CONFIG_INDEX], "num_seqs": w.num_seqs,
+        "config": {"workload": workload_name, "num_seqs": w.num_seqs,
                    "total_tokens": w.total_tokens, "max_seqlen": w.max_seqlen, "h_qk": w.h_qk,
                    "h_v": w.h_v, "d_k": w.d_k, "d_v": w.d_v, "chunk": 64,
                    "gates": "fp32", "out": "bf16", "state": "fp32", "kernel": args.kernel,
@@ -403,6 +408,8 @@ def main(argv=None):
     ap.add_argument("--kernel", choices=["tc", "simt"], default="tc")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer timing")
+    ap.add_argument("--subset-seqs", type=int, default=0,
+                    help="time only the first K sequences of the batch (small profiling case)")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="seconds of untimed steps while the clock sampler warms up")
     args = ap.parse_args(argv)

@@ -11,6 +11,9 @@ for the fp32 SIMT kernel.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -60,6 +63,10 @@ def errors(o, s, o_ref, s_ref):
 
 def check(e, kernel="tc", f32_out=False, label=""):
     tol = TOL_SIMT_F32_OUT if (kernel == "simt" and f32_out) else TOL[kernel]
+    log = os.environ.get("GDN_PARITY_LOG")
+    if log:  # one JSON line per comparison, for a table of measured errors
+        with open(log, "a") as f:
+            f.write(json.dumps({"label": label, "kernel": kernel, "tol": tol, **e}) + "\n")
     assert e["nan_o"] == 0 and e["nan_s"] == 0, (label, e)
     assert e["max_abs"] <= tol[0], (label, e)
     assert e["mean_abs"] <= tol[1], (label, e)
