@@ -127,36 +127,57 @@ struct Tmaps {
 
 // Exact-decay fallback for a chunk whose log-decay spans more than
 // kMaxDecaySpan (the factorised e^{G_i - G_j} = a_i b_j could leave fp32
-// range): 32 entries of one A row (krow) or P row, each decay by its own exp.
-// Kept out of line: it is rare and its code would crowd the hot loop.
-__device__ __noinline__ void exact_row(float* out, const uint32_t* v, const float* r, const float* G,
-                                       float Gl2i, float ci, int j0, int i, int krow) {
+// range): the 32 weights of one A row (krow) or P row, each decay by its own
+// exp; the caller multiplies them by the K K^T / Q K^T entries. Kept out of
+// line: it is rare and its code would crowd the hot loop. It sees only its
+// own output array, so the caller's TMEM values stay in registers.
+__device__ __noinline__ void exact_row(float* out, const float* r, const float* G, float Gl2i,
+                                       float ci, int j0, int i, int krow) {
   for (int e = 0; e < 32; ++e) {
     const int j = j0 + e;
-    const float x = r[j] * exp2f(Gl2i - G[j] * 1.4426950408889634f) * __uint_as_float(v[e]);
+    const float x = r[j] * exp2f(Gl2i - G[j] * 1.4426950408889634f);
     out[e] = krow ? ((j < i) ? ci * x : 0.f) : ((j <= i) ? x : 0.f);
   }
 }
 
 // ---------------------------------------------------------------- the solve
-// C[16 x 8] += X[16 x 16 block at (xr, xc)] * Y[16 x 8 block at (yr, yc)] in
-// fp32 FMA, fp32 smem with row stride LDF. Lane (g, t) = (lane / 4, lane % 4)
-// owns rows g, g + 8 and columns 2t, 2t + 1; all operand loads are issued up
-// front so the four accumulation chains run back to back.
-__device__ __forceinline__ void fma_tile16(const float* X, int xr, int xc, const float* Y, int yr, int yc,
-                                           float (&c)[4], int lane) {
+// Warp-level tensor-core tiles for the block merges: mma.sync m16n8k8 with
+// tf32 operands, each fp32 operand split as hi + lo (both tf32) and the
+// product taken as hi*hi + hi*lo + lo*hi, which keeps close to fp32 accuracy.
+// Fragment layout (lane = 4 g + t): A rows g, g+8 x columns t, t+4; B rows
+// t, t+4 x column g; C rows g, g+8 x columns 2t, 2t+1.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// c[16 x 8] += X[xr.., xc + k) * Y[yr + k, yc..) over k in [0, 8 nk8), fp32 smem with row
+// stride LDF.
+__device__ __forceinline__ void mma_tile(const float* X, int xr, int xc, const float* Y, int yr,
+                                         int yc, int nk8, float (&c)[4], int lane) {
   const int g = lane >> 2, t = lane & 3;
-  const float* xr0 = X + (xr + g) * LDF + xc;
-  const float* xr1 = xr0 + 8 * LDF;
-  const float* yr0 = Y + yr * LDF + yc + 2 * t;
-#pragma unroll 4
-  for (int k = 0; k < 16; ++k) {
-    const float a0 = xr0[k], a1 = xr1[k];
-    const float2 b = *reinterpret_cast<const float2*>(yr0 + k * LDF);
-    c[0] = fmaf(a0, b.x, c[0]);
-    c[1] = fmaf(a0, b.y, c[1]);
-    c[2] = fmaf(a1, b.x, c[2]);
-    c[3] = fmaf(a1, b.y, c[3]);
+  const float* x0 = X + (xr + g) * LDF + xc + t;
+  const float* x1 = x0 + 8 * LDF;
+  const float* y0 = Y + (yr + t) * LDF + yc + g;
+  for (int k = 0; k < nk8; ++k) {
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    split_tf32(x0[8 * k], ah[0], al[0]);
+    split_tf32(x1[8 * k], ah[1], al[1]);
+    split_tf32(x0[8 * k + 4], ah[2], al[2]);
+    split_tf32(x1[8 * k + 4], ah[3], al[3]);
+    split_tf32(y0[8 * k * LDF], bh[0], bl[0]);
+    split_tf32(y0[(8 * k + 4) * LDF], bh[1], bl[1]);
+    mma_tf32(c, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+    mma_tf32(c, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+    mma_tf32(c, al[0], al[1], al[2], al[3], bh[0], bh[1]);
   }
 }
 __device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float (&c)[4], float sgn,
@@ -166,63 +187,72 @@ __device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float
   *reinterpret_cast<float2*>(&M[(r0 + g + 8) * LDF + c0 + 2 * t]) = make_float2(sgn * c[2], sgn * c[3]);
 }
 
-// T = (I + A)^-1 for the strictly-lower 64x64 A (fp32, stride LDF), by 16x16
-// blocks: the four diagonal blocks D_b by right-looking elimination (once
-// t_x is final, every later row of the column is updated at once), the two
-// 16-row merges T_{b+1,b} = -D_{b+1} A_{b+1,b} D_b inside each 32x32 diagonal
-// block, then T_21 = -T_22 (A_21 T_11) for the lower-left 32x32 block. All in
-// fp32. Blocks above the diagonal are not written. 256 threads (8 warps);
-// every merge product is split into 8-column halves.
+// T = (I + A)^-1 for the strictly-lower 64x64 A (fp32, stride LDF), in 16x16
+// blocks (the blocked order of the open-jev-fast README's GDN kernel):
+//  1. the four diagonal blocks D_b by forward substitution, one column per
+//     lane, each row of A read as float4 broadcasts;
+//  2. T_{b+1,b} = -D_{b+1} (A_{b+1,b} D_b) inside both 32x32 diagonal blocks;
+//  3. T_21 = -T_22 (A_21 T_11) for the lower-left 32x32 block.
+// Steps 2 and 3 run on the warp-level tensor cores (three-term tf32). Their
+// intermediate products are parked in T's upper triangle, which nothing reads
+// as T. Blocks above the diagonal are not otherwise written. 256 threads
+// (8 warps); ends with every T entry visible to all of them.
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ T,
                                                  int wa) {
   const int wq = wa >> 5, ln = wa & 31;
   if (wq < 4 && ln < 16) {
-    const int b = wq * 16, l = ln;  // lane l owns column l of D_wq
+    const int b = 16 * wq, l = ln;  // lane l owns column l of D_wq
     float t[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) t[i] = (i == l) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) {
+      const float* row = A + (b + i) * LDF + b;
+      float acc = (i == l) ? 1.f : 0.f;
 #pragma unroll
-    for (int x = 0; x < 15; ++x) {
-      const float tx = t[x];
-#pragma unroll
-      for (int i = x + 1; i < 16; ++i) t[i] = fmaf(-A[(b + i) * LDF + b + x], tx, t[i]);
+      for (int x4 = 0; x4 < i; x4 += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(row + x4);
+        acc = fmaf(-a4.x, t[x4], acc);
+        if (x4 + 1 < i) acc = fmaf(-a4.y, t[x4 + 1], acc);
+        if (x4 + 2 < i) acc = fmaf(-a4.z, t[x4 + 2], acc);
+        if (x4 + 3 < i) acc = fmaf(-a4.w, t[x4 + 3], acc);
+      }
+      t[i] = acc;
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) T[(b + i) * LDF + b + l] = t[i];
   }
   named_bar_sync(1, 256);
-  // Both merge levels as "C = X * Y over a run of 16-wide k blocks, then
-  // store" steps; a warp computes 8 columns of one 16x16 output block. One
-  // tile routine serves all of them through short runtime loops.
-  for (int lvl = 0; lvl < 2; ++lvl) {
-    // level 0: T_{2k+1,2k} = -D_{2k+1} (A_{2k+1,2k} D_{2k}), warps 0-3
-    // level 1: T_{rb,cb} = -T_22 (A_21 T_11) blocks, all 8 warps
-    const bool active = lvl == 1 || wq < 4;
-    int rb, cb, cc;
-    if (lvl == 0) {
-      rb = 2 * (wq >> 1) + 1;
-      cb = 2 * (wq >> 1);
-    } else {
-      rb = 2 + (wq >> 2);
-      cb = (wq >> 1) & 1;
-    }
-    cc = 8 * (wq & 1);
-    // X = A[rb, k0..k1) T[k0..k1, cb]; level 0: k = cb only; level 1: k = cb..1
-    const int xk0 = cb, xk1 = lvl == 0 ? cb + 1 : 2;
+  // step 2: warp wq < 4 takes pair p = wq >> 1 (b = 32 p), columns 8 h of the 16-wide block
+  const int h = wq & 1;
+  if (wq < 4) {
+    const int b = 32 * (wq >> 1);
     float c[4] = {};
-    if (active)
-      for (int kb = xk0; kb < xk1; ++kb) fma_tile16(A, 16 * rb, 16 * kb, T, 16 * kb, 16 * cb + cc, c, ln);
-    if (active) store_tile(T, 16 * rb, 16 * cb + cc, c, 1.f, ln);
-    named_bar_sync(1, 256);
-    // Y = T[rb, k0..k1) X[k0..k1, cb]; level 0: k = rb (D_rb); level 1: k = 2..rb (T_22)
-    const int yk0 = lvl == 0 ? rb : 2, yk1 = rb + 1;
-    float y[4] = {};
-    if (active)
-      for (int kb = yk0; kb < yk1; ++kb) fma_tile16(T, 16 * rb, 16 * kb, T, 16 * kb, 16 * cb + cc, y, ln);
-    named_bar_sync(1, 256);
-    if (active) store_tile(T, 16 * rb, 16 * cb + cc, y, -1.f, ln);
-    named_bar_sync(1, 256);
+    mma_tile(A, b + 16, b, T, b, b + 8 * h, 2, c, ln);  // A_{b+1,b} D_b
+    store_tile(T, b, b + 16 + 8 * h, c, 1.f, ln);       // parked in block (b, b+1)
   }
+  named_bar_sync(1, 256);
+  if (wq < 4) {
+    const int b = 32 * (wq >> 1);
+    float c[4] = {};
+    mma_tile(T, b + 16, b + 16, T, b, b + 16 + 8 * h, 2, c, ln);  // D_{b+1} X
+    store_tile(T, b + 16, b + 8 * h, c, -1.f, ln);
+  }
+  named_bar_sync(1, 256);
+  // step 3: warp wq -> output block (rb, cb) = (2 + (wq >> 2), (wq >> 1) & 1), columns 8 h
+  const int rb = 2 + (wq >> 2), cb = (wq >> 1) & 1;
+  {
+    float c[4] = {};
+    // X = A_{rb, cb..1} T_{cb..1, cb}  (T_11 is lower triangular)
+    mma_tile(A, 16 * rb, 16 * cb, T, 16 * cb, 16 * cb + 8 * h, 2 * (2 - cb), c, ln);
+    store_tile(T, 16 * (rb - 2), 32 + 16 * cb + 8 * h, c, 1.f, ln);  // parked in the upper right
+  }
+  named_bar_sync(1, 256);
+  {
+    float c[4] = {};
+    // T_{rb,cb} = -T_{rb, 2..rb} X_{2..rb, cb}
+    mma_tile(T, 16 * rb, 32, T, 0, 32 + 16 * cb + 8 * h, 2 * (rb - 1), c, ln);
+    store_tile(T, 16 * rb, 16 * cb + 8 * h, c, -1.f, ln);
+  }
+  named_bar_sync(1, 256);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -597,7 +627,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (exact) {
         // rare: every decay by its own exp (A and P rows into registers first)
         float row[32];
-        exact_row(row, v, ps->r, sc + SC_G, Gl2i, ps->beta[i] * ps->r[i], 32 * hf, i, krow);
+        {
+          float wgt[32];
+          exact_row(wgt, ps->r, sc + SC_G, Gl2i, ps->beta[i] * ps->r[i], 32 * hf, i, krow);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) row[e] = wgt[e] * __uint_as_float(v[e]);
+        }
         if (krow) {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
