@@ -1,40 +1,46 @@
 // Tensor-core (tcgen05 / TMEM / TMA) kernel for the chunked gated delta rule.
 //
-// Chunked form (open-jev-fast README, Phase 3 item 1: per 64-token chunk the
-// gate cumsum, K K^T, the (I + A)^-1 solve, u and w, the chunk output and the
-// state update; the cost is per chunk). With S the d_k x d_v state entering a
-// chunk of m <= 64 rows, G_i = sum_{s<=i} g_s, r^k_i / r^q_i the L2-norm
-// scales of k_i / q_i:
+// Chunked form (open-jev-fast README, Phase 3 item 1: per chunk the gate
+// cumsum, K K^T, the (I + A)^-1 solve, u and w, the chunk output and the state
+// update). With S the d_k x d_v state entering a chunk of m <= 64 rows,
+// G_i = sum_{s<=i} g_s (G_m: the whole chunk), r^k_i / r^q_i the L2-norm
+// scales of k_i / q_i, and M_ij = q_i.k_j for j <= i (0 above):
 //
 //   A_ij = beta_i r^k_i r^k_j e^{G_i-G_j} k_i.k_j   (j < i)     T = (I + A)^-1
 //   U  = T diag(beta) V               W = T diag(beta e^G r^k) K
-//   U' = U - W S
-//   o_i = scale r^q_i ( e^{G_i} S^T q_i + sum_{j<=i} e^{G_i-G_j} r^k_j (q_i.k_j) u'_j )
-//   S  <- e^{G_m} S + sum_j (e^{G_m-G_j} r^k_j) k_j u'_j^T
+//   U' = U - W S                      s_j = e^{G_m-G_j} r^k_j
+//   o_i = scale r^q_i e^{G_i-G_m} ( e^{G_m} S^T q_i + sum_j s_j u'_j M_ij )
+//   S  <- e^{G_m} S + sum_j s_j k_j u'_j^T
+//
+// The stored state is S~ = S / mu. A chunk's decay e^{G_m} is folded into the
+// operand scalars (lambda = mu e^{G_m} becomes the new mu) and only applied to
+// the stored state when |log lambda| would pass kMaxLogScale, so the state is
+// not rewritten every chunk. A chunk ends early when the log-decay inside it
+// spans more than kMaxSpan, which keeps every factorised exponential in fp32
+// range for any finite gate.
 //
 // One CTA owns one (sequence, value head) chain and walks its chunks in order.
 // All dense products run on tcgen05 in the "d-major" orientation, where the
 // 128 TMEM lanes index d_v (or d_k) so every MMA has M = 128:
-//   [K;Q] K^T          -> KK^T (lanes 0-63), QK^T (lanes 64-127)       (per chunk)
-//   W^T  = K^T T_w^T    (T_w = T diag(beta e^G r^k), bf16)
-//   U'^T = V^T T_b^T (T_b = T diag(beta) as bf16 hi + lo) - S^T W^T
-//   QS^T = -S^T Q^T                 (the inter-chunk term, weighted by e^{G_i} at the end)
-//   O^T  = U'^T P^T                 (P_ij = e^{G_i-G_j} r^k_j q_i.k_j, j <= i)
-//   S^T += (U' diag(s))^T K         (s_j = e^{G_m-G_j} r^k_j; U' diag(s) as bf16 hi + lo,
-//                                    read by the MMA straight from TMEM)
-// Operand precision: the products feeding the fp32 state carry T and U' as
-// bf16 hi + lo pairs (about 16 significant bits); S and W enter as bf16; every
-// accumulation is fp32 in TMEM. Decays, norms and the 64x64 unit-lower-
-// triangular inverse (16x16 blocks merged level by level, the blocked order
-// the open-jev-fast README's GDN kernel also uses) run on CUDA cores in fp32.
+//   [K;Q] K^T                    KK^T (lanes 0-63) and QK^T (lanes 64-127)
+//   W'^T  = K^T T_w^T            T_w = -nu T diag(beta e^G r^k), bf16
+//   U'^T  = V^T T_b^T + S~^T W'^T   T_b = T diag(beta) as bf16 hi + lo
+//   O^T   = S~^T Q^T + (U' diag(s/lambda))^T M^T
+//   S~^T += (U' diag(s/lambda))^T K
+// S~^T and U' diag(s/lambda) (bf16 hi + lo) are A operands read straight from
+// TMEM. Operand precision: T and U' s carry about 16 significant bits (hi +
+// lo); S~ and W enter as bf16; every accumulation is fp32. Decays, norms and
+// the 64x64 unit-lower-triangular inverse run on CUDA cores in fp32, the
+// inverse's block merges on the warp-level tensor cores (three-term tf32).
 //
-// Warp roles (512 threads): warp 0 loads K/Q/V tiles by TMA (128-byte swizzle),
-// clears rows past the sequence end and scans the gates; warp 1 allocates TMEM and issues the state-independent MMAs;
-// warp 2 issues the state-dependent MMAs; warps 4-11 (WG-A) prepare chunk c+1
-// (norms, A and P, the solve, T_b / T_w, W^T) while warps 12-15 (WG-B) run
-// chunk c's state step (S -> bf16 operand, U' split, output epilogue). Every
-// mbarrier wait is bounded: on timeout the CTA reports GDN_ERR_DEVICE_TIMEOUT
-// and unwinds.
+// Warp roles (512 threads): warp 0 scans the gates, sizes the chunks and loads
+// K/Q/V tiles by TMA (128-byte swizzle) into a 3-deep K/Q ring and a 2-deep V
+// ring; warp 1 allocates TMEM and issues [K;Q] K^T; warp 2 issues the
+// state-dependent MMAs; warp 3 takes the q norms; warps 4-11 (WG-A) prepare
+// chunk c+1 (k norms, A and M, the solve, T_b / T_w, the W and U products)
+// while warps 12-15 (WG-B) run chunk c's state step (U' split, S~ -> bf16
+// operand, output epilogue). Every mbarrier wait is bounded: on timeout the
+// CTA reports GDN_ERR_DEVICE_TIMEOUT and unwinds.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -48,46 +54,64 @@ using namespace ptx;
 
 constexpr int kTcThreads = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait: far above any legal wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMaxSpan = 30.0f;      // largest log-decay span inside one chunk
+constexpr float kMaxLogScale = 50.0f;  // largest |log mu| of the stored state
 
 // TMEM columns (fp32 unless noted)
-constexpr uint32_t TM_S = 0;     // S^T: lanes d_v, columns d_k            (128)
-constexpr uint32_t TM_R = 128;   // U^T, then U'^T: lanes d_v, columns j    (64)
-constexpr uint32_t TM_O = 192;   // O^T: lanes d_v, columns i               (64)
-constexpr uint32_t TM_KQ = 256;  // [K;Q] K^T, then W^T                     (64)
-constexpr uint32_t TM_UH = 320;  // (U' diag(s))^T hi, packed bf16 pairs    (32)
-constexpr uint32_t TM_UL = 352;  // (U' diag(s))^T lo                       (32)
-constexpr uint32_t TM_UU = 384;  // U'^T as bf16                            (32)
-constexpr uint32_t TM_QS = 448;  // -S^T Q^T: lanes d_v, columns i          (64)
+constexpr uint32_t TM_S = 0;     // S~^T: lanes d_v, columns d_k             (128)
+constexpr uint32_t TM_KQ = 128;  // [K;Q] K^T                                 (64)
+constexpr uint32_t TM_W = 192;   // W'^T: lanes d_k, columns j                (64)
+constexpr uint32_t TM_R = 256;   // U^T, then U'^T: lanes d_v, columns j      (64)
+constexpr uint32_t TM_O = 320;   // O^T: lanes d_v, columns i                 (64)
+constexpr uint32_t TM_UH = 384;  // (U' diag(s/lambda))^T hi, packed bf16     (32)
+constexpr uint32_t TM_UL = 416;  // (U' diag(s/lambda))^T lo                  (32)
+constexpr uint32_t TM_SB = 448;  // S~^T as packed bf16                       (64)
 constexpr uint32_t kTmemCols = 512;
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMaxDecaySpan = 80.0f;  // chunks whose log-decay spans more use exact exps
-
-// Barrier indices
+// Barrier indices (arrival count 1 each)
 enum {
-  B_TMA0 = 0, B_TMA1, B_READY0, B_READY1, B_EMPTY0, B_EMPTY1, B_KQ_DONE, B_P1_MID, B_W_DONE,
-  B_KQ_FREE, B_P1_DONE0, B_P1_DONE1, B_CS_FREE0, B_CS_FREE1, B_CS_FREE2, B_S_READY, B_UP_DONE,
-  B_UOPS_READY, B_O_DONE, B_STATE_DONE, B_EPI_DONE, B_DRAIN1, B_DRAIN2, kNumBars
+  B_FULL0 = 0, B_FULL1, B_FULL2,  // chunk tiles + gate scalars landed (slot c % 3)
+  B_KQE0, B_KQE1, B_KQE2,         // K/Q slot released (chunk c's last MMA done)
+  B_VE0, B_VE1,                   // V slot released (slot c % 2)
+  B_RQ0, B_RQ1, B_RQ2,            // q norms of slot c % 3 written
+  B_KQ_DONE, B_KQ_FREE, B_W_DONE, B_R_FREE,
+  B_P1_DONE0, B_P1_DONE1,         // chunk prepared (c % 2)
+  B_S_READY, B_UP_DONE, B_WFREE0, B_WFREE1, B_UOPS_READY, B_STATE_DONE, B_O_DONE, B_EPI_DONE,
+  B_MFREE0, B_MFREE1, B_CSF0, B_CSF1, B_CSF2,
+  B_DRAIN1, B_DRAIN2, B_DRAINA, kNumBars
 };
 
-// Per-chunk values WG-A hands to WG-B (three buffers, indexed by chunk % 3).
+// Gate scalars the producer writes next to each K/Q slot (floats).
+constexpr int SC_G = 0;        // G_i (rows past m repeat G_{m-1})
+constexpr int SC_B = 64;       // beta_i (0 past m)
+constexpr int SC_RQ = 128;     // r^q_i (written by warp 3)
+constexpr int SC_GMAX = 192;   // max / min of G over the chunk's rows
+constexpr int SC_GMIN = 193;
+constexpr int SC_GM = 194;     // G_m
+constexpr int SC_LAMLOG = 195; // log lambda used by s and the output weights (0 when eager)
+constexpr int SC_NULOG = 196;  // log of the W' weight applied to e^{G_j}
+constexpr int SC_RMW = 197;    // factor applied to the stored state first (1 unless eager)
+constexpr int SC_MUNEXT = 198; // mu after this chunk
+constexpr int SC_M = 199;      // rows (int)
+constexpr int SC_FLAGS = 200;  // bit 0: last chunk of the sequence; bit 1: eager
+constexpr int SC_T0 = 202;     // first row (int64, two words)
+
+// Per-chunk values WG-A hands to WG-B (three buffers, chunk % 3).
 struct ChunkScalars {
-  float cq[64];  // -scale r^q_i e^{G_i}: weight of the (-S^T q_i) column
-  float co[64];  // scale r^q_i: weight of the intra-chunk column
-  float s[64];   // e^{G_m - G_j} r^k_j: state-update weight of row j
-  float eGC;     // e^{G_m}: decay of the whole chunk
-  int pad[31];
+  float co[64];  // scale r^q_i e^{G_i - G_m} lambda: output weight of row i (0 past m)
+  float s[64];   // e^{G_m - G_j} r^k_j / lambda: weight of u'_j (0 past m)
+  long long t0;  // first row of the chunk
+  float mu_next; // mu after the chunk
+  int m, last, pad[3];
 };
 // WG-A private per-chunk values.
 struct PrepScalars {
   float d[64];     // r^k_j e^{Gmax - G_j}
   float r[64];     // r^k_j
-  float tw[64];    // beta_j e^{G_j} r^k_j: column scale of T_w
+  float tw[64];    // column scale of T_w
   float beta[64];
 };
-// Stage scalars: G[64], beta[64], Gmax, Gmin written by the producer; WG-A
-// parks half-row partial sums of |q_i|^2 in [SC_QSS, SC_QSS + 64).
-constexpr int SC_G = 0, SC_B = 64, SC_QSS = 128, SC_GMAX = 192, SC_GMIN = 193;
 
 constexpr int LDF = 68;  // row stride (floats) of the fp32 64x64 scratch of the solve
 
@@ -96,49 +120,33 @@ template <int DK, int DV>
 struct TcLayout {
   static constexpr int NKA = DK / 64;  // 64-element atom columns of K / Q
   static constexpr int NVA = DV / 64;
-  static constexpr uint32_t KQ_BYTES = NKA * 16384u;  // [K ac][Q ac] per atom column
-  static constexpr uint32_t V_BYTES = NVA * 8192u;
+  static constexpr uint32_t KQ_BYTES = NKA * 16384u;  // [K atom][Q atom] per atom column
   static constexpr uint32_t SCAL_BYTES = 1024u;
-  static constexpr uint32_t STAGE_BYTES = KQ_BYTES + V_BYTES + SCAL_BYTES;
-  static constexpr uint32_t STAGE0 = 0;
+  static constexpr uint32_t SLOT_BYTES = KQ_BYTES + SCAL_BYTES;
+  static constexpr uint32_t V_BYTES = NVA * 8192u;
   static constexpr uint32_t SCR_BYTES = 17408u;           // 64 x 68 fp32, 1024-aligned size
-  static constexpr uint32_t P0 = 2 * STAGE_BYTES;         // P (bf16 64x64) x2
-  static constexpr uint32_t TB0 = P0 + 2 * 8192u;         // T_b hi/lo (or fp32 T) x2
-  static constexpr uint32_t TW = TB0 + 2 * SCR_BYTES;     // T_w bf16
-  static constexpr uint32_t WT0 = TW + 8192u;             // W^T bf16 128x64 (or fp32 A) x2
-  static constexpr uint32_t SOP = WT0 + 2 * SCR_BYTES;    // -S^T bf16 [128][DK]; output staging
-  static constexpr uint32_t SOP_BYTES =
-      (NKA * 16384u > 64u * DV * 4u) ? NKA * 16384u : 64u * DV * 4u;
+  static constexpr uint32_t RING0 = 0;                     // K/Q slots x3
+  static constexpr uint32_t V0 = 3 * SLOT_BYTES;           // V slots x2
+  static constexpr uint32_t M0 = V0 + 2 * V_BYTES;         // M (bf16 64x64) x2; output staging
+  static constexpr uint32_t TB = M0 + 2 * 8192u;           // fp32 T, then T_b hi / lo
+  static constexpr uint32_t TW = TB + SCR_BYTES;           // T_w bf16
+  static constexpr uint32_t WT0 = TW + 8192u;              // fp32 A, then W'^T bf16, x2
   static constexpr bool NEED_ZERO = (DK == 64) || (DV == 64);
-  static constexpr uint32_t ZERO = SOP + SOP_BYTES;       // 8 KB of zeros (M padding)
+  static constexpr uint32_t ZERO = WT0 + 2 * SCR_BYTES;   // 8 KB of zeros (M padding)
   static constexpr uint32_t CS0 = ZERO + (NEED_ZERO ? 8192u : 0u);
   static constexpr uint32_t PS = CS0 + 3 * (uint32_t)sizeof(ChunkScalars);
   static constexpr uint32_t BARS = PS + (uint32_t)sizeof(PrepScalars);
   static constexpr uint32_t MISC = BARS + kNumBars * 8u;  // tmem base, abort flag
   static constexpr uint32_t TOTAL = MISC + 64u;
   static constexpr uint32_t DYN_SMEM = TOTAL + 1024u;     // alignment slack
-  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(SLOT_BYTES % 1024 == 0, "slot alignment");
+  static_assert(sizeof(ChunkScalars) % 16 == 0, "chunk scalars alignment");
   static_assert(DYN_SMEM <= 232448u, "shared memory budget");
 };
 
 struct Tmaps {
   CUtensorMap q, k, v;
 };
-
-// Exact-decay fallback for a chunk whose log-decay spans more than
-// kMaxDecaySpan (the factorised e^{G_i - G_j} = a_i b_j could leave fp32
-// range): the 32 weights of one A row (krow) or P row, each decay by its own
-// exp; the caller multiplies them by the K K^T / Q K^T entries. Kept out of
-// line: it is rare and its code would crowd the hot loop. It sees only its
-// own output array, so the caller's TMEM values stay in registers.
-__device__ __noinline__ void exact_row(float* out, const float* r, const float* G, float Gl2i,
-                                       float ci, int j0, int i, int krow) {
-  for (int e = 0; e < 32; ++e) {
-    const int j = j0 + e;
-    const float x = r[j] * exp2f(Gl2i - G[j] * 1.4426950408889634f);
-    out[e] = krow ? ((j < i) ? ci * x : 0.f) : ((j <= i) ? x : 0.f);
-  }
-}
 
 // ---------------------------------------------------------------- the solve
 // Warp-level tensor-core tiles for the block merges: mma.sync m16n8k8 with
@@ -167,6 +175,7 @@ __device__ __forceinline__ void mma_tile(const float* X, int xr, int xc, const f
   const float* x0 = X + (xr + g) * LDF + xc + t;
   const float* x1 = x0 + 8 * LDF;
   const float* y0 = Y + (yr + t) * LDF + yc + g;
+#pragma unroll 1
   for (int k = 0; k < nk8; ++k) {
     uint32_t ah[4], al[4], bh[2], bl[2];
     split_tf32(x0[8 * k], ah[0], al[0]);
@@ -221,38 +230,73 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, fl
     for (int i = 0; i < 16; ++i) T[(b + i) * LDF + b + l] = t[i];
   }
   named_bar_sync(1, 256);
-  // step 2: warp wq < 4 takes pair p = wq >> 1 (b = 32 p), columns 8 h of the 16-wide block
-  const int h = wq & 1;
-  if (wq < 4) {
-    const int b = 32 * (wq >> 1);
-    float c[4] = {};
-    mma_tile(A, b + 16, b, T, b, b + 8 * h, 2, c, ln);  // A_{b+1,b} D_b
-    store_tile(T, b, b + 16 + 8 * h, c, 1.f, ln);       // parked in block (b, b+1)
+  // Steps 2 and 3 as four passes of "c = X * Y over nk8 k-steps, store +-c",
+  // one tile per warp (warps 4-7 sit out the two step-2 passes):
+  //   pass 0: A_{b+1,b} D_b                      -> parked in block (b, b+1)
+  //   pass 1: -D_{b+1} (pass 0)                  -> T_{b+1,b}
+  //   pass 2: A_{rb, cb..1} T_{cb..1, cb}        -> parked in the upper right
+  //   pass 3: -T_{rb, 2..rb} (pass 2)            -> T_{rb,cb}
+  // with b = 32 (wq >> 1) in step 2 and (rb, cb) = (2 + (wq >> 2), (wq >> 1) & 1) in step 3.
+  const int h8 = 8 * (wq & 1);
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const bool step2 = pass < 2;
+    if (!step2 || wq < 4) {
+      const int b = 32 * (wq >> 1), rb = 2 + (wq >> 2), cb = (wq >> 1) & 1;
+      const float* X;
+      const float* Y;
+      int xr, xc, yr, yc, nk8, sr, sc;
+      float sgn;
+      if (pass == 0) {
+        X = A; xr = b + 16; xc = b; Y = T; yr = b; yc = b + h8; nk8 = 2; sr = b; sc = b + 16 + h8; sgn = 1.f;
+      } else if (pass == 1) {
+        X = T; xr = b + 16; xc = b + 16; Y = T; yr = b; yc = b + 16 + h8; nk8 = 2; sr = b + 16; sc = b + h8;
+        sgn = -1.f;
+      } else if (pass == 2) {
+        X = A; xr = 16 * rb; xc = 16 * cb; Y = T; yr = 16 * cb; yc = 16 * cb + h8; nk8 = 2 * (2 - cb);
+        sr = 16 * (rb - 2); sc = 32 + 16 * cb + h8; sgn = 1.f;
+      } else {
+        X = T; xr = 16 * rb; xc = 32; Y = T; yr = 0; yc = 32 + 16 * cb + h8; nk8 = 2 * (rb - 1);
+        sr = 16 * rb; sc = 16 * cb + h8; sgn = -1.f;
+      }
+      float c[4] = {};
+      mma_tile(X, xr, xc, Y, yr, yc, nk8, c, ln);
+      store_tile(T, sr, sc, c, sgn, ln);
+    }
+    named_bar_sync(1, 256);
   }
-  named_bar_sync(1, 256);
-  if (wq < 4) {
-    const int b = 32 * (wq >> 1);
-    float c[4] = {};
-    mma_tile(T, b + 16, b + 16, T, b, b + 16 + 8 * h, 2, c, ln);  // D_{b+1} X
-    store_tile(T, b + 16, b + 8 * h, c, -1.f, ln);
+}
+
+// First row of a 64-row window (cumulative log-decays s0 at row lane, s1 at
+// row lane + 32; mv valid rows) at which the span of {0, G_0 .. G_row}
+// passes kMaxSpan, or 64. Called by a whole warp, only for windows whose
+// span is too wide, so it is kept out of line.
+__device__ __noinline__ int span_limit_row(float s0, float s1, int mv, int lane) {
+  float mx0 = fmaxf(s0, 0.f), mn0 = fminf(s0, 0.f), mx1 = s1, mn1 = s1;
+  for (int o = 1; o < 32; o <<= 1) {
+    const float a0 = __shfl_up_sync(0xffffffffu, mx0, o), a1 = __shfl_up_sync(0xffffffffu, mn0, o);
+    const float a2 = __shfl_up_sync(0xffffffffu, mx1, o), a3 = __shfl_up_sync(0xffffffffu, mn1, o);
+    if (lane >= o) {
+      mx0 = fmaxf(mx0, a0);
+      mn0 = fminf(mn0, a1);
+      mx1 = fmaxf(mx1, a2);
+      mn1 = fminf(mn1, a3);
+    }
   }
-  named_bar_sync(1, 256);
-  // step 3: warp wq -> output block (rb, cb) = (2 + (wq >> 2), (wq >> 1) & 1), columns 8 h
-  const int rb = 2 + (wq >> 2), cb = (wq >> 1) & 1;
-  {
-    float c[4] = {};
-    // X = A_{rb, cb..1} T_{cb..1, cb}  (T_11 is lower triangular)
-    mma_tile(A, 16 * rb, 16 * cb, T, 16 * cb, 16 * cb + 8 * h, 2 * (2 - cb), c, ln);
-    store_tile(T, 16 * (rb - 2), 32 + 16 * cb + 8 * h, c, 1.f, ln);  // parked in the upper right
+  mx1 = fmaxf(mx1, __shfl_sync(0xffffffffu, mx0, 31));
+  mn1 = fminf(mn1, __shfl_sync(0xffffffffu, mn0, 31));
+  const unsigned over0 = __ballot_sync(0xffffffffu, lane < mv && mx0 - mn0 > kMaxSpan);
+  const unsigned over1 = __ballot_sync(0xffffffffu, lane + 32 < mv && mx1 - mn1 > kMaxSpan);
+  return over0 ? __ffs(over0) - 1 : (over1 ? 32 + __ffs(over1) - 1 : kChunk);
+}
+
+// A bounded wait gave up: the CTA reports it once and every role unwinds.
+// Out of line: it only runs on that cold path.
+__device__ __noinline__ void fail_wait(Status* st, volatile int* abort_flag, uint32_t detail) {
+  if (!*abort_flag) {
+    *abort_flag = 1;
+    report(st, GDN_ERR_DEVICE_TIMEOUT, detail);
   }
-  named_bar_sync(1, 256);
-  {
-    float c[4] = {};
-    // T_{rb,cb} = -T_{rb, 2..rb} X_{2..rb, cb}
-    mma_tile(T, 16 * rb, 32, T, 0, 32 + 16 * cb + 8 * h, 2 * (rb - 1), c, ln);
-    store_tile(T, 16 * rb, 16 * cb + 8 * h, c, -1.f, ln);
-  }
-  named_bar_sync(1, 256);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -260,7 +304,6 @@ template <int DK, int DV>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gdn_tc_kernel(const Params p, const __grid_constant__ Tmaps tm) {
   using L = TcLayout<DK, DV>;
-  using L_ = L;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -282,11 +325,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int hq = h / (p.h_v / p.h_qk);
   int64_t bos, eos;
   seq_bounds(p, n, bos, eos);
-  const int nchunks = (int)((eos - bos + kChunk - 1) / kChunk);
+  const int64_t len = eos - bos;
 
   // ---- setup
   if (tid == 0) {
-    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], (b == B_READY0 || b == B_READY1) ? 32u : 1u);
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], 1u);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -305,456 +348,438 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_ptr;
 
-  auto fail = [&](int where) {
-    if (!*abort_flag) {
-      *abort_flag = 1;
-      report(p.status, GDN_ERR_DEVICE_TIMEOUT, (uint32_t)(unit * 16 + where));
-    }
+  auto fail = [&](int where) { fail_wait(p.status, abort_flag, (uint32_t)(unit * 16 + where)); };
+  auto slot_kq = [&](int c) { return sbase + L::RING0 + (uint32_t)(c % 3) * L::SLOT_BYTES; };
+  auto slot_v = [&](int c) { return sbase + L::V0 + (uint32_t)(c & 1) * L::V_BYTES; };
+  auto slot_sc = [&](int c) {
+    return reinterpret_cast<float*>(sm + L::RING0 + (uint32_t)(c % 3) * L::SLOT_BYTES + L::KQ_BYTES);
   };
-  auto stage_kq = [&](int s) { return sbase + L::STAGE0 + (uint32_t)s * L::STAGE_BYTES; };
-  auto stage_v = [&](int s) { return stage_kq(s) + L::KQ_BYTES; };
-  auto stage_scal = [&](int s) {
-    return reinterpret_cast<float*>(sm + L::STAGE0 + (uint32_t)s * L::STAGE_BYTES + L::KQ_BYTES +
-                                    L::V_BYTES);
-  };
-  auto chunk_rows = [&](int c) {
-    const int64_t t0 = bos + (int64_t)c * kChunk;
-    return (int)((eos - t0) < kChunk ? (eos - t0) : kChunk);
-  };
+  auto sc_int = [](const float* sc, int k) { return __float_as_int(sc[k]); };
+  auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, abort_flag, kWaitLimitNs); };
 
   if (warp == 0) {
     // ================================================================ producer
-    // TMA tiles for chunk c+1 are requested before chunk c is finished here;
-    // then chunk c's tail rows are cleared, its gates scanned and its q norms
-    // taken, and the stage is published to WG-A and the MMA issuer.
+    // Scans the gates of the next 64 rows, ends the chunk early if the log-decay
+    // span would pass kMaxSpan, keeps the state-scale bookkeeping, and requests
+    // the chunk's tiles once its ring slots are free. It never waits for data.
     const uint32_t tx_bytes = (uint32_t)(2 * L::NKA + L::NVA) * 8192u;
-    int issued[2] = {-1, -1};
-    auto issue = [&](int c) {
-      const int s = c & 1;
-      const int t0 = (int)(bos + (int64_t)c * kChunk);
-      uint8_t* kq = sm + L::STAGE0 + s * L::STAGE_BYTES;
-      mbar_arrive_expect_tx(&bars[B_TMA0 + s], tx_bytes);
-      for (int a = 0; a < L::NKA; ++a) {
-        tma_load_3d(kq + a * 16384, &tm.k, &bars[B_TMA0 + s], 64 * a, hq, t0);
-        tma_load_3d(kq + a * 16384 + 8192, &tm.q, &bars[B_TMA0 + s], 64 * a, hq, t0);
-      }
-      for (int a = 0; a < L::NVA; ++a)
-        tma_load_3d(kq + L::KQ_BYTES + a * 8192, &tm.v, &bars[B_TMA0 + s], 64 * a, h, t0);
-    };
-    auto load_gates = [&](int c, float& g0, float& g1, float& b0, float& b1) {
-      const int64_t t0 = bos + (int64_t)c * kChunk;
-      const int m = chunk_rows(c);
-      g0 = g1 = b0 = b1 = 0.f;
-      if (lane < m) {
-        g0 = load_gate(p.g, (t0 + lane) * p.h_v + h, p.gate_f32);
-        b0 = load_gate(p.beta, (t0 + lane) * p.h_v + h, p.gate_f32);
-      }
-      if (lane + 32 < m) {
-        g1 = load_gate(p.g, (t0 + lane + 32) * p.h_v + h, p.gate_f32);
-        b1 = load_gate(p.beta, (t0 + lane + 32) * p.h_v + h, p.gate_f32);
-      }
-    };
-    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-    if (nchunks > 0) {
-      if (lane == 0) issue(0);
-      issued[0] = 0;
-      load_gates(0, g0, g1, b0, b1);
-    }
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1;
-      if (!mbar_wait(&bars[B_TMA0 + s], (c >> 1) & 1, abort_flag, kWaitLimitNs)) {
-        fail(1);
-        break;
-      }
-      const int m = chunk_rows(c);
-      const uint32_t kq = stage_kq(s), vv = stage_v(s);
-      if (m < kChunk) {  // rows of the next sequence (or TMA zero fill): clear them
-        const int rows = kChunk - m, nreg = 2 * L::NKA + L::NVA;
-        for (int idx = lane; idx < rows * 8 * nreg; idx += 32) {
-          const int reg = idx / (rows * 8), rem = idx % (rows * 8);
-          const int r = m + (rem >> 3), ch = rem & 7;
-          const uint32_t base = reg < 2 * L::NKA ? kq + (reg >> 1) * 16384u + (reg & 1) * 8192u
-                                                 : vv + (reg - 2 * L::NKA) * 8192u;
-          st_shared_v4(base + r * 128u + ch * 16u, 0, 0, 0, 0);
+    int issued = 0;
+    if (len > 0) {
+      int64_t start = 0;
+      float logmu = 0.f;
+      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+      auto load_gates = [&](int64_t st) {
+        const int64_t avail = len - st;
+        g0 = g1 = b0 = b1 = 0.f;
+        if (lane < avail) {
+          g0 = load_gate(p.g, (bos + st + lane) * p.h_v + h, p.gate_f32);
+          b0 = load_gate(p.beta, (bos + st + lane) * p.h_v + h, p.gate_f32);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      // gate cumsum over the chunk and its span
-      float c0v = g0, c1v = g1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u0 = __shfl_up_sync(0xffffffffu, c0v, o);
-        const float u1 = __shfl_up_sync(0xffffffffu, c1v, o);
-        if (lane >= o) {
-          c0v += u0;
-          c1v += u1;
+        if (lane + 32 < avail) {
+          g1 = load_gate(p.g, (bos + st + lane + 32) * p.h_v + h, p.gate_f32);
+          b1 = load_gate(p.beta, (bos + st + lane + 32) * p.h_v + h, p.gate_f32);
         }
-      }
-      c1v += __shfl_sync(0xffffffffu, c0v, 31);
-      float gmax = fmaxf(c0v, c1v), gmin = fminf(c0v, c1v);
+      };
+      for (int c = 0;; ++c) {
+        load_gates(start);  // the producer runs chunks ahead: this latency is off the critical path
+        const int mv = (int)(len - start < kChunk ? len - start : kChunk);
+        // inclusive prefix sums and prefix max / min (the chunk start, 0, included)
+        float s0 = g0, s1 = g1;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
-        gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
-      }
-      float* sc = stage_scal(s);
-      sc[SC_G + lane] = c0v;
-      sc[SC_G + lane + 32] = c1v;
-      sc[SC_B + lane] = b0;
-      sc[SC_B + lane + 32] = b1;
-      if (lane == 0) {
-        sc[SC_GMAX] = gmax;
-        sc[SC_GMIN] = gmin;
-      }
-      mbar_arrive(&bars[B_READY0 + s]);
-      // next chunk: gates into registers, then its tiles once the stage is free
-      if (c + 1 < nchunks) {
-        load_gates(c + 1, g0, g1, b0, b1);
-        const int s1 = (c + 1) & 1;
-        if (c + 1 >= 2 &&
-            !mbar_wait(&bars[B_EMPTY0 + s1], (((c + 1) >> 1) + 1) & 1, abort_flag, kWaitLimitNs)) {
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u0 = __shfl_up_sync(0xffffffffu, s0, o), u1 = __shfl_up_sync(0xffffffffu, s1, o);
+          if (lane >= o) { s0 += u0; s1 += u1; }
+        }
+        s1 += __shfl_sync(0xffffffffu, s0, 31);
+        // span of the whole window (with the chunk start, 0); only a window that is too
+        // wide needs the row where the span first passes the limit
+        float wmax = fmaxf(fmaxf(lane < mv ? s0 : 0.f, lane + 32 < mv ? s1 : 0.f), 0.f);
+        float wmin = fminf(fminf(lane < mv ? s0 : 0.f, lane + 32 < mv ? s1 : 0.f), 0.f);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+          wmin = fminf(wmin, __shfl_xor_sync(0xffffffffu, wmin, o));
+        }
+        const int first = (wmax - wmin > kMaxSpan) ? span_limit_row(s0, s1, mv, lane) : kChunk;
+        const int m = first < 1 ? 1 : (first < mv ? first : mv);
+        // rows past m: no decay, no write
+        const float Gm = __shfl_sync(0xffffffffu, (m - 1) < 32 ? s0 : s1, (m - 1) & 31);
+        if (lane >= m) { s0 = Gm; b0 = 0.f; }
+        if (lane + 32 >= m) { s1 = Gm; b1 = 0.f; }
+        float gmax = fmaxf(lane < m ? s0 : -3.0e38f, lane + 32 < m ? s1 : -3.0e38f);
+        float gmin = fminf(lane < m ? s0 : 3.0e38f, lane + 32 < m ? s1 : 3.0e38f);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+          gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
+        }
+        const float loglam = logmu + Gm;
+        const bool eager = fabsf(loglam) > kMaxLogScale;
+        const bool last = start + m >= len;
+        // ring slots: K/Q of chunk c-3 and V of chunk c-2 released
+        bool ok = true;
+        if (c >= 3) ok = wait(B_KQE0 + c % 3, ((c / 3) + 1) & 1);
+        if (ok && c >= 2) ok = wait(B_VE0 + (c & 1), ((c >> 1) + 1) & 1);
+        if (!ok) {
           fail(0);
           break;
         }
-        if (lane == 0) issue(c + 1);
-        issued[s1] = c + 1;
+        float* sc = slot_sc(c);
+        sc[SC_G + lane] = s0;
+        sc[SC_G + lane + 32] = s1;
+        sc[SC_B + lane] = b0;
+        sc[SC_B + lane + 32] = b1;
+        __syncwarp();  // every lane's scalars before lane 0's arrive publishes them
+        if (lane == 0) {
+          sc[SC_GMAX] = gmax;
+          sc[SC_GMIN] = gmin;
+          sc[SC_GM] = Gm;
+          sc[SC_LAMLOG] = eager ? 0.f : loglam;
+          sc[SC_NULOG] = eager ? -Gm : logmu;
+          sc[SC_RMW] = eager ? exp2f(loglam * kLog2e) : 1.f;
+          sc[SC_MUNEXT] = eager ? 1.f : exp2f(loglam * kLog2e);
+          sc[SC_M] = __int_as_float(m);
+          sc[SC_FLAGS] = __int_as_float((last ? 1 : 0) | (eager ? 2 : 0));
+          *reinterpret_cast<long long*>(&sc[SC_T0]) = (long long)(bos + start);
+          // the arrive publishes the scalars; the tiles complete the phase
+          const int row = (int)(bos + start);
+          uint64_t* full = &bars[B_FULL0 + c % 3];
+          mbar_arrive_expect_tx(full, tx_bytes);
+          const uint32_t kq = slot_kq(c), vv = slot_v(c);
+#pragma unroll 1
+          for (int a = 0; a < 2 * L::NKA + L::NVA; ++a) {  // K, Q per atom column, then V
+            const bool isv = a >= 2 * L::NKA;
+            const int ac = isv ? a - 2 * L::NKA : (a >> 1);
+            const CUtensorMap* map = isv ? &tm.v : ((a & 1) ? &tm.q : &tm.k);
+            uint8_t* dst = isv ? sm + (vv - sbase) + ac * 8192 : sm + (kq - sbase) + ac * 16384 + (a & 1) * 8192;
+            tma_load_3d(dst, map, full, 64 * ac, isv ? h : hq, row);
+          }
+        }
+        __syncwarp();
+        issued = c + 1;
+        if (last) break;
+        start += m;
+        logmu = eager ? 0.f : loglam;
       }
     }
-    // on abort, let the loads already issued land before the CTA can exit
-    // (in the normal path they were all consumed and these return at once)
-    for (int s = 0; s < 2; ++s)
-      if (issued[s] >= 0)
-        mbar_wait(&bars[B_TMA0 + s], (issued[s] >> 1) & 1, nullptr, 100000000ull);
+    // let every requested tile land before the CTA can exit (on the normal path
+    // they were all consumed and these return at once)
+    if (lane == 0)
+      for (int c = issued - 3 < 0 ? 0 : issued - 3; c < issued; ++c)
+        mbar_wait(&bars[B_FULL0 + c % 3], (c / 3) & 1, nullptr, 100000000ull);
   } else if (warp == 1) {
-    // ================================================================ state-independent MMAs
-    if (lane == 0) {
+    // ================================================================ [K;Q] K^T
+    if (lane == 0 && len > 0) {
       constexpr uint32_t id_kq = idesc_bf16(128, 64, 0, 0);
-      constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1;
-        if (!mbar_wait(&bars[B_READY0 + s], (c >> 1) & 1, abort_flag, kWaitLimitNs) ||
-            (c >= 1 && !mbar_wait(&bars[B_KQ_FREE], (c - 1) & 1, abort_flag, kWaitLimitNs))) {
+      for (int c = 0;; ++c) {
+        if (!wait(B_FULL0 + c % 3, (c / 3) & 1) || (c >= 1 && !wait(B_KQ_FREE, (c - 1) & 1))) {
           fail(2);
           break;
         }
         tc_fence_after();
-        const uint32_t kq = stage_kq(s);
-        // [K;Q] K^T : A = rows of K then Q (K-major), B = K (K-major, N = 64)
-        const uint64_t dkq = sdesc(kq, 16, 1024);
-#pragma unroll
-        for (int a = 0; a < L::NKA; ++a)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t d = sdesc_add(dkq, a * 16384u + k * 32u);
-            mma_ss(tmem + TM_KQ, d, d, id_kq, (a | k) != 0);
-          }
-        mma_commit(&bars[B_KQ_DONE]);
-        if (!mbar_wait(&bars[B_P1_MID], c & 1, abort_flag, kWaitLimitNs)) {
-          fail(3);
-          break;
+        // A = rows of K then Q (K-major), B = K (K-major, N = 64)
+        const uint64_t dkq = sdesc(slot_kq(c), 16, 1024);
+#pragma unroll 1
+        for (int kk = 0; kk < 4 * L::NKA; ++kk) {
+          const uint64_t d = sdesc_add(dkq, (kk >> 2) * 16384u + (kk & 3) * 32u);
+          mma_ss(tmem + TM_KQ, d, d, id_kq, kk != 0);
         }
-        tc_fence_after();
-        // W^T = K^T T_w^T : A = K^T (MN-major, d_k atoms 16 KB apart or the zero page)
-        const uint32_t lbo_k = (L::NKA == 2) ? 16384u : (sbase + L::ZERO - kq);
-        const uint64_t dka = sdesc(kq, lbo_k, 1024), dtw = sdesc(sbase + L::TW, 16, 1024);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + TM_KQ, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
-        mma_commit(&bars[B_W_DONE]);
+        mma_commit(&bars[B_KQ_DONE]);
+        if (sc_int(slot_sc(c), SC_FLAGS) & 1) break;
       }
       mma_commit(&bars[B_DRAIN1]);  // every MMA this thread issued has finished before exit
       mbar_wait(&bars[B_DRAIN1], 0, nullptr, 100000000ull);
     }
   } else if (warp == 2) {
     // ================================================================ state-dependent MMAs
-    if (lane == 0) {
-      constexpr uint32_t id_u = idesc_bf16(128, 64, 1, 0);
+    if (lane == 0 && len > 0) {
       constexpr uint32_t id_sw = idesc_bf16(128, 64, 0, 1);
       constexpr uint32_t id_qs = idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_st = idesc_bf16(128, DK, 0, 1);
       constexpr uint32_t id_pu = idesc_bf16(128, 64, 0, 0);
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1, par = c & 1;
-        if (!mbar_wait(&bars[B_P1_DONE0 + par], (c >> 1) & 1, abort_flag, kWaitLimitNs)) {
+      for (int c = 0;; ++c) {
+        const int par = c & 1;
+        if (!wait(B_P1_DONE0 + par, (c >> 1) & 1) || !wait(B_S_READY, c & 1)) {
           fail(4);
           break;
         }
         tc_fence_after();
-        const uint32_t kq = stage_kq(s), vv = stage_v(s);
-        const uint32_t tb = sbase + L::TB0 + par * L::SCR_BYTES;
-        const uint32_t wt = sbase + L::WT0 + par * L::SCR_BYTES;
-        const uint32_t sop = sbase + L::SOP;
-        // U^T = V^T (T_b hi + lo)^T : A = V^T MN-major (d_v atoms 8 KB apart or the zero page).
-        // State-independent: issued as soon as the chunk is prepared.
-        const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
-        const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(tb, 16, 1024);
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_R, sdesc_add(dva, k * 2048u), sdesc_add(dtb, half * 8192u + k * 32u), id_u,
-                   (half | k) != 0);
-        if (!mbar_wait(&bars[B_S_READY], c & 1, abort_flag, kWaitLimitNs)) {
-          fail(5);
-          break;
-        }
-        tc_fence_after();
-        // U'^T += (-S^T) W^T : A = -S^T K-major, B = W^T MN-major [d_k][j]
-        const uint64_t dsop = sdesc(sop, 16, 1024), dwt = sdesc(wt, 16, 1024);
-#pragma unroll
-        for (int a = 0; a < L::NKA; ++a)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_R, sdesc_add(dsop, a * 16384u + k * 32u), sdesc_add(dwt, (a * 4 + k) * 2048u),
-                   id_sw, 1);
+        const bool last = cscal[c % 3].last;  // read now: the buffer is reused after this chunk
+        const uint32_t kq = slot_kq(c);
+        // U'^T += S~^T W'^T : A = S~^T (bf16, TMEM), B = W'^T MN-major [d_k][j]
+        const uint64_t dwt = sdesc(sbase + L::WT0 + par * L::SCR_BYTES, 16, 1024);
+#pragma unroll 1
+        for (int kk = 0; kk < 4 * L::NKA; ++kk)
+          mma_ts(tmem + TM_R, tmem + TM_SB + kk * 8u, sdesc_add(dwt, kk * 2048u), id_sw, 1);
         mma_commit(&bars[B_UP_DONE]);
-        // QS^T = (-S^T) Q^T (raw q tile, K-major), once the last epilogue has read its block
-        if (c >= 1 && !mbar_wait(&bars[B_EPI_DONE], (c - 1) & 1, abort_flag, kWaitLimitNs)) {
+        mma_commit(&bars[B_WFREE0 + par]);
+        // O^T = S~^T Q^T (raw q tile, K-major), once the last epilogue has read O
+        if (c >= 1 && !wait(B_EPI_DONE, (c - 1) & 1)) {
           fail(6);
           break;
         }
         tc_fence_after();
         const uint64_t dq = sdesc(kq + 8192u, 16, 1024);
-#pragma unroll
-        for (int a = 0; a < L::NKA; ++a)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + TM_QS, sdesc_add(dsop, a * 16384u + k * 32u), sdesc_add(dq, a * 16384u + k * 32u),
-                   id_qs, (a | k) != 0);
-        if (!mbar_wait(&bars[B_UOPS_READY], c & 1, abort_flag, kWaitLimitNs)) {
+#pragma unroll 1
+        for (int kk = 0; kk < 4 * L::NKA; ++kk)
+          mma_ts(tmem + TM_O, tmem + TM_SB + kk * 8u, sdesc_add(dq, (kk >> 2) * 16384u + (kk & 3) * 32u),
+                 id_qs, kk != 0);
+        if (!wait(B_UOPS_READY, c & 1)) {
           fail(7);
           break;
         }
         tc_fence_after();
-        // S^T += (U' diag(s))^T K : A from TMEM (hi, then lo), B = K MN-major (N = d_k)
-        const uint32_t lbo_kn = (L::NKA == 2) ? 16384u : 16u;
-        const uint64_t dkn = sdesc(kq, lbo_kn, 1024);
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + TM_S, tmem + (half ? TM_UL : TM_UH) + k * 8u, sdesc_add(dkn, k * 2048u), id_st, 1);
+        // S~^T += (U' s)^T K : A from TMEM (hi, then lo), B = K MN-major (N = d_k)
+        const uint64_t dkn = sdesc(kq, (L::NKA == 2) ? 16384u : 16u, 1024);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)  // hi (kk < 4), then lo
+          mma_ts(tmem + TM_S, tmem + TM_UH + kk * 8u, sdesc_add(dkn, (kk & 3) * 2048u), id_st, 1);
         mma_commit(&bars[B_STATE_DONE]);
-        // O^T = U'^T P^T : A from TMEM (bf16 U'), B = P K-major [i][j]
-        const uint64_t dpp = sdesc(sbase + L::P0 + par * 8192u, 16, 1024);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + TM_O, tmem + TM_UU + k * 8u, sdesc_add(dpp, k * 32u), id_pu, k != 0);
+        // O^T += (U' s)^T M^T : B = M K-major [i][j]
+        const uint64_t dm = sdesc(sbase + L::M0 + par * 8192u, 16, 1024);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, (kk & 3) * 32u), id_pu, 1);
         mma_commit(&bars[B_O_DONE]);
-        mma_commit(&bars[B_EMPTY0 + s]);
+        mma_commit(&bars[B_KQE0 + c % 3]);
+        if (last) break;
       }
       mma_commit(&bars[B_DRAIN2]);
       mbar_wait(&bars[B_DRAIN2], 0, nullptr, 100000000ull);
     }
-  } else if (warp >= 4 && warp < 12) {
-    // ================================================================ WG-A: chunk preparation
-    const int wa = tid - 128;         // 0..255
-    const int L = wa & 127;           // TMEM lane
-    const int hf = wa >> 7;           // which 32-column half of a 64-wide block
-    const uint32_t lane_off = (uint32_t)((L & ~31) << 16);
-    const bool krow = L < 64;
-    const int i = L & 63;
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c & 1, par = c & 1;
-      bool ok = mbar_wait(&bars[B_READY0 + s], (c >> 1) & 1, abort_flag, kWaitLimitNs);
-      // P, T_b and W^T of this parity were last read by chunk c-2's MMAs
-      if (ok && c >= 2)
-        ok = mbar_wait(&bars[B_EMPTY0 + s], ((c >> 1) + 1) & 1, abort_flag, kWaitLimitNs);
-      // chunk scalars c % 3 were last read by chunk c-3's epilogue
-      if (ok && c >= 3)
-        ok = mbar_wait(&bars[B_CS_FREE0 + c % 3], ((c / 3) + 1) & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(8);
-      named_bar_sync(1, 256);
-      if (*abort_flag) break;
-      const float* sc = stage_scal(s);
-      ChunkScalars& cs = cscal[c % 3];
-      const float gmax = sc[SC_GMAX];
-      const bool exact = (gmax - sc[SC_GMIN]) > kMaxDecaySpan;
-      const float Gi = sc[SC_G + i], Gl2i = Gi * kLog2e, GCl2 = sc[SC_G + 63] * kLog2e;
-      const float ai = exp2f((Gi - gmax) * kLog2e);
-      ok = mbar_wait(&bars[B_KQ_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(9);
-      named_bar_sync(1, 256);
-      if (*abort_flag) break;
-      tc_fence_after();
-      float qss_own = 0.f;
-      uint32_t v[32];  // row L of [K;Q] K^T, columns [32 hf, 32 hf + 32)
-      tmem_ld32(tmem + lane_off + TM_KQ + 32 * hf, v);
-      tmem_ld_wait();
-      float* Abuf = reinterpret_cast<float*>(sm + L_::WT0 + par * L_::SCR_BYTES);
-      float* Tbuf = reinterpret_cast<float*>(sm + L_::TB0 + par * L_::SCR_BYTES);
-      if (krow && (i >> 5) == hf) {
-        // r^k_i from the diagonal of K K^T (fp32 sum of exact bf16 products)
-        float diag = 0.f;
+  } else if (warp == 3) {
+    // ================================================================ q norms
+    // r^q only weights the output rows, so it is taken here, off the path of
+    // the chunk preparation: sum of squares of each raw q row from the tile.
+    if (len > 0) {
+      for (int c = 0;; ++c) {
+        bool ok = true;
+        if (lane == 0) ok = wait(B_FULL0 + c % 3, (c / 3) & 1);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+          if (lane == 0) fail(14);
+          break;
+        }
+        const uint32_t qt = slot_kq(c) + 8192u;
+#pragma unroll 1
+        for (int rr = 0; rr < 2; ++rr) {
+          const uint32_t row = qt + (uint32_t)(lane + 32 * rr) * 128u;
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll 1
+          for (int k = 0; k < 8 * L::NKA; ++k) {
+            // the row's 16-byte pieces in any order (the swizzle only permutes them)
+            const int kp = (k & ~7) | ((k + lane) & 7);
+            uint32_t x[4];
+            ld_shared_v4(row + (kp >> 3) * 16384u + (kp & 7) * 16u, x[0], x[1], x[2], x[3]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j == (i & 31)) diag = __uint_as_float(v[j]);
-        const float ri = p.l2norm ? 1.0f / sqrtf(diag + 1e-6f) : 1.f;
-        const float bi = sc[SC_B + i];
-        ps->d[i] = ri * exp2f((gmax - Gi) * kLog2e);
-        ps->r[i] = ri;
-        ps->beta[i] = bi;
-        ps->tw[i] = bi * exp2f(Gl2i) * ri;
-        cs.s[i] = exp2f(GCl2 - Gl2i) * ri;
-      } else if (!krow) {
-        // |q_i|^2 over this thread's half of the raw q row (r^q only scales the output)
-        float ss0 = 0.f, ss1 = 0.f;
-        const uint32_t rbase = stage_kq(s) + 8192u + i * 128u;
-#pragma unroll
-        for (int k = 0; k < 4 * L_::NKA; ++k) {
-          const int idx = hf * 4 * L_::NKA + k;
-          uint32_t x[4];
-          ld_shared_v4(rbase + (idx >> 3) * 16384u + (idx & 7) * 16u, x[0], x[1], x[2], x[3]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = bf16_lo_f(x[e]), hi = bf16_hi_f(x[e]);
-            ss0 = fmaf(lo, lo, ss0);
-            ss1 = fmaf(hi, hi, ss1);
+            for (int e = 0; e < 4; ++e) {
+              const float lo = bf16_lo_f(x[e]), hi = bf16_hi_f(x[e]);
+              a0 = fmaf(lo, lo, a0);
+              a1 = fmaf(hi, hi, a1);
+            }
           }
+          slot_sc(c)[SC_RQ + lane + 32 * rr] = p.l2norm ? 1.0f / sqrtf(a0 + a1 + 1e-6f) : 1.f;
         }
-        if (hf == 1) const_cast<float*>(sc)[SC_QSS + i] = ss0 + ss1;
-        else qss_own = ss0 + ss1;
-      }
-      named_bar_sync(1, 256);
-      if (!krow && hf == 0) {
-        const float rq = p.l2norm ? 1.0f / sqrtf(qss_own + sc[SC_QSS + i] + 1e-6f) : 1.f;
-        const float co = p.scale * rq;
-        cs.co[i] = co;
-        cs.cq[i] = -co * exp2f(Gl2i);
-        if (i == 0) cs.eGC = exp2f(GCl2);
-      }
-      if (exact) {
-        // rare: every decay by its own exp (A and P rows into registers first)
-        float row[32];
-        {
-          float wgt[32];
-          exact_row(wgt, ps->r, sc + SC_G, Gl2i, ps->beta[i] * ps->r[i], 32 * hf, i, krow);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) row[e] = wgt[e] * __uint_as_float(v[e]);
-        }
-        if (krow) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(&Abuf[i * LDF + 32 * hf + 4 * q]) =
-                make_float4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
-        } else {
-          const uint32_t prow = sbase + L_::P0 + par * 8192u;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st_shared_v4(prow + sw128(i, 4 * hf + q), pack_bf16(row[8 * q], row[8 * q + 1]),
-                         pack_bf16(row[8 * q + 2], row[8 * q + 3]), pack_bf16(row[8 * q + 4], row[8 * q + 5]),
-                         pack_bf16(row[8 * q + 6], row[8 * q + 7]));
-        }
-      } else if (krow) {
-        // A_ij = beta_i r_i r_j e^{G_i - G_j} k_i.k_j  (j < i), fp32 into the scratch
-        const float cia = ps->beta[i] * ps->r[i] * ai;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int j0 = 32 * hf + 4 * q;
-          const float4 d4 = *reinterpret_cast<const float4*>(&ps->d[j0]);
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float a4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            a4[e] = (j0 + e < i) ? (cia * __uint_as_float(v[4 * q + e])) * dd[e] : 0.f;
-          *reinterpret_cast<float4*>(&Abuf[i * LDF + j0]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
-        }
-      } else {
-        // P_ij = e^{G_i - G_j} r^k_j q_i.k_j  (j <= i), bf16 K-major [i][j]
-        const uint32_t prow = sbase + L_::P0 + par * 8192u;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int j0 = 32 * hf + 8 * q;
-          const float4 da = *reinterpret_cast<const float4*>(&ps->d[j0]);
-          const float4 db = *reinterpret_cast<const float4*>(&ps->d[j0 + 4]);
-          const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-          float pv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            pv[e] = (j0 + e <= i) ? (ai * __uint_as_float(v[8 * q + e])) * dd[e] : 0.f;
-          st_shared_v4(prow + sw128(i, 4 * hf + q), pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
-                       pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_bar_sync(1, 256);
-      // ---- T = (I + A)^-1
-      solve_unit_lower(Abuf, Tbuf, wa);
-      // ---- T_b = T diag(beta) as bf16 hi + lo; T_w = T diag(beta e^G r^k)
-      {
-        const int ti = wa & 63, qq = wa >> 6;  // row ti, columns [16 qq, 16 qq + 16)
-        float t[16];
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const float4 x = *reinterpret_cast<const float4*>(&Tbuf[ti * LDF + 16 * qq + 4 * k4]);
-          const bool zero = qq > (ti >> 4);  // block above the diagonal
-          t[4 * k4 + 0] = zero ? 0.f : x.x;
-          t[4 * k4 + 1] = zero ? 0.f : x.y;
-          t[4 * k4 + 2] = zero ? 0.f : x.z;
-          t[4 * k4 + 3] = zero ? 0.f : x.w;
-        }
-        named_bar_sync(1, 256);  // every thread has read T before it is overwritten
-        const uint32_t tb = sbase + L_::TB0 + par * L_::SCR_BYTES;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int j0 = 16 * qq + 8 * q;
-          const float4 ba = *reinterpret_cast<const float4*>(&ps->beta[j0]);
-          const float4 bb = *reinterpret_cast<const float4*>(&ps->beta[j0 + 4]);
-          const float4 wa4 = *reinterpret_cast<const float4*>(&ps->tw[j0]);
-          const float4 wb4 = *reinterpret_cast<const float4*>(&ps->tw[j0 + 4]);
-          const float bt[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
-          const float wt8[8] = {wa4.x, wa4.y, wa4.z, wa4.w, wb4.x, wb4.y, wb4.z, wb4.w};
-          uint32_t hi4[4], lo4[4], w4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x0 = t[8 * q + 2 * e] * bt[2 * e], x1 = t[8 * q + 2 * e + 1] * bt[2 * e + 1];
-            hi4[e] = pack_bf16(x0, x1);
-            lo4[e] = pack_bf16(x0 - bf16_lo_f(hi4[e]), x1 - bf16_hi_f(hi4[e]));
-            w4[e] = pack_bf16(t[8 * q + 2 * e] * wt8[2 * e], t[8 * q + 2 * e + 1] * wt8[2 * e + 1]);
-          }
-          const uint32_t off = sw128(ti, 2 * qq + q);
-          st_shared_v4(tb + off, hi4[0], hi4[1], hi4[2], hi4[3]);
-          st_shared_v4(tb + 8192u + off, lo4[0], lo4[1], lo4[2], lo4[3]);
-          st_shared_v4(sbase + L_::TW + off, w4[0], w4[1], w4[2], w4[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (wa == 0) mbar_arrive(&bars[B_P1_MID]);
-      // ---- W^T: TMEM -> bf16 MN-major [d_k][j]
-      ok = mbar_wait(&bars[B_W_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(10);
-      named_bar_sync(1, 256);
-      if (*abort_flag) break;
-      tc_fence_after();
-      {
-        tmem_ld32(tmem + lane_off + TM_KQ + 32 * hf, v);
-        tmem_ld_wait();
-        const uint32_t wt = sbase + L_::WT0 + par * L_::SCR_BYTES;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_shared_v4(wt + sw128(L, 4 * hf + q),
-                       pack_bf16(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
-                       pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                       pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                       pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_bar_sync(1, 256);
-      if (wa == 0) {
-        mbar_arrive(&bars[B_P1_DONE0 + par]);
-        mbar_arrive(&bars[B_KQ_FREE]);
+        float* sc = slot_sc(c);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_RQ0 + c % 3]);
+        if (sc_int(sc, SC_FLAGS) & 1) break;
       }
     }
-  } else if (warp >= 12) {
+  } else if (warp < 12) {
+    // ================================================================ WG-A: chunk preparation
+    const int wa = tid - 128;         // 0..255
+    const int Ln = wa & 127;          // TMEM lane
+    const int hf = wa >> 7;           // which 32-column half of a 64-wide block
+    const uint32_t lane_off = (uint32_t)((Ln & ~31) << 16);
+    const bool krow = Ln < 64;
+    const int i = Ln & 63;
+    bool issued_mma = false;
+    if (len > 0) {
+      for (int c = 0;; ++c) {
+        const int par = c & 1;
+        bool ok = wait(B_FULL0 + c % 3, (c / 3) & 1);
+        // M / staging, W'^T / A and the chunk scalars of this parity were released by chunk c-2 / c-3
+        if (ok && c >= 2) ok = wait(B_MFREE0 + par, ((c >> 1) + 1) & 1);
+        if (ok && c >= 2) ok = wait(B_WFREE0 + par, ((c >> 1) + 1) & 1);
+        if (ok && c >= 3) ok = wait(B_CSF0 + c % 3, ((c / 3) + 1) & 1);
+        if (ok) ok = wait(B_KQ_DONE, c & 1);
+        if (!ok) fail(8);
+        if (named_bar_or(1, 256, !ok || *abort_flag)) break;
+        tc_fence_after();
+        const float* sc = slot_sc(c);
+        ChunkScalars& cs = cscal[c % 3];
+        const int m = sc_int(sc, SC_M);
+        const bool last = sc_int(sc, SC_FLAGS) & 1;
+        const float gmax = sc[SC_GMAX], Gm = sc[SC_GM], lamlog = sc[SC_LAMLOG];
+        const float Gi = sc[SC_G + i];
+        uint32_t v[32];  // row Ln of [K;Q] K^T, columns [32 hf, 32 hf + 32)
+        tmem_ld32(tmem + lane_off + TM_KQ + 32 * hf, v);
+        tmem_ld_wait();
+        tc_fence_before();
+        float* Abuf = reinterpret_cast<float*>(sm + L::WT0 + par * L::SCR_BYTES);
+        float* Tbuf = reinterpret_cast<float*>(sm + L::TB);
+        if (krow && (i >> 5) == hf) {
+          // r^k_i from the diagonal of K K^T (fp32 sum of exact bf16 products)
+          float diag = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == (i & 31)) diag = __uint_as_float(v[j]);
+          const float ri = p.l2norm ? 1.0f / sqrtf(diag + 1e-6f) : 1.f;
+          const float bi = sc[SC_B + i];
+          const bool live = i < m;
+          ps->d[i] = live ? ri * exp2f((gmax - Gi) * kLog2e) : 0.f;
+          ps->r[i] = ri;
+          ps->beta[i] = bi;
+          ps->tw[i] = live ? -bi * ri * exp2f((Gi + sc[SC_NULOG]) * kLog2e) : 0.f;
+          cs.s[i] = live ? ri * exp2f((Gm - Gi - lamlog) * kLog2e) : 0.f;
+        }
+        named_bar_sync(1, 256);
+        if (wa == 0) mbar_arrive(&bars[B_KQ_FREE]);  // [K;Q] K^T is in registers
+        if (krow) {
+          // A_ij = beta_i r_i r_j e^{G_i - G_j} k_i.k_j  (j < i < m), fp32 into the scratch
+          const float cia = i < m ? ps->beta[i] * ps->r[i] * exp2f((Gi - gmax) * kLog2e) : 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int j0 = 32 * hf + 4 * q;
+            const float4 d4 = *reinterpret_cast<const float4*>(&ps->d[j0]);
+            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+            float a4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              a4[e] = (j0 + e < i) ? (cia * __uint_as_float(v[4 * q + e])) * dd[e] : 0.f;
+            *reinterpret_cast<float4*>(&Abuf[i * LDF + j0]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+          }
+        } else {
+          // M_ij = q_i.k_j  (j <= i), bf16 K-major [i][j]
+          const uint32_t mrow = sbase + L::M0 + par * 8192u;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int j0 = 32 * hf + 8 * q;
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w4[e] = pack_bf16(j0 + 2 * e <= i ? __uint_as_float(v[8 * q + 2 * e]) : 0.f,
+                                j0 + 2 * e + 1 <= i ? __uint_as_float(v[8 * q + 2 * e + 1]) : 0.f);
+            st_shared_v4(mrow + sw128(i, 4 * hf + q), w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 256);
+        // ---- T = (I + A)^-1
+        solve_unit_lower(Abuf, Tbuf, wa);
+        // ---- T_b = T diag(beta) as bf16 hi + lo; T_w = T diag(tw)
+        {
+          const int ti = wa & 63, qq = wa >> 6;  // row ti, columns [16 qq, 16 qq + 16)
+          float t[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 x = *reinterpret_cast<const float4*>(&Tbuf[ti * LDF + 16 * qq + 4 * k4]);
+            const bool zero = qq > (ti >> 4);  // block above the diagonal
+            t[4 * k4 + 0] = zero ? 0.f : x.x;
+            t[4 * k4 + 1] = zero ? 0.f : x.y;
+            t[4 * k4 + 2] = zero ? 0.f : x.z;
+            t[4 * k4 + 3] = zero ? 0.f : x.w;
+          }
+          named_bar_sync(1, 256);  // every thread has read T before it is overwritten
+          const uint32_t tb = sbase + L::TB;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int j0 = 16 * qq + 8 * q;
+            const float4 ba = *reinterpret_cast<const float4*>(&ps->beta[j0]);
+            const float4 bb = *reinterpret_cast<const float4*>(&ps->beta[j0 + 4]);
+            const float4 wa4 = *reinterpret_cast<const float4*>(&ps->tw[j0]);
+            const float4 wb4 = *reinterpret_cast<const float4*>(&ps->tw[j0 + 4]);
+            const float bt[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+            const float wt8[8] = {wa4.x, wa4.y, wa4.z, wa4.w, wb4.x, wb4.y, wb4.z, wb4.w};
+            uint32_t hi4[4], lo4[4], w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x0 = t[8 * q + 2 * e] * bt[2 * e], x1 = t[8 * q + 2 * e + 1] * bt[2 * e + 1];
+              hi4[e] = pack_bf16(x0, x1);
+              lo4[e] = pack_bf16(x0 - bf16_lo_f(hi4[e]), x1 - bf16_hi_f(hi4[e]));
+              w4[e] = pack_bf16(t[8 * q + 2 * e] * wt8[2 * e], t[8 * q + 2 * e + 1] * wt8[2 * e + 1]);
+            }
+            const uint32_t off = sw128(ti, 2 * qq + q);
+            st_shared_v4(tb + off, hi4[0], hi4[1], hi4[2], hi4[3]);
+            st_shared_v4(tb + 8192u + off, lo4[0], lo4[1], lo4[2], lo4[3]);
+            st_shared_v4(sbase + L::TW + off, w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 256);
+        // ---- W'^T = K^T T_w^T and U^T = V^T T_b^T, issued from here
+        if (wa == 0) {
+          if (c >= 1 && !wait(B_R_FREE, (c - 1) & 1)) {
+            fail(10);
+          } else {
+            tc_fence_after();
+            constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
+            const uint32_t kq = slot_kq(c), vv = slot_v(c);
+            const uint32_t lbo_k = (L::NKA == 2) ? 16384u : (sbase + L::ZERO - kq);
+            const uint64_t dka = sdesc(kq, lbo_k, 1024), dtw = sdesc(sbase + L::TW, 16, 1024);
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + TM_W, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
+            const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
+            const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(sbase + L::TB, 16, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < 8; ++kk)  // T_b hi, then lo
+              mma_ss(tmem + TM_R, sdesc_add(dva, (kk & 3) * 2048u), sdesc_add(dtb, (kk >> 2) * 8192u + (kk & 3) * 32u),
+                     id_w, kk != 0);
+            mma_commit(&bars[B_W_DONE]);
+            mma_commit(&bars[B_VE0 + par]);
+            issued_mma = true;
+          }
+        }
+        ok = wait(B_W_DONE, c & 1);
+        if (!ok) fail(9);
+        if (named_bar_or(1, 256, !ok || *abort_flag)) break;
+        tc_fence_after();
+        // ---- W'^T: TMEM -> bf16 MN-major [d_k][j] (over the A scratch of this parity)
+        {
+          tmem_ld32(tmem + lane_off + TM_W + 32 * hf, v);
+          tmem_ld_wait();
+          const uint32_t wt = sbase + L::WT0 + par * L::SCR_BYTES;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_shared_v4(wt + sw128(Ln, 4 * hf + q),
+                         pack_bf16(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                         pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                         pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                         pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        // ---- output weights (need warp 3's q norms)
+        ok = true;
+        if (!krow && hf == 0) {
+          ok = wait(B_RQ0 + c % 3, (c / 3) & 1);
+          const float rq = sc[SC_RQ + i];
+          cs.co[i] = i < m ? p.scale * rq * exp2f((Gi - Gm + lamlog) * kLog2e) : 0.f;
+          if (i == 0) {
+            cs.t0 = *reinterpret_cast<const long long*>(&sc[SC_T0]);
+            cs.mu_next = sc[SC_MUNEXT];
+            cs.m = m;
+            cs.last = last ? 1 : 0;
+          }
+        }
+        if (!ok) fail(15);
+        if (named_bar_or(1, 256, !ok || *abort_flag)) break;
+        if (wa == 0) mbar_arrive(&bars[B_P1_DONE0 + par]);
+        if (last) break;
+      }
+    }
+    if (wa == 0 && issued_mma) {
+      mma_commit(&bars[B_DRAINA]);
+      mbar_wait(&bars[B_DRAINA], 0, nullptr, 100000000ull);
+    }
+  } else {
     // ================================================================ WG-B: state step + epilogue
     const int wb = tid - 384;  // == TMEM lane == d_v index
     const uint32_t lane_off = (uint32_t)((wb & ~31) << 16);
     const bool live = wb < DV;
-    // initial state -> S^T in TMEM (lane d_v, column d_k)
+    // initial state -> S~^T in TMEM (lane d_v, column d_k), mu = 1
     {
       const int64_t slot = state_slot(p, n);
       const float* s0 = slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + h) * DK * DV : nullptr;
@@ -768,137 +793,138 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tmem_st_wait();
     }
-    // S -> -S^T (bf16 operand of chunk c's MMAs); S *= e^{G_m} of chunk c
-    auto s_convert = [&](int c) -> bool {
-      const int par = c & 1;
-      bool ok = mbar_wait(&bars[B_P1_DONE0 + par], (c >> 1) & 1, abort_flag, kWaitLimitNs);
-      if (ok && c >= 1) ok = mbar_wait(&bars[B_STATE_DONE], (c - 1) & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(11);
-      named_bar_sync(2, 128);
-      if (*abort_flag) return false;
-      tc_fence_after();
-      const float eGC = cscal[c % 3].eGC;
+    float mu = 1.f;
+    bool ok_all = true;
+    const size_t osz = p.out_f32 ? 4 : 2;
+    const int pieces = (int)(DV * osz / 16);  // 16-byte pieces of one output row
+    const int pshift = __ffs(pieces) - 1;
+    for (int c = -1;; ++c) {
+      bool more = len > 0 && c < 0;
+      if (c >= 0) {
+        // ---- U'^T -> (U' diag(s/lambda))^T as bf16 hi / lo A operands
+        const ChunkScalars& cs = cscal[c % 3];
+        bool ok = wait(B_P1_DONE0 + (c & 1), (c >> 1) & 1) && wait(B_UP_DONE, c & 1);
+        if (!ok) fail(12);
+        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        tc_fence_after();
 #pragma unroll 1
-      for (int xb = 0; xb < DK / 32; ++xb) {
-        uint32_t va[32];
-        tmem_ld32(tmem + lane_off + TM_S + xb * 32, va);
-        tmem_ld_wait();
-        const uint32_t row = sbase + L_::SOP + (xb >> 1) * 16384u;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st_shared_v4(row + sw128(wb, (xb & 1) * 4 + q),
-                       pack_bf16(-__uint_as_float(va[8 * q + 0]), -__uint_as_float(va[8 * q + 1])),
-                       pack_bf16(-__uint_as_float(va[8 * q + 2]), -__uint_as_float(va[8 * q + 3])),
-                       pack_bf16(-__uint_as_float(va[8 * q + 4]), -__uint_as_float(va[8 * q + 5])),
-                       pack_bf16(-__uint_as_float(va[8 * q + 6]), -__uint_as_float(va[8 * q + 7])));
-#pragma unroll
-        for (int x = 0; x < 32; ++x) va[x] = __float_as_uint(__uint_as_float(va[x]) * eGC);
-        tmem_st32(tmem + lane_off + TM_S + xb * 32, va);
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_bar_sync(2, 128);
-      if (wb == 0) mbar_arrive(&bars[B_S_READY]);
-      return true;
-    };
-    bool run = nchunks == 0 || s_convert(0);
-    for (int c = 0; run && c < nchunks; ++c) {
-      const ChunkScalars& cs = cscal[c % 3];
-      // ---- U' -> (U' s) hi / lo and U' as bf16, into TMEM A operands
-      bool ok = mbar_wait(&bars[B_UP_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(12);
-      named_bar_sync(2, 128);
-      if (*abort_flag) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int hb = 0; hb < 2; ++hb) {  // tokens [32 hb, 32 hb + 32)
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_off + TM_R + hb * 32, u);
-        tmem_ld_wait();
-        uint32_t hi[16], lo[16], uu[16];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 s4 = *reinterpret_cast<const float4*>(&cs.s[hb * 32 + q * 4]);
-          const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float a0 = __uint_as_float(u[q * 4 + 2 * e]), a1 = __uint_as_float(u[q * 4 + 2 * e + 1]);
-            const float x0 = a0 * sv[2 * e], x1 = a1 * sv[2 * e + 1];
-            const uint32_t hh = pack_bf16(x0, x1);
-            hi[q * 2 + e] = hh;
-            lo[q * 2 + e] = pack_bf16(x0 - bf16_lo_f(hh), x1 - bf16_hi_f(hh));
-            uu[q * 2 + e] = pack_bf16(a0, a1);
-          }
-        }
-        tmem_st16(tmem + lane_off + TM_UH + hb * 16, hi);
-        tmem_st16(tmem + lane_off + TM_UL + hb * 16, lo);
-        tmem_st16(tmem + lane_off + TM_UU + hb * 16, uu);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      named_bar_sync(2, 128);
-      if (wb == 0) mbar_arrive(&bars[B_UOPS_READY]);
-      // ---- the next chunk's state operand first: it is on the serial path
-      if (c + 1 < nchunks && !s_convert(c + 1)) break;
-      // ---- epilogue: o_i = cq_i (-S^T q_i) + co_i (U'^T P^T)_i, stored straight to out
-      ok = mbar_wait(&bars[B_O_DONE], c & 1, abort_flag, kWaitLimitNs);
-      if (!ok) fail(13);
-      named_bar_sync(2, 128);
-      if (*abort_flag) break;
-      tc_fence_after();
-      {
-        const int64_t t0 = bos + (int64_t)c * kChunk;
-        const int m = chunk_rows(c);
-        const bool odd = wb & 1;
-#pragma unroll 1
-        for (int hb = 0; hb < 2; ++hb) {  // tokens [32 hb, 32 hb + 32)
-          uint32_t oq[32], oi[32];
-          tmem_ld32(tmem + lane_off + TM_QS + hb * 32, oq);
-          tmem_ld32(tmem + lane_off + TM_O + hb * 32, oi);
+        for (int hb = 0; hb < 2; ++hb) {  // columns j in [32 hb, 32 hb + 32)
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_off + TM_R + hb * 32, u);
           tmem_ld_wait();
+          uint32_t hi[16], lo[16];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 a4 = *reinterpret_cast<const float4*>(&cs.cq[hb * 32 + q * 4]);
-            const float4 b4 = *reinterpret_cast<const float4*>(&cs.co[hb * 32 + q * 4]);
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+            const float4 s4 = *reinterpret_cast<const float4*>(&cs.s[hb * 32 + q * 4]);
+            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              oq[q * 4 + e] = __float_as_uint(fmaf(av[e], __uint_as_float(oq[q * 4 + e]),
-                                                   bv[e] * __uint_as_float(oi[q * 4 + e])));
-          }
-          if (p.out_f32) {
-            if (live) {
-#pragma unroll
-              for (int ii = 0; ii < 32; ++ii)
-                if (hb * 32 + ii < m)
-                  reinterpret_cast<float*>(p.out)[((size_t)(t0 + hb * 32 + ii) * p.h_v + h) * DV + wb] =
-                      __uint_as_float(oq[ii]);
-            }
-          } else {
-            // lanes 2k and 2k+1 swap values so each stores a bf16 pair (d_v 2k, 2k+1)
-            // of one token: a warp writes two 64-byte row segments per store
-#pragma unroll
-            for (int tp = 0; tp < 16; ++tp) {
-              const float x0 = __uint_as_float(oq[2 * tp]), x1 = __uint_as_float(oq[2 * tp + 1]);
-              const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
-              const int row = hb * 32 + 2 * tp + (odd ? 1 : 0);
-              const uint32_t word = odd ? pack_bf16(got, x1) : pack_bf16(x0, got);
-              if (live && row < m)
-                reinterpret_cast<uint32_t*>(p.out)[(((size_t)(t0 + row) * p.h_v + h) * DV + (wb & ~1)) >> 1] = word;
+            for (int e = 0; e < 2; ++e) {
+              const float x0 = __uint_as_float(u[q * 4 + 2 * e]) * sv[2 * e];
+              const float x1 = __uint_as_float(u[q * 4 + 2 * e + 1]) * sv[2 * e + 1];
+              const uint32_t hh = pack_bf16(x0, x1);
+              hi[q * 2 + e] = hh;
+              lo[q * 2 + e] = pack_bf16(x0 - bf16_lo_f(hh), x1 - bf16_hi_f(hh));
             }
           }
+          tmem_st16(tmem + lane_off + TM_UH + hb * 16, hi);
+          tmem_st16(tmem + lane_off + TM_UL + hb * 16, lo);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar_sync(2, 128);
+        if (wb == 0) {
+          mbar_arrive(&bars[B_R_FREE]);
+          mbar_arrive(&bars[B_UOPS_READY]);
+        }
+        more = !cs.last;
+      }
+      if (more) {
+        // ---- S~ -> bf16 A operand for chunk c+1 (first applying its decay when eager)
+        const int cn = c + 1;
+        const float* sc = slot_sc(cn);
+        bool ok = wait(B_FULL0 + cn % 3, (cn / 3) & 1);
+        if (ok && c >= 0) ok = wait(B_STATE_DONE, c & 1);
+        if (!ok) fail(11);
+        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        tc_fence_after();
+        const bool eager = sc_int(sc, SC_FLAGS) & 2;
+        const float rmw = sc[SC_RMW];
+#pragma unroll 1
+        for (int xb = 0; xb < DK / 32; ++xb) {
+          uint32_t va[32];
+          tmem_ld32(tmem + lane_off + TM_S + xb * 32, va);
+          tmem_ld_wait();
+          if (eager) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) va[x] = __float_as_uint(__uint_as_float(va[x]) * rmw);
+            tmem_st32(tmem + lane_off + TM_S + xb * 32, va);
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) pk[x] = pack_bf16(__uint_as_float(va[2 * x]), __uint_as_float(va[2 * x + 1]));
+          tmem_st16(tmem + lane_off + TM_SB + xb * 16, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        named_bar_sync(2, 128);
+        if (wb == 0) mbar_arrive(&bars[B_S_READY]);
+      }
+      if (c >= 0) {
+        // ---- epilogue: out_i = co_i O^T_i, staged through the M buffer of this parity
+        const ChunkScalars& cs = cscal[c % 3];
+        bool ok = wait(B_O_DONE, c & 1);
+        if (!ok) fail(13);
+        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        tc_fence_after();
+        uint8_t* stage = sm + L::M0 + (c & 1) * 8192u;
+        const int m = cs.m;
+        const long long t0 = cs.t0;
+#pragma unroll 1
+        for (int p0 = 0; p0 < m; p0 += 16) {
+          uint32_t o[16];
+          tmem_ld16(tmem + lane_off + TM_O + p0, o);
+          tmem_ld_wait();
+          float co[16];
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
+            co[4 * t4] = c4.x;
+            co[4 * t4 + 1] = c4.y;
+            co[4 * t4 + 2] = c4.z;
+            co[4 * t4 + 3] = c4.w;
+          }
+          if (live && p.out_f32) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              reinterpret_cast<float*>(stage)[t * DV + wb] = co[t] * __uint_as_float(o[t]);
+          } else if (live) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              reinterpret_cast<__nv_bfloat16*>(stage)[t * DV + wb] = __float2bfloat16_rn(co[t] * __uint_as_float(o[t]));
+          }
+          named_bar_sync(2, 128);
+          const int rows = m - p0 < 16 ? m - p0 : 16;
+          for (int idx = wb; idx < (rows << pshift); idx += 128) {
+            const int r = idx >> pshift, pc = idx & (pieces - 1);
+            const uint4 x = *reinterpret_cast<const uint4*>(stage + (size_t)r * DV * osz + pc * 16);
+            char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + h) * DV) * osz;
+            *reinterpret_cast<uint4*>(dst + pc * 16) = x;
+          }
+          named_bar_sync(2, 128);
+        }
+        tc_fence_before();
+        named_bar_sync(2, 128);
+        mu = cs.mu_next;
+        if (wb == 0) {
+          mbar_arrive(&bars[B_EPI_DONE]);
+          mbar_arrive(&bars[B_MFREE0 + (c & 1)]);
+          mbar_arrive(&bars[B_CSF0 + c % 3]);
         }
       }
-      tc_fence_before();
-      named_bar_sync(2, 128);
-      if (wb == 0) {
-        mbar_arrive(&bars[B_EPI_DONE]);
-        mbar_arrive(&bars[B_CS_FREE0 + c % 3]);
-      }
+      if (!more) break;
     }
-    // final state
-    if (!*abort_flag && p.final_state) {
+    // final state S = mu S~ (every MMA on S~ finished before the last O_DONE)
+    if (ok_all && !*abort_flag && p.final_state) {
       tc_fence_after();
       float* fs = p.final_state + ((size_t)n * p.h_v + h) * DK * DV;
 #pragma unroll 1
@@ -908,7 +934,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld_wait();
         if (live) {
 #pragma unroll
-          for (int x = 0; x < 32; ++x) fs[(size_t)(xb * 32 + x) * DV + wb] = __uint_as_float(v[x]);
+          for (int x = 0; x < 32; ++x) fs[(size_t)(xb * 32 + x) * DV + wb] = mu * __uint_as_float(v[x]);
         }
       }
     }

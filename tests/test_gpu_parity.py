@@ -134,6 +134,33 @@ def test_fp32_outputs_bf16_gates_custom_scale(kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("gates", ["steep", "wipes", "mixed_sign"])
+def test_extreme_gates(kernel, gates):
+    """Decays far outside the benchmark range: steep ones (log-decay up to -40
+    per token, so chunks end after a few rows), occasional state wipes
+    (g = -200) and gates of both signs that still decay on average (a state
+    that grows without bound amplifies any rounding). The kernels must still
+    match the oracle, with every exponential factor kept in range."""
+    w = workloads.random_workload([300, 1, 140], h_qk=2, h_v=4, d_k=128, d_v=128, seed=15,
+                                  gate_dtype=torch.float32, out_dtype=torch.float32,
+                                  init_sd=0.05)
+    rng = np.random.default_rng(16)
+    T, H = w.g.shape
+    if gates == "steep":
+        g = -rng.uniform(0.0, 40.0, (T, H))
+    elif gates == "wipes":
+        g = np.where(rng.random((T, H)) < 0.03, -200.0, -0.01)
+    else:  # both signs (G not monotone inside a chunk), decaying on average
+        g = rng.normal(-0.05, 0.15, (T, H))
+    w.g = torch.from_numpy(g.astype(np.float32))
+    o_ref, s_ref = oracle.run_workload(w)
+    o, s = run_lib(w, kernel)
+    # the stated bounds (the fp32 SIMT kernel's tighter in-range bounds do not
+    # apply to decays of e^-40 per token)
+    check(errors(o, s, o_ref, s_ref), "tc", label=f"gates {gates} ({kernel})")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_beta_one_stores_v_on_gpu(kernel):
     """b = 1, q = k (unit): o_t = scale v_t at every token, within bf16."""
     w = workloads.random_workload([150, 70], h_qk=1, h_v=2, d_k=128, d_v=128, seed=9,
