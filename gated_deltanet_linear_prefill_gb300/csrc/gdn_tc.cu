@@ -74,8 +74,9 @@ enum {
   B_FULL0 = 0, B_FULL1, B_FULL2,  // chunk tiles + gate scalars landed (slot c % 3)
   B_KQE0, B_KQE1, B_KQE2,         // K/Q slot released (chunk c's last MMA done)
   B_VE0, B_VE1,                   // V slot released (slot c % 2)
-  B_RQ0, B_RQ1, B_RQ2,            // q norms of slot c % 3 written
-  B_KQ_DONE, B_KQ_FREE, B_W_DONE, B_R_FREE,
+  B_RQ0, B_RQ1, B_RQ2,            // k and q norms of slot c % 3 written
+  B_KQ_DONE, B_KQ_FREE, B_W_DONE, B_R_FREE, B_W_FREE,
+  B_WCONV0, B_WCONV1,             // W'^T of chunk c converted to bf16 (c % 2)
   B_P1_DONE0, B_P1_DONE1,         // chunk prepared (c % 2)
   B_S_READY, B_UP_DONE, B_WFREE0, B_WFREE1, B_UOPS_READY, B_STATE_DONE, B_O_DONE, B_EPI_DONE,
   B_MFREE0, B_MFREE1, B_CSF0, B_CSF1, B_CSF2,
@@ -86,16 +87,17 @@ enum {
 constexpr int SC_G = 0;        // G_i (rows past m repeat G_{m-1})
 constexpr int SC_B = 64;       // beta_i (0 past m)
 constexpr int SC_RQ = 128;     // r^q_i (written by warp 3)
-constexpr int SC_GMAX = 192;   // max / min of G over the chunk's rows
-constexpr int SC_GMIN = 193;
-constexpr int SC_GM = 194;     // G_m
-constexpr int SC_LAMLOG = 195; // log lambda used by s and the output weights (0 when eager)
-constexpr int SC_NULOG = 196;  // log of the W' weight applied to e^{G_j}
-constexpr int SC_RMW = 197;    // factor applied to the stored state first (1 unless eager)
-constexpr int SC_MUNEXT = 198; // mu after this chunk
-constexpr int SC_M = 199;      // rows (int)
-constexpr int SC_FLAGS = 200;  // bit 0: last chunk of the sequence; bit 1: eager
-constexpr int SC_T0 = 202;     // first row (int64, two words)
+constexpr int SC_RK = 192;     // r^k_i (written by warp 3)
+constexpr int SC_GMAX = 256;   // max / min of G over the chunk's rows
+constexpr int SC_GMIN = 257;
+constexpr int SC_GM = 258;     // G_m
+constexpr int SC_LAMLOG = 259; // log lambda used by s and the output weights (0 when eager)
+constexpr int SC_NULOG = 260;  // log of the W' weight applied to e^{G_j}
+constexpr int SC_RMW = 261;    // factor applied to the stored state first (1 unless eager)
+constexpr int SC_MUNEXT = 262; // mu after this chunk
+constexpr int SC_M = 263;      // rows (int)
+constexpr int SC_FLAGS = 264;  // bit 0: last chunk of the sequence; bit 1: eager
+constexpr int SC_T0 = 266;     // first row (int64, two words)
 
 // Per-chunk values WG-A hands to WG-B (three buffers, chunk % 3).
 struct ChunkScalars {
@@ -121,7 +123,7 @@ struct TcLayout {
   static constexpr int NKA = DK / 64;  // 64-element atom columns of K / Q
   static constexpr int NVA = DV / 64;
   static constexpr uint32_t KQ_BYTES = NKA * 16384u;  // [K atom][Q atom] per atom column
-  static constexpr uint32_t SCAL_BYTES = 1024u;
+  static constexpr uint32_t SCAL_BYTES = 2048u;
   static constexpr uint32_t SLOT_BYTES = KQ_BYTES + SCAL_BYTES;
   static constexpr uint32_t V_BYTES = NVA * 8192u;
   static constexpr uint32_t SCR_BYTES = 17408u;           // 64 x 68 fp32, 1024-aligned size
@@ -146,6 +148,7 @@ struct TcLayout {
 
 struct Tmaps {
   CUtensorMap q, k, v;
+  CUtensorMap o;  // out [T, h_v, d_v]: box d_v x 1 head x 32 rows (bf16) or 16 rows (fp32)
 };
 
 // ---------------------------------------------------------------- the solve
@@ -175,6 +178,9 @@ __device__ __forceinline__ void mma_tile(const float* X, int xr, int xc, const f
   const float* x0 = X + (xr + g) * LDF + xc + t;
   const float* x1 = x0 + 8 * LDF;
   const float* y0 = Y + (yr + t) * LDF + yc + g;
+  // the three partial products accumulate separately, so their MMAs do not wait
+  // on one another
+  float c1[4] = {}, c2[4] = {};
 #pragma unroll 1
   for (int k = 0; k < nk8; ++k) {
     uint32_t ah[4], al[4], bh[2], bl[2];
@@ -185,9 +191,11 @@ __device__ __forceinline__ void mma_tile(const float* X, int xr, int xc, const f
     split_tf32(y0[8 * k * LDF], bh[0], bl[0]);
     split_tf32(y0[(8 * k + 4) * LDF], bh[1], bl[1]);
     mma_tf32(c, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
-    mma_tf32(c, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
-    mma_tf32(c, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+    mma_tf32(c1, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+    mma_tf32(c2, al[0], al[1], al[2], al[3], bh[0], bh[1]);
   }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) c[e] += c1[e] + c2[e];
 }
 __device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float (&c)[4], float sgn,
                                            int lane) {
@@ -267,35 +275,32 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, fl
   }
 }
 
-// First row of a 64-row window (cumulative log-decays s0 at row lane, s1 at
-// row lane + 32; mv valid rows) at which the span of {0, G_0 .. G_row}
-// passes kMaxSpan, or 64. Called by a whole warp, only for windows whose
-// span is too wide, so it is kept out of line.
-__device__ __noinline__ int span_limit_row(float s0, float s1, int mv, int lane) {
-  float mx0 = fmaxf(s0, 0.f), mn0 = fminf(s0, 0.f), mx1 = s1, mn1 = s1;
-  for (int o = 1; o < 32; o <<= 1) {
-    const float a0 = __shfl_up_sync(0xffffffffu, mx0, o), a1 = __shfl_up_sync(0xffffffffu, mn0, o);
-    const float a2 = __shfl_up_sync(0xffffffffu, mx1, o), a3 = __shfl_up_sync(0xffffffffu, mn1, o);
-    if (lane >= o) {
-      mx0 = fmaxf(mx0, a0);
-      mn0 = fminf(mn0, a1);
-      mx1 = fmaxf(mx1, a2);
-      mn1 = fminf(mn1, a3);
-    }
-  }
-  mx1 = fmaxf(mx1, __shfl_sync(0xffffffffu, mx0, 31));
-  mn1 = fminf(mn1, __shfl_sync(0xffffffffu, mn0, 31));
-  const unsigned over0 = __ballot_sync(0xffffffffu, lane < mv && mx0 - mn0 > kMaxSpan);
-  const unsigned over1 = __ballot_sync(0xffffffffu, lane + 32 < mv && mx1 - mn1 > kMaxSpan);
-  return over0 ? __ffs(over0) - 1 : (over1 ? 32 + __ffs(over1) - 1 : kChunk);
-}
+// Shared words of the MISC block: the TMEM base, the abort flag, the status
+// pointer and the unit, so that the slow path of a wait needs only addresses.
+constexpr uint32_t MISC_TMEM = 0, MISC_ABORT = 4, MISC_STATUS = 8, MISC_UNIT = 16;
+constexpr uint32_t kDrainWait = 0x8000u;  // site flag: a drain (ignores abort, shorter limit)
 
-// A bounded wait gave up: the CTA reports it once and every role unwinds.
-// Out of line: it only runs on that cold path.
-__device__ __noinline__ void fail_wait(Status* st, volatile int* abort_flag, uint32_t detail) {
-  if (!*abort_flag) {
-    *abort_flag = 1;
-    report(st, GDN_ERR_DEVICE_TIMEOUT, detail);
+// Slow path of every mbarrier wait: polls (each poll may park the thread until
+// the phase completes) until the phase is done, another role has aborted, or
+// the time limit passes. On timeout the CTA reports GDN_ERR_DEVICE_TIMEOUT
+// once (detail: unit * 16 + site) and raises the abort flag so that every role
+// unwinds. Out of line: a wait rarely gets here.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint32_t misc, uint32_t site) {
+  const bool drain = (site & kDrainWait) != 0;
+  const uint64_t limit = drain ? 100000000ull : kWaitLimitNs;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (!drain && ld_shared_volatile_u32(misc + MISC_ABORT)) return false;
+    if (globaltimer() - t0 > limit) {
+      if (!drain && !ld_shared_volatile_u32(misc + MISC_ABORT)) {
+        st_shared_volatile_u32(misc + MISC_ABORT, 1u);
+        Status* st;
+        asm volatile("ld.shared.u64 %0, [%1];" : "=l"(st) : "r"(misc + MISC_STATUS));
+        report(st, GDN_ERR_DEVICE_TIMEOUT, ld_shared_volatile_u32(misc + MISC_UNIT) * 16u + (site & 15u));
+      }
+      return false;
+    }
   }
 }
 
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = smem_u32(sm);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BARS);
   uint32_t* tmem_base_ptr = reinterpret_cast<uint32_t*>(sm + L::MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC + MISC_ABORT);
   ChunkScalars* cscal = reinterpret_cast<ChunkScalars*>(sm + L::CS0);
   PrepScalars* ps = reinterpret_cast<PrepScalars*>(sm + L::PS);
 
@@ -331,6 +336,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], 1u);
     *abort_flag = 0;
+    *reinterpret_cast<Status**>(sm + L::MISC + MISC_STATUS) = p.status;
+    *reinterpret_cast<uint32_t*>(sm + L::MISC + MISC_UNIT) = (uint32_t)unit;
     mbar_init_fence();
   }
   if (L::NEED_ZERO) {
@@ -341,6 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&tm.q);
     tma_prefetch_desc(&tm.k);
     tma_prefetch_desc(&tm.v);
+    tma_prefetch_desc(&tm.o);
   }
   if (warp == 1) tmem_alloc(tmem_base_ptr, kTmemCols);
   tc_fence_before();
@@ -348,14 +356,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_ptr;
 
-  auto fail = [&](int where) { fail_wait(p.status, abort_flag, (uint32_t)(unit * 16 + where)); };
   auto slot_kq = [&](int c) { return sbase + L::RING0 + (uint32_t)(c % 3) * L::SLOT_BYTES; };
   auto slot_v = [&](int c) { return sbase + L::V0 + (uint32_t)(c & 1) * L::V_BYTES; };
   auto slot_sc = [&](int c) {
     return reinterpret_cast<float*>(sm + L::RING0 + (uint32_t)(c % 3) * L::SLOT_BYTES + L::KQ_BYTES);
   };
   auto sc_int = [](const float* sc, int k) { return __float_as_int(sc[k]); };
-  auto wait = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, abort_flag, kWaitLimitNs); };
+  // bounded wait on barrier b; `site` names the wait in a timeout report
+  auto wait = [&](int b, uint32_t parity, uint32_t site) {
+    const uint32_t bar = sbase + L::BARS + 8u * (uint32_t)b;
+    return mbar_try_wait(bar, parity) || wait_slow(bar, parity, sbase + L::MISC, site);
+  };
 
   if (warp == 0) {
     // ================================================================ producer
@@ -380,6 +391,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           b1 = load_gate(p.beta, (bos + st + lane + 32) * p.h_v + h, p.gate_f32);
         }
       };
+#pragma unroll 1
       for (int c = 0;; ++c) {
         load_gates(start);  // the producer runs chunks ahead: this latency is off the critical path
         const int mv = (int)(len - start < kChunk ? len - start : kChunk);
@@ -391,17 +403,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane >= o) { s0 += u0; s1 += u1; }
         }
         s1 += __shfl_sync(0xffffffffu, s0, 31);
-        // span of the whole window (with the chunk start, 0); only a window that is too
-        // wide needs the row where the span first passes the limit
-        float wmax = fmaxf(fmaxf(lane < mv ? s0 : 0.f, lane + 32 < mv ? s1 : 0.f), 0.f);
-        float wmin = fminf(fminf(lane < mv ? s0 : 0.f, lane + 32 < mv ? s1 : 0.f), 0.f);
+        // rows of the chunk: the window, halved while the span of {0, G_0 .. G_{m-1}}
+        // passes kMaxSpan (only decays far outside the usual range get here)
+        int m = mv;
+#pragma unroll 1
+        for (;;) {
+          float wmax = fmaxf(fmaxf(lane < m ? s0 : 0.f, lane + 32 < m ? s1 : 0.f), 0.f);
+          float wmin = fminf(fminf(lane < m ? s0 : 0.f, lane + 32 < m ? s1 : 0.f), 0.f);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-          wmin = fminf(wmin, __shfl_xor_sync(0xffffffffu, wmin, o));
+          for (int o = 16; o > 0; o >>= 1) {
+            wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+            wmin = fminf(wmin, __shfl_xor_sync(0xffffffffu, wmin, o));
+          }
+          if (wmax - wmin <= kMaxSpan || m == 1) break;
+          m = (m + 1) >> 1;
         }
-        const int first = (wmax - wmin > kMaxSpan) ? span_limit_row(s0, s1, mv, lane) : kChunk;
-        const int m = first < 1 ? 1 : (first < mv ? first : mv);
         // rows past m: no decay, no write
         const float Gm = __shfl_sync(0xffffffffu, (m - 1) < 32 ? s0 : s1, (m - 1) & 31);
         if (lane >= m) { s0 = Gm; b0 = 0.f; }
@@ -418,12 +434,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool last = start + m >= len;
         // ring slots: K/Q of chunk c-3 and V of chunk c-2 released
         bool ok = true;
-        if (c >= 3) ok = wait(B_KQE0 + c % 3, ((c / 3) + 1) & 1);
-        if (ok && c >= 2) ok = wait(B_VE0 + (c & 1), ((c >> 1) + 1) & 1);
-        if (!ok) {
-          fail(0);
-          break;
-        }
+        if (c >= 3) ok = wait(B_KQE0 + c % 3, ((c / 3) + 1) & 1, 0);
+        if (ok && c >= 2) ok = wait(B_VE0 + (c & 1), ((c >> 1) + 1) & 1, 0);
+        if (!ok) break;
         float* sc = slot_sc(c);
         sc[SC_G + lane] = s0;
         sc[SC_G + lane + 32] = s1;
@@ -466,14 +479,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // they were all consumed and these return at once)
     if (lane == 0)
       for (int c = issued - 3 < 0 ? 0 : issued - 3; c < issued; ++c)
-        mbar_wait(&bars[B_FULL0 + c % 3], (c / 3) & 1, nullptr, 100000000ull);
+        wait(B_FULL0 + c % 3, (c / 3) & 1, kDrainWait);
   } else if (warp == 1) {
     // ================================================================ [K;Q] K^T
     if (lane == 0 && len > 0) {
       constexpr uint32_t id_kq = idesc_bf16(128, 64, 0, 0);
+#pragma unroll 1
       for (int c = 0;; ++c) {
-        if (!wait(B_FULL0 + c % 3, (c / 3) & 1) || (c >= 1 && !wait(B_KQ_FREE, (c - 1) & 1))) {
-          fail(2);
+        if (!wait(B_FULL0 + c % 3, (c / 3) & 1, 2) || (c >= 1 && !wait(B_KQ_FREE, (c - 1) & 1, 2))) {
           break;
         }
         tc_fence_after();
@@ -488,7 +501,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (sc_int(slot_sc(c), SC_FLAGS) & 1) break;
       }
       mma_commit(&bars[B_DRAIN1]);  // every MMA this thread issued has finished before exit
-      mbar_wait(&bars[B_DRAIN1], 0, nullptr, 100000000ull);
+      wait(B_DRAIN1, 0, kDrainWait);
     }
   } else if (warp == 2) {
     // ================================================================ state-dependent MMAs
@@ -497,10 +510,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t id_qs = idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_st = idesc_bf16(128, DK, 0, 1);
       constexpr uint32_t id_pu = idesc_bf16(128, 64, 0, 0);
+#pragma unroll 1
       for (int c = 0;; ++c) {
         const int par = c & 1;
-        if (!wait(B_P1_DONE0 + par, (c >> 1) & 1) || !wait(B_S_READY, c & 1)) {
-          fail(4);
+        if (!wait(B_P1_DONE0 + par, (c >> 1) & 1, 4) || !wait(B_WCONV0 + par, (c >> 1) & 1, 4) ||
+            !wait(B_S_READY, c & 1, 4)) {
           break;
         }
         tc_fence_after();
@@ -514,8 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mma_commit(&bars[B_UP_DONE]);
         mma_commit(&bars[B_WFREE0 + par]);
         // O^T = S~^T Q^T (raw q tile, K-major), once the last epilogue has read O
-        if (c >= 1 && !wait(B_EPI_DONE, (c - 1) & 1)) {
-          fail(6);
+        if (c >= 1 && !wait(B_EPI_DONE, (c - 1) & 1, 4)) {
           break;
         }
         tc_fence_after();
@@ -524,8 +537,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kk = 0; kk < 4 * L::NKA; ++kk)
           mma_ts(tmem + TM_O, tmem + TM_SB + kk * 8u, sdesc_add(dq, (kk >> 2) * 16384u + (kk & 3) * 32u),
                  id_qs, kk != 0);
-        if (!wait(B_UOPS_READY, c & 1)) {
-          fail(7);
+        if (!wait(B_UOPS_READY, c & 1, 7)) {
           break;
         }
         tc_fence_after();
@@ -545,27 +557,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (last) break;
       }
       mma_commit(&bars[B_DRAIN2]);
-      mbar_wait(&bars[B_DRAIN2], 0, nullptr, 100000000ull);
+      wait(B_DRAIN2, 0, kDrainWait);
     }
   } else if (warp == 3) {
-    // ================================================================ q norms
-    // r^q only weights the output rows, so it is taken here, off the path of
-    // the chunk preparation: sum of squares of each raw q row from the tile.
+    // ================================================================ k and q norms
+    // Sums of squares of each raw k and q row, straight from the tiles, off the
+    // path of the chunk preparation (which reads the scales from the slot).
     if (len > 0) {
+#pragma unroll 1
       for (int c = 0;; ++c) {
         bool ok = true;
-        if (lane == 0) ok = wait(B_FULL0 + c % 3, (c / 3) & 1);
+        if (lane == 0) ok = wait(B_FULL0 + c % 3, (c / 3) & 1, 14);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) {
-          if (lane == 0) fail(14);
-          break;
-        }
-        const uint32_t qt = slot_kq(c) + 8192u;
+        if (!ok) break;
+        float* sc = slot_sc(c);
 #pragma unroll 1
-        for (int rr = 0; rr < 2; ++rr) {
-          const uint32_t row = qt + (uint32_t)(lane + 32 * rr) * 128u;
+        for (int rr = 0; rr < 4; ++rr) {  // k rows lane, lane + 32; then q rows
+          const uint32_t row = slot_kq(c) + (rr >> 1) * 8192u + (uint32_t)(lane + 32 * (rr & 1)) * 128u;
           float a0 = 0.f, a1 = 0.f;
-#pragma unroll 1
+#pragma unroll 4
           for (int k = 0; k < 8 * L::NKA; ++k) {
             // the row's 16-byte pieces in any order (the swizzle only permutes them)
             const int kp = (k & ~7) | ((k + lane) & 7);
@@ -578,9 +588,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               a1 = fmaf(hi, hi, a1);
             }
           }
-          slot_sc(c)[SC_RQ + lane + 32 * rr] = p.l2norm ? 1.0f / sqrtf(a0 + a1 + 1e-6f) : 1.f;
+          sc[((rr >> 1) ? SC_RQ : SC_RK) + lane + 32 * (rr & 1)] = p.l2norm ? 1.0f / sqrtf(a0 + a1 + 1e-6f) : 1.f;
         }
-        float* sc = slot_sc(c);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_RQ0 + c % 3]);
         if (sc_int(sc, SC_FLAGS) & 1) break;
@@ -596,15 +605,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int i = Ln & 63;
     bool issued_mma = false;
     if (len > 0) {
+#pragma unroll 1
       for (int c = 0;; ++c) {
         const int par = c & 1;
-        bool ok = wait(B_FULL0 + c % 3, (c / 3) & 1);
+        bool ok = wait(B_FULL0 + c % 3, (c / 3) & 1, 8);
         // M / staging, W'^T / A and the chunk scalars of this parity were released by chunk c-2 / c-3
-        if (ok && c >= 2) ok = wait(B_MFREE0 + par, ((c >> 1) + 1) & 1);
-        if (ok && c >= 2) ok = wait(B_WFREE0 + par, ((c >> 1) + 1) & 1);
-        if (ok && c >= 3) ok = wait(B_CSF0 + c % 3, ((c / 3) + 1) & 1);
-        if (ok) ok = wait(B_KQ_DONE, c & 1);
-        if (!ok) fail(8);
+        if (ok && c >= 2) ok = wait(B_MFREE0 + par, ((c >> 1) + 1) & 1, 8);
+        if (ok && c >= 2) ok = wait(B_WFREE0 + par, ((c >> 1) + 1) & 1, 8);
+        if (ok && c >= 3) ok = wait(B_CSF0 + c % 3, ((c / 3) + 1) & 1, 8);
+        // T_b / T_w of chunk c-1 read by its W and U products
+        if (ok && c >= 1) ok = wait(B_W_DONE, (c - 1) & 1, 8);
+        if (ok) ok = wait(B_RQ0 + c % 3, (c / 3) & 1, 8);
+        if (ok) ok = wait(B_KQ_DONE, c & 1, 8);
         if (named_bar_or(1, 256, !ok || *abort_flag)) break;
         tc_fence_after();
         const float* sc = slot_sc(c);
@@ -619,20 +631,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         float* Abuf = reinterpret_cast<float*>(sm + L::WT0 + par * L::SCR_BYTES);
         float* Tbuf = reinterpret_cast<float*>(sm + L::TB);
-        if (krow && (i >> 5) == hf) {
-          // r^k_i from the diagonal of K K^T (fp32 sum of exact bf16 products)
-          float diag = 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j == (i & 31)) diag = __uint_as_float(v[j]);
-          const float ri = p.l2norm ? 1.0f / sqrtf(diag + 1e-6f) : 1.f;
-          const float bi = sc[SC_B + i];
-          const bool live = i < m;
-          ps->d[i] = live ? ri * exp2f((gmax - Gi) * kLog2e) : 0.f;
-          ps->r[i] = ri;
-          ps->beta[i] = bi;
-          ps->tw[i] = live ? -bi * ri * exp2f((Gi + sc[SC_NULOG]) * kLog2e) : 0.f;
-          cs.s[i] = live ? ri * exp2f((Gm - Gi - lamlog) * kLog2e) : 0.f;
+        if (wa < 64) {
+          // per-row scalars of the A / T_w / state-update weights
+          const float ri = sc[SC_RK + wa], bi = sc[SC_B + wa], Gw = sc[SC_G + wa];
+          const bool live = wa < m;
+          ps->d[wa] = live ? ri * exp2f((gmax - Gw) * kLog2e) : 0.f;
+          ps->r[wa] = ri;
+          ps->beta[wa] = bi;
+          ps->tw[wa] = live ? -bi * ri * exp2f((Gw + sc[SC_NULOG]) * kLog2e) : 0.f;
+          cs.s[wa] = live ? ri * exp2f((Gm - Gw - lamlog) * kLog2e) : 0.f;
+        } else if (wa < 128) {
+          // output weights
+          const int r = wa - 64;
+          const float Gw = sc[SC_G + r];
+          cs.co[r] = r < m ? p.scale * sc[SC_RQ + r] * exp2f((Gw - Gm + lamlog) * kLog2e) : 0.f;
+          if (r == 0) {
+            cs.t0 = *reinterpret_cast<const long long*>(&sc[SC_T0]);
+            cs.mu_next = sc[SC_MUNEXT];
+            cs.m = m;
+            cs.last = last ? 1 : 0;
+          }
         }
         named_bar_sync(1, 256);
         if (wa == 0) mbar_arrive(&bars[B_KQ_FREE]);  // [K;Q] K^T is in registers
@@ -709,10 +727,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(1, 256);
         // ---- W'^T = K^T T_w^T and U^T = V^T T_b^T, issued from here
+        // (the chunk is published as soon as its products are issued: WG-B converts W'^T)
         if (wa == 0) {
-          if (c >= 1 && !wait(B_R_FREE, (c - 1) & 1)) {
-            fail(10);
-          } else {
+          // R and the W' accumulator were read by WG-B for chunk c-1
+          const bool okw = c < 1 || (wait(B_R_FREE, (c - 1) & 1, 10) && wait(B_W_FREE, (c - 1) & 1, 10));
+          if (okw) {
             tc_fence_after();
             constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
             const uint32_t kq = slot_kq(c), vv = slot_v(c);
@@ -730,49 +749,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_commit(&bars[B_W_DONE]);
             mma_commit(&bars[B_VE0 + par]);
             issued_mma = true;
+            mbar_arrive(&bars[B_P1_DONE0 + par]);
           }
         }
-        ok = wait(B_W_DONE, c & 1);
-        if (!ok) fail(9);
-        if (named_bar_or(1, 256, !ok || *abort_flag)) break;
-        tc_fence_after();
-        // ---- W'^T: TMEM -> bf16 MN-major [d_k][j] (over the A scratch of this parity)
-        {
-          tmem_ld32(tmem + lane_off + TM_W + 32 * hf, v);
-          tmem_ld_wait();
-          const uint32_t wt = sbase + L::WT0 + par * L::SCR_BYTES;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st_shared_v4(wt + sw128(Ln, 4 * hf + q),
-                         pack_bf16(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
-                         pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                         pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                         pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        // ---- output weights (need warp 3's q norms)
-        ok = true;
-        if (!krow && hf == 0) {
-          ok = wait(B_RQ0 + c % 3, (c / 3) & 1);
-          const float rq = sc[SC_RQ + i];
-          cs.co[i] = i < m ? p.scale * rq * exp2f((Gi - Gm + lamlog) * kLog2e) : 0.f;
-          if (i == 0) {
-            cs.t0 = *reinterpret_cast<const long long*>(&sc[SC_T0]);
-            cs.mu_next = sc[SC_MUNEXT];
-            cs.m = m;
-            cs.last = last ? 1 : 0;
-          }
-        }
-        if (!ok) fail(15);
-        if (named_bar_or(1, 256, !ok || *abort_flag)) break;
-        if (wa == 0) mbar_arrive(&bars[B_P1_DONE0 + par]);
         if (last) break;
       }
     }
     if (wa == 0 && issued_mma) {
       mma_commit(&bars[B_DRAINA]);
-      mbar_wait(&bars[B_DRAINA], 0, nullptr, 100000000ull);
+      wait(B_DRAINA, 0, kDrainWait);
     }
   } else {
     // ================================================================ WG-B: state step + epilogue
@@ -798,13 +783,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const size_t osz = p.out_f32 ? 4 : 2;
     const int pieces = (int)(DV * osz / 16);  // 16-byte pieces of one output row
     const int pshift = __ffs(pieces) - 1;
+#pragma unroll 1
     for (int c = -1;; ++c) {
       bool more = len > 0 && c < 0;
       if (c >= 0) {
         // ---- U'^T -> (U' diag(s/lambda))^T as bf16 hi / lo A operands
         const ChunkScalars& cs = cscal[c % 3];
-        bool ok = wait(B_P1_DONE0 + (c & 1), (c >> 1) & 1) && wait(B_UP_DONE, c & 1);
-        if (!ok) fail(12);
+        bool ok = wait(B_P1_DONE0 + (c & 1), (c >> 1) & 1, 12) && wait(B_UP_DONE, c & 1, 12);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
 #pragma unroll 1
@@ -842,9 +827,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---- S~ -> bf16 A operand for chunk c+1 (first applying its decay when eager)
         const int cn = c + 1;
         const float* sc = slot_sc(cn);
-        bool ok = wait(B_FULL0 + cn % 3, (cn / 3) & 1);
-        if (ok && c >= 0) ok = wait(B_STATE_DONE, c & 1);
-        if (!ok) fail(11);
+        bool ok = wait(B_FULL0 + cn % 3, (cn / 3) & 1, 11);
+        if (ok && c >= 0) ok = wait(B_STATE_DONE, c & 1, 11);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
         const bool eager = sc_int(sc, SC_FLAGS) & 2;
@@ -870,48 +854,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (wb == 0) mbar_arrive(&bars[B_S_READY]);
       }
       if (c >= 0) {
-        // ---- epilogue: out_i = co_i O^T_i, staged through the M buffer of this parity
+        // ---- epilogue: out_i = co_i O^T_i, staged through the M buffer of this parity and
+        // written by tensor stores (32 bf16 or 16 fp32 rows per pass); a pass that would run
+        // past the chunk's rows is copied out row by row instead
         const ChunkScalars& cs = cscal[c % 3];
-        bool ok = wait(B_O_DONE, c & 1);
-        if (!ok) fail(13);
+        bool ok = wait(B_O_DONE, c & 1, 13);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
         uint8_t* stage = sm + L::M0 + (c & 1) * 8192u;
         const int m = cs.m;
         const long long t0 = cs.t0;
+        const int PT = p.out_f32 ? 16 : 32;
 #pragma unroll 1
-        for (int p0 = 0; p0 < m; p0 += 16) {
-          uint32_t o[16];
-          tmem_ld16(tmem + lane_off + TM_O + p0, o);
-          tmem_ld_wait();
-          float co[16];
-#pragma unroll
-          for (int t4 = 0; t4 < 4; ++t4) {
-            const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
-            co[4 * t4] = c4.x;
-            co[4 * t4 + 1] = c4.y;
-            co[4 * t4 + 2] = c4.z;
-            co[4 * t4 + 3] = c4.w;
+        for (int p0 = 0; p0 < m; p0 += PT) {
+          if (p0 > 0) {  // the previous pass's store has read the staging rows
+            if (wb == 0) bulk_wait_read();
+            named_bar_sync(2, 128);
           }
+          uint32_t oa[16], ob[16];
+          tmem_ld16(tmem + lane_off + TM_O + p0, oa);
+          if (PT == 32) tmem_ld16(tmem + lane_off + TM_O + p0 + 16, ob);
+          tmem_ld_wait();
           if (live && p.out_f32) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-              reinterpret_cast<float*>(stage)[t * DV + wb] = co[t] * __uint_as_float(o[t]);
+            for (int t4 = 0; t4 < 4; ++t4) {
+              const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
+              float* st = reinterpret_cast<float*>(stage) + (4 * t4) * DV + wb;
+              st[0] = c4.x * __uint_as_float(oa[4 * t4]);
+              st[DV] = c4.y * __uint_as_float(oa[4 * t4 + 1]);
+              st[2 * DV] = c4.z * __uint_as_float(oa[4 * t4 + 2]);
+              st[3 * DV] = c4.w * __uint_as_float(oa[4 * t4 + 3]);
+            }
           } else if (live) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-              reinterpret_cast<__nv_bfloat16*>(stage)[t * DV + wb] = __float2bfloat16_rn(co[t] * __uint_as_float(o[t]));
+            for (int t4 = 0; t4 < 8; ++t4) {
+              const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
+              __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage) + (4 * t4) * DV + wb;
+              const uint32_t* o4 = t4 < 4 ? &oa[4 * t4] : &ob[4 * t4 - 16];
+              st[0] = __float2bfloat16_rn(c4.x * __uint_as_float(o4[0]));
+              st[DV] = __float2bfloat16_rn(c4.y * __uint_as_float(o4[1]));
+              st[2 * DV] = __float2bfloat16_rn(c4.z * __uint_as_float(o4[2]));
+              st[3 * DV] = __float2bfloat16_rn(c4.w * __uint_as_float(o4[3]));
+            }
           }
+          fence_proxy_async_smem();
           named_bar_sync(2, 128);
-          const int rows = m - p0 < 16 ? m - p0 : 16;
-          for (int idx = wb; idx < (rows << pshift); idx += 128) {
-            const int r = idx >> pshift, pc = idx & (pieces - 1);
-            const uint4 x = *reinterpret_cast<const uint4*>(stage + (size_t)r * DV * osz + pc * 16);
-            char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + h) * DV) * osz;
-            *reinterpret_cast<uint4*>(dst + pc * 16) = x;
+          const int rows = m - p0 < PT ? m - p0 : PT;
+          if (rows == PT) {
+            if (wb == 0) {
+              tma_store_3d(&tm.o, stage, 0, h, (int)(t0 + p0));
+              bulk_commit();
+            }
+          } else {
+            for (int idx = wb; idx < (rows << pshift); idx += 128) {
+              const int r = idx >> pshift, pc = idx & (pieces - 1);
+              const uint4 x = *reinterpret_cast<const uint4*>(stage + (size_t)r * DV * osz + pc * 16);
+              char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + h) * DV) * osz;
+              *reinterpret_cast<uint4*>(dst + pc * 16) = x;
+            }
           }
-          named_bar_sync(2, 128);
         }
+        if (wb == 0) bulk_wait_read();  // the M buffer is free again
         tc_fence_before();
         named_bar_sync(2, 128);
         mu = cs.mu_next;
@@ -921,8 +924,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive(&bars[B_CSF0 + c % 3]);
         }
       }
+      if (more) {
+        // ---- W'^T of chunk c+1: TMEM -> bf16 MN-major [d_k][j] (over its A scratch), for
+        // warp 2's U' product; done here so the chunk preparation does not wait for W'
+        const int cn = c + 1, pn = cn & 1;
+        bool ok = wait(B_W_DONE, cn & 1, 15);
+        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        tc_fence_after();
+        const uint32_t wt = sbase + L::WT0 + pn * L::SCR_BYTES;
+#pragma unroll 1
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t w[32];
+          tmem_ld32(tmem + lane_off + TM_W + 32 * hb, w);
+          tmem_ld_wait();
+          if (wb < DK) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(wt + sw128(wb, 4 * hb + q),
+                           pack_bf16(__uint_as_float(w[8 * q + 0]), __uint_as_float(w[8 * q + 1])),
+                           pack_bf16(__uint_as_float(w[8 * q + 2]), __uint_as_float(w[8 * q + 3])),
+                           pack_bf16(__uint_as_float(w[8 * q + 4]), __uint_as_float(w[8 * q + 5])),
+                           pack_bf16(__uint_as_float(w[8 * q + 6]), __uint_as_float(w[8 * q + 7])));
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(2, 128);
+        if (wb == 0) {
+          mbar_arrive(&bars[B_W_FREE]);
+          mbar_arrive(&bars[B_WCONV0 + pn]);
+        }
+      }
       if (!more) break;
     }
+    if (wb == 0) bulk_wait_all();
     // final state S = mu S~ (every MMA on S~ finished before the last O_DONE)
     if (ok_all && !*abort_flag && p.final_state) {
       tc_fence_after();
@@ -976,13 +1011,29 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t T, int H, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// out [T, H, D] (bf16 or fp32) for tensor stores: box = D x 1 head x 32 rows (bf16) or 16 rows
+// (fp32), unswizzled, i.e. the row-major staging tile of one epilogue pass.
+bool encode_out(CUtensorMap* m, void* base, int64_t T, int H, int D, bool f32) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  const cuuint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es};
+  cuuint32_t box[3] = {(cuuint32_t)D, 1, f32 ? 16u : 32u};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DK, int DV>
 cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   using L = TcLayout<DK, DV>;
   Tmaps tm;
   if (!encode_rows(&tm.q, p.q, p.total_tokens, p.h_qk, DK) ||
       !encode_rows(&tm.k, p.k, p.total_tokens, p.h_qk, DK) ||
-      !encode_rows(&tm.v, p.v, p.total_tokens, p.h_v, DV))
+      !encode_rows(&tm.v, p.v, p.total_tokens, p.h_v, DV) ||
+      !encode_out(&tm.o, p.out, p.total_tokens, p.h_v, DV, p.out_f32 != 0))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV>), (int)L::DYN_SMEM);
   if (e != cudaSuccess) return e;

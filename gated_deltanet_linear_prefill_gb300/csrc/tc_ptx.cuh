@@ -57,35 +57,26 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 // One bounded probe of the phase. The suspend-time hint lets the hardware park
 // the thread until the phase completes (or the hint runs out) instead of
 // returning at once, so waiting warps do not spin on the barrier.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
                                               uint32_t suspend_ns = 20000u) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
       : "memory");
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. Gives up when
-// *abort becomes non-zero (abort may be null: drain waits ignore it) or after
-// `limit_ns` of global time; returns false then (the caller reports the
-// timeout and unwinds).
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                           uint64_t limit_ns) {
-  const uint64_t t0 = globaltimer();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (abort && *abort) return false;
-    if (globaltimer() - t0 > limit_ns) return false;
-  }
+// Volatile shared-memory word access by address.
+__device__ __forceinline__ uint32_t ld_shared_volatile_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                         volatile int* abort, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort, limit_ns);
+__device__ __forceinline__ void st_shared_volatile_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- proxies / fences
@@ -116,6 +107,27 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+// Tensor store shared -> global (bulk-group completion). Coordinates must be
+// non-negative; the innermost one times the element size a multiple of 16.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every committed bulk store of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
