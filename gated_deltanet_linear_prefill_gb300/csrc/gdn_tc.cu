@@ -158,9 +158,10 @@ struct Tmaps {
 // Fragment layout (lane = 4 g + t): A rows g, g+8 x columns t, t+4; B rows
 // t, t+4 x column g; C rows g, g+8 x columns 2t, 2t+1.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-  const float r = x - __uint_as_float(hi);
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+  // hi keeps the sign, exponent and top 10 mantissa bits; lo = x - hi is exact in fp32
+  // and enters the MMA as tf32 (its own low bits dropped: about 2^-21 of x)
+  hi = __float_as_uint(x) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
 }
 __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -170,29 +171,39 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// c[16 x 8] += X[xr.., xc + k) * Y[yr + k, yc..) over k in [0, 8 nk8), fp32 smem with row
-// stride LDF.
+// c[16 x 8] += X[xr.., xc + k) * Y[yr + k, yc..) over k in [0, 8 nk8), nk8 <= 4, fp32 smem
+// with row stride LDF. Every operand is loaded and split before the MMAs, and the three
+// partial products accumulate separately, so the steps overlap.
 __device__ __forceinline__ void mma_tile(const float* X, int xr, int xc, const float* Y, int yr,
                                          int yc, int nk8, float (&c)[4], int lane) {
   const int g = lane >> 2, t = lane & 3;
   const float* x0 = X + (xr + g) * LDF + xc + t;
   const float* x1 = x0 + 8 * LDF;
   const float* y0 = Y + (yr + t) * LDF + yc + g;
-  // the three partial products accumulate separately, so their MMAs do not wait
-  // on one another
+  float xa[4][4], yb[4][2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const bool on = k < nk8;
+    xa[k][0] = on ? x0[8 * k] : 0.f;
+    xa[k][1] = on ? x1[8 * k] : 0.f;
+    xa[k][2] = on ? x0[8 * k + 4] : 0.f;
+    xa[k][3] = on ? x1[8 * k + 4] : 0.f;
+    yb[k][0] = on ? y0[8 * k * LDF] : 0.f;
+    yb[k][1] = on ? y0[(8 * k + 4) * LDF] : 0.f;
+  }
   float c1[4] = {}, c2[4] = {};
-#pragma unroll 1
-  for (int k = 0; k < nk8; ++k) {
-    uint32_t ah[4], al[4], bh[2], bl[2];
-    split_tf32(x0[8 * k], ah[0], al[0]);
-    split_tf32(x1[8 * k], ah[1], al[1]);
-    split_tf32(x0[8 * k + 4], ah[2], al[2]);
-    split_tf32(x1[8 * k + 4], ah[3], al[3]);
-    split_tf32(y0[8 * k * LDF], bh[0], bl[0]);
-    split_tf32(y0[(8 * k + 4) * LDF], bh[1], bl[1]);
-    mma_tf32(c, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
-    mma_tf32(c1, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
-    mma_tf32(c2, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < nk8) {
+      uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split_tf32(xa[k][e], ah[e], al[e]);
+      split_tf32(yb[k][0], bh[0], bl[0]);
+      split_tf32(yb[k][1], bh[1], bl[1]);
+      mma_tf32(c, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+      mma_tf32(c1, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+      mma_tf32(c2, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+    }
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) c[e] += c1[e] + c2[e];
@@ -246,7 +257,7 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, fl
   //   pass 3: -T_{rb, 2..rb} (pass 2)            -> T_{rb,cb}
   // with b = 32 (wq >> 1) in step 2 and (rb, cb) = (2 + (wq >> 2), (wq >> 1) & 1) in step 3.
   const int h8 = 8 * (wq & 1);
-#pragma unroll 1
+#pragma unroll
   for (int pass = 0; pass < 4; ++pass) {
     const bool step2 = pass < 2;
     if (!step2 || wq < 4) {
