@@ -74,7 +74,7 @@ enum {
   B_FULL0 = 0, B_FULL1, B_FULL2,  // chunk tiles + gate scalars landed (slot c % 3)
   B_KQE0, B_KQE1, B_KQE2,         // K/Q slot released (chunk c's last MMA done)
   B_VE0, B_VE1,                   // V slot released (slot c % 2)
-  B_RQ0, B_RQ1, B_RQ2,            // k and q norms of slot c % 3 written
+  B_RQ0, B_RQ1, B_RQ2,            // q norms of slot c % 3 written
   B_KQ_DONE, B_KQ_FREE, B_W_DONE, B_R_FREE, B_W_FREE,
   B_WCONV0, B_WCONV1,             // W'^T of chunk c converted to bf16 (c % 2)
   B_P1_DONE0, B_P1_DONE1,         // chunk prepared (c % 2)
@@ -87,7 +87,6 @@ enum {
 constexpr int SC_G = 0;        // G_i (rows past m repeat G_{m-1})
 constexpr int SC_B = 64;       // beta_i (0 past m)
 constexpr int SC_RQ = 128;     // r^q_i (written by warp 3)
-constexpr int SC_RK = 192;     // r^k_i (written by warp 3)
 constexpr int SC_GMAX = 256;   // max / min of G over the chunk's rows
 constexpr int SC_GMIN = 257;
 constexpr int SC_GM = 258;     // G_m
@@ -571,9 +570,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       wait(B_DRAIN2, 0, kDrainWait);
     }
   } else if (warp == 3) {
-    // ================================================================ k and q norms
-    // Sums of squares of each raw k and q row, straight from the tiles, off the
-    // path of the chunk preparation (which reads the scales from the slot).
+    // ================================================================ q norms
+    // Sum of squares of each raw q row (lane and lane + 32), straight from the tile,
+    // off the path of the chunk preparation (r^q only weights the output rows).
     if (len > 0) {
 #pragma unroll 1
       for (int c = 0;; ++c) {
@@ -582,25 +581,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         float* sc = slot_sc(c);
-#pragma unroll 1
-        for (int rr = 0; rr < 4; ++rr) {  // k rows lane, lane + 32; then q rows
-          const uint32_t row = slot_kq(c) + (rr >> 1) * 8192u + (uint32_t)(lane + 32 * (rr & 1)) * 128u;
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll 4
-          for (int k = 0; k < 8 * L::NKA; ++k) {
-            // the row's 16-byte pieces in any order (the swizzle only permutes them)
-            const int kp = (k & ~7) | ((k + lane) & 7);
-            uint32_t x[4];
-            ld_shared_v4(row + (kp >> 3) * 16384u + (kp & 7) * 16u, x[0], x[1], x[2], x[3]);
+        const uint32_t r0 = slot_kq(c) + 8192u + (uint32_t)lane * 128u, r1 = r0 + 32u * 128u;
+        float acc[8] = {};
+#pragma unroll 2
+        for (int k = 0; k < 8 * L::NKA; ++k) {
+          // the row's 16-byte pieces in any order (the swizzle only permutes them)
+          const uint32_t off = (uint32_t)(k >> 3) * 16384u + (uint32_t)(((k + lane) & 7) * 16);
+          uint32_t x[4], y[4];
+          ld_shared_v4(r0 + off, x[0], x[1], x[2], x[3]);
+          ld_shared_v4(r1 + off, y[0], y[1], y[2], y[3]);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = bf16_lo_f(x[e]), hi = bf16_hi_f(x[e]);
-              a0 = fmaf(lo, lo, a0);
-              a1 = fmaf(hi, hi, a1);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float a = bf16_lo_f(x[e]), b = bf16_hi_f(x[e]), cc = bf16_lo_f(y[e]), d = bf16_hi_f(y[e]);
+            acc[e & 1] = fmaf(a, a, acc[e & 1]);
+            acc[2 + (e & 1)] = fmaf(b, b, acc[2 + (e & 1)]);
+            acc[4 + (e & 1)] = fmaf(cc, cc, acc[4 + (e & 1)]);
+            acc[6 + (e & 1)] = fmaf(d, d, acc[6 + (e & 1)]);
           }
-          sc[((rr >> 1) ? SC_RQ : SC_RK) + lane + 32 * (rr & 1)] = p.l2norm ? 1.0f / sqrtf(a0 + a1 + 1e-6f) : 1.f;
         }
+        const float s0 = acc[0] + acc[1] + acc[2] + acc[3], s1 = acc[4] + acc[5] + acc[6] + acc[7];
+        sc[SC_RQ + lane] = p.l2norm ? 1.0f / sqrtf(s0 + 1e-6f) : 1.f;
+        sc[SC_RQ + lane + 32] = p.l2norm ? 1.0f / sqrtf(s1 + 1e-6f) : 1.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_RQ0 + c % 3]);
         if (sc_int(sc, SC_FLAGS) & 1) break;
@@ -642,21 +643,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         float* Abuf = reinterpret_cast<float*>(sm + L::WT0 + par * L::SCR_BYTES);
         float* Tbuf = reinterpret_cast<float*>(sm + L::TB);
-        if (wa < 64) {
+        if (krow && (i >> 5) == hf) {
+          // r^k_i from the diagonal of K K^T (fp32 sum of exact bf16 products), then the
           // per-row scalars of the A / T_w / state-update weights
-          const float ri = sc[SC_RK + wa], bi = sc[SC_B + wa], Gw = sc[SC_G + wa];
-          const bool live = wa < m;
-          ps->d[wa] = live ? ri * exp2f((gmax - Gw) * kLog2e) : 0.f;
-          ps->r[wa] = ri;
-          ps->beta[wa] = bi;
-          ps->tw[wa] = live ? -bi * ri * exp2f((Gw + sc[SC_NULOG]) * kLog2e) : 0.f;
-          cs.s[wa] = live ? ri * exp2f((Gm - Gw - lamlog) * kLog2e) : 0.f;
-        } else if (wa < 128) {
+          float diag = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == (i & 31)) diag = __uint_as_float(v[j]);
+          const float ri = p.l2norm ? 1.0f / sqrtf(diag + 1e-6f) : 1.f;
+          const float bi = sc[SC_B + i];
+          const bool live = i < m;
+          ps->d[i] = live ? ri * exp2f((gmax - Gi) * kLog2e) : 0.f;
+          ps->r[i] = ri;
+          ps->beta[i] = bi;
+          ps->tw[i] = live ? -bi * ri * exp2f((Gi + sc[SC_NULOG]) * kLog2e) : 0.f;
+          cs.s[i] = live ? ri * exp2f((Gm - Gi - lamlog) * kLog2e) : 0.f;
+        } else if (!krow && hf == 0) {
           // output weights
-          const int r = wa - 64;
-          const float Gw = sc[SC_G + r];
-          cs.co[r] = r < m ? p.scale * sc[SC_RQ + r] * exp2f((Gw - Gm + lamlog) * kLog2e) : 0.f;
-          if (r == 0) {
+          cs.co[i] = i < m ? p.scale * sc[SC_RQ + i] * exp2f((Gi - Gm + lamlog) * kLog2e) : 0.f;
+          if (i == 0) {
             cs.t0 = *reinterpret_cast<const long long*>(&sc[SC_T0]);
             cs.mu_next = sc[SC_MUNEXT];
             cs.m = m;
