@@ -78,25 +78,26 @@ enum {
   B_KQ_DONE, B_KQ_FREE, B_W_DONE, B_R_FREE, B_W_FREE,
   B_WCONV0, B_WCONV1,             // W'^T of chunk c converted to bf16 (c % 2)
   B_P1_DONE0, B_P1_DONE1,         // chunk prepared (c % 2)
+  B_T_READY0, B_T_READY1,         // T_b / T_w of chunk c written (c % 2)
   B_S_READY, B_UP_DONE, B_WFREE0, B_WFREE1, B_UOPS_READY, B_STATE_DONE, B_O_DONE, B_EPI_DONE,
   B_MFREE0, B_MFREE1, B_CSF0, B_CSF1, B_CSF2,
-  B_DRAIN1, B_DRAIN2, B_DRAINA, kNumBars
+  B_DRAIN1, B_DRAIN2, kNumBars
 };
 
 // Gate scalars the producer writes next to each K/Q slot (floats).
 constexpr int SC_G = 0;        // G_i (rows past m repeat G_{m-1})
 constexpr int SC_B = 64;       // beta_i (0 past m)
 constexpr int SC_RQ = 128;     // r^q_i (written by warp 3)
-constexpr int SC_GMAX = 256;   // max / min of G over the chunk's rows
-constexpr int SC_GMIN = 257;
-constexpr int SC_GM = 258;     // G_m
-constexpr int SC_LAMLOG = 259; // log lambda used by s and the output weights (0 when eager)
-constexpr int SC_NULOG = 260;  // log of the W' weight applied to e^{G_j}
-constexpr int SC_RMW = 261;    // factor applied to the stored state first (1 unless eager)
-constexpr int SC_MUNEXT = 262; // mu after this chunk
-constexpr int SC_M = 263;      // rows (int)
-constexpr int SC_FLAGS = 264;  // bit 0: last chunk of the sequence; bit 1: eager
-constexpr int SC_T0 = 266;     // first row (int64, two words)
+constexpr int SC_GMAX = 192;   // max / min of G over the chunk's rows
+constexpr int SC_GMIN = 193;
+constexpr int SC_GM = 194;     // G_m
+constexpr int SC_LAMLOG = 195; // log lambda used by s and the output weights (0 when eager)
+constexpr int SC_NULOG = 196;  // log of the W' weight applied to e^{G_j}
+constexpr int SC_RMW = 197;    // factor applied to the stored state first (1 unless eager)
+constexpr int SC_MUNEXT = 198; // mu after this chunk
+constexpr int SC_M = 199;      // rows (int)
+constexpr int SC_FLAGS = 200;  // bit 0: last chunk of the sequence; bit 1: eager
+constexpr int SC_T0 = 202;     // first row (int64, two words)
 
 // Per-chunk values WG-A hands to WG-B (three buffers, chunk % 3).
 struct ChunkScalars {
@@ -122,14 +123,15 @@ struct TcLayout {
   static constexpr int NKA = DK / 64;  // 64-element atom columns of K / Q
   static constexpr int NVA = DV / 64;
   static constexpr uint32_t KQ_BYTES = NKA * 16384u;  // [K atom][Q atom] per atom column
-  static constexpr uint32_t SCAL_BYTES = 2048u;
+  static constexpr uint32_t SCAL_BYTES = 1024u;
   static constexpr uint32_t SLOT_BYTES = KQ_BYTES + SCAL_BYTES;
   static constexpr uint32_t V_BYTES = NVA * 8192u;
   static constexpr uint32_t SCR_BYTES = 17408u;           // 64 x 68 fp32, 1024-aligned size
   static constexpr uint32_t RING0 = 0;                     // K/Q slots x3
   static constexpr uint32_t V0 = 3 * SLOT_BYTES;           // V slots x2
-  static constexpr uint32_t M0 = V0 + 2 * V_BYTES;         // M (bf16 64x64) x2; output staging
-  static constexpr uint32_t TB = M0 + 2 * 8192u;           // fp32 T, then T_b hi / lo
+  static constexpr uint32_t M0 = V0 + 2 * V_BYTES;         // M (bf16 64x64) x2
+  static constexpr uint32_t STG = M0 + 2 * 8192u;          // output staging (one pass)
+  static constexpr uint32_t TB = STG + 8192u;              // fp32 T, then T_b hi / lo
   static constexpr uint32_t TW = TB + SCR_BYTES;           // T_w bf16
   static constexpr uint32_t WT0 = TW + 8192u;              // fp32 A, then W'^T bf16, x2
   static constexpr bool NEED_ZERO = (DK == 64) || (DV == 64);
@@ -491,16 +493,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = issued - 3 < 0 ? 0 : issued - 3; c < issued; ++c)
         wait(B_FULL0 + c % 3, (c / 3) & 1, kDrainWait);
   } else if (warp == 1) {
-    // ================================================================ [K;Q] K^T
+    // ================================================================ state-independent MMAs
+    // [K;Q] K^T of chunk c+1 as soon as its tiles are in and WG-A has read chunk c's;
+    // then W'^T = K^T T_w^T and U^T = V^T T_b^T of chunk c once WG-A has written T_b / T_w.
     if (lane == 0 && len > 0) {
       constexpr uint32_t id_kq = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
-      for (int c = 0;; ++c) {
-        if (!wait(B_FULL0 + c % 3, (c / 3) & 1, 2) || (c >= 1 && !wait(B_KQ_FREE, (c - 1) & 1, 2))) {
-          break;
-        }
-        tc_fence_after();
-        // A = rows of K then Q (K-major), B = K (K-major, N = 64)
+      constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
+      auto issue_kq = [&](int c) {
         const uint64_t dkq = sdesc(slot_kq(c), 16, 1024);
 #pragma unroll 1
         for (int kk = 0; kk < 4 * L::NKA; ++kk) {
@@ -508,7 +507,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_ss(tmem + TM_KQ, d, d, id_kq, kk != 0);
         }
         mma_commit(&bars[B_KQ_DONE]);
-        if (sc_int(slot_sc(c), SC_FLAGS) & 1) break;
+      };
+      bool run = wait(B_FULL0, 0, 2);
+      if (run) {
+        tc_fence_after();
+        issue_kq(0);
+      }
+#pragma unroll 1
+      for (int c = 0; run; ++c) {
+        const int par = c & 1;
+        const bool last = sc_int(slot_sc(c), SC_FLAGS) & 1;
+        if (!last) {
+          if (!wait(B_FULL0 + (c + 1) % 3, ((c + 1) / 3) & 1, 2) || !wait(B_KQ_FREE, c & 1, 2)) break;
+          tc_fence_after();
+          issue_kq(c + 1);
+        }
+        // R and the W' accumulator were read by WG-B for chunk c-1
+        if (!wait(B_T_READY0 + par, (c >> 1) & 1, 10) ||
+            (c >= 1 && (!wait(B_R_FREE, (c - 1) & 1, 10) || !wait(B_W_FREE, (c - 1) & 1, 10))))
+          break;
+        tc_fence_after();
+        const uint32_t kq = slot_kq(c), vv = slot_v(c);
+        const uint32_t lbo_k = (L::NKA == 2) ? 16384u : (sbase + L::ZERO - kq);
+        const uint64_t dka = sdesc(kq, lbo_k, 1024), dtw = sdesc(sbase + L::TW, 16, 1024);
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem + TM_W, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
+        const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
+        const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(sbase + L::TB, 16, 1024);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)  // T_b hi, then lo
+          mma_ss(tmem + TM_R, sdesc_add(dva, (kk & 3) * 2048u), sdesc_add(dtb, (kk >> 2) * 8192u + (kk & 3) * 32u),
+                 id_w, kk != 0);
+        mma_commit(&bars[B_W_DONE]);
+        mma_commit(&bars[B_VE0 + par]);
+        if (last) break;
       }
       mma_commit(&bars[B_DRAIN1]);  // every MMA this thread issued has finished before exit
       wait(B_DRAIN1, 0, kDrainWait);
@@ -564,6 +597,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, (kk & 3) * 32u), id_pu, 1);
         mma_commit(&bars[B_O_DONE]);
         mma_commit(&bars[B_KQE0 + c % 3]);
+        mma_commit(&bars[B_MFREE0 + par]);
         if (last) break;
       }
       mma_commit(&bars[B_DRAIN2]);
@@ -615,7 +649,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_off = (uint32_t)((Ln & ~31) << 16);
     const bool krow = Ln < 64;
     const int i = Ln & 63;
-    bool issued_mma = false;
     if (len > 0) {
 #pragma unroll 1
       for (int c = 0;; ++c) {
@@ -625,8 +658,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ok && c >= 2) ok = wait(B_MFREE0 + par, ((c >> 1) + 1) & 1, 8);
         if (ok && c >= 2) ok = wait(B_WFREE0 + par, ((c >> 1) + 1) & 1, 8);
         if (ok && c >= 3) ok = wait(B_CSF0 + c % 3, ((c / 3) + 1) & 1, 8);
-        // T_b / T_w of chunk c-1 read by its W and U products
-        if (ok && c >= 1) ok = wait(B_W_DONE, (c - 1) & 1, 8);
         if (ok) ok = wait(B_RQ0 + c % 3, (c / 3) & 1, 8);
         if (ok) ok = wait(B_KQ_DONE, c & 1, 8);
         if (named_bar_or(1, 256, !ok || *abort_flag)) break;
@@ -699,7 +730,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 256);
+        // T_b / T_w of chunk c-1 have been read by its W and U products
+        ok = c < 1 || wait(B_W_DONE, (c - 1) & 1, 9);
+        if (named_bar_or(1, 256, !ok || *abort_flag)) break;
         // ---- T = (I + A)^-1
         solve_unit_lower(Abuf, Tbuf, wa);
         // ---- T_b = T diag(beta) as bf16 hi + lo; T_w = T diag(tw)
@@ -743,37 +776,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(1, 256);
         // ---- W'^T = K^T T_w^T and U^T = V^T T_b^T, issued from here
-        // (the chunk is published as soon as its products are issued: WG-B converts W'^T)
+        // T_b / T_w go to warp 1's W and U products; the chunk's scalars and M to the
+        // state step (WG-B converts W'^T)
         if (wa == 0) {
-          // R and the W' accumulator were read by WG-B for chunk c-1
-          const bool okw = c < 1 || (wait(B_R_FREE, (c - 1) & 1, 10) && wait(B_W_FREE, (c - 1) & 1, 10));
-          if (okw) {
-            tc_fence_after();
-            constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
-            const uint32_t kq = slot_kq(c), vv = slot_v(c);
-            const uint32_t lbo_k = (L::NKA == 2) ? 16384u : (sbase + L::ZERO - kq);
-            const uint64_t dka = sdesc(kq, lbo_k, 1024), dtw = sdesc(sbase + L::TW, 16, 1024);
-#pragma unroll 1
-            for (int k = 0; k < 4; ++k)
-              mma_ss(tmem + TM_W, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
-            const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
-            const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(sbase + L::TB, 16, 1024);
-#pragma unroll 1
-            for (int kk = 0; kk < 8; ++kk)  // T_b hi, then lo
-              mma_ss(tmem + TM_R, sdesc_add(dva, (kk & 3) * 2048u), sdesc_add(dtb, (kk >> 2) * 8192u + (kk & 3) * 32u),
-                     id_w, kk != 0);
-            mma_commit(&bars[B_W_DONE]);
-            mma_commit(&bars[B_VE0 + par]);
-            issued_mma = true;
-            mbar_arrive(&bars[B_P1_DONE0 + par]);
-          }
+          mbar_arrive(&bars[B_T_READY0 + par]);
+          mbar_arrive(&bars[B_P1_DONE0 + par]);
         }
         if (last) break;
       }
-    }
-    if (wa == 0 && issued_mma) {
-      mma_commit(&bars[B_DRAINA]);
-      wait(B_DRAINA, 0, kDrainWait);
     }
   } else {
     // ================================================================ WG-B: state step + epilogue
@@ -870,23 +880,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (wb == 0) mbar_arrive(&bars[B_S_READY]);
       }
       if (c >= 0) {
-        // ---- epilogue: out_i = co_i O^T_i, staged through the M buffer of this parity and
-        // written by tensor stores (32 bf16 or 16 fp32 rows per pass); a pass that would run
-        // past the chunk's rows is copied out row by row instead
+        // ---- epilogue: out_i = co_i O^T_i, staged in shared memory and written by tensor
+        // stores (32 bf16 or 16 fp32 rows per pass); a pass that would run past the chunk's
+        // rows is copied out row by row instead
         const ChunkScalars& cs = cscal[c % 3];
         bool ok = wait(B_O_DONE, c & 1, 13);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
-        uint8_t* stage = sm + L::M0 + (c & 1) * 8192u;
+        uint8_t* stage = sm + L::STG;
         const int m = cs.m;
         const long long t0 = cs.t0;
         const int PT = p.out_f32 ? 16 : 32;
 #pragma unroll 1
         for (int p0 = 0; p0 < m; p0 += PT) {
-          if (p0 > 0) {  // the previous pass's store has read the staging rows
-            if (wb == 0) bulk_wait_read();
-            named_bar_sync(2, 128);
-          }
+          // the previous pass's (or chunk's) store has read the staging rows
+          if (wb == 0) bulk_wait_read();
+          named_bar_sync(2, 128);
           uint32_t oa[16], ob[16];
           tmem_ld16(tmem + lane_off + TM_O + p0, oa);
           if (PT == 32) tmem_ld16(tmem + lane_off + TM_O + p0 + 16, ob);
@@ -930,13 +939,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
-        if (wb == 0) bulk_wait_read();  // the M buffer is free again
         tc_fence_before();
         named_bar_sync(2, 128);
         mu = cs.mu_next;
         if (wb == 0) {
           mbar_arrive(&bars[B_EPI_DONE]);
-          mbar_arrive(&bars[B_MFREE0 + (c & 1)]);
           mbar_arrive(&bars[B_CSF0 + c % 3]);
         }
       }
