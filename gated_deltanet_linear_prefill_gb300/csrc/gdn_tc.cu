@@ -403,9 +403,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           b1 = load_gate(p.beta, (bos + st + lane + 32) * p.h_v + h, p.gate_f32);
         }
       };
+      load_gates(0);
 #pragma unroll 1
       for (int c = 0;; ++c) {
-        load_gates(start);  // the producer runs chunks ahead: this latency is off the critical path
         const int mv = (int)(len - start < kChunk ? len - start : kChunk);
         // inclusive prefix sums and prefix max / min (the chunk start, 0, included)
         float s0 = g0, s1 = g1;
@@ -444,6 +444,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float loglam = logmu + Gm;
         const bool eager = fabsf(loglam) > kMaxLogScale;
         const bool last = start + m >= len;
+        const float b0c = b0, b1c = b1;
+        if (!last) load_gates(start + m);  // the next chunk's gates, in flight while this one waits
         // ring slots: K/Q of chunk c-3 and V of chunk c-2 released
         bool ok = true;
         if (c >= 3) ok = wait(B_KQE0 + c % 3, ((c / 3) + 1) & 1, 0);
@@ -452,8 +454,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float* sc = slot_sc(c);
         sc[SC_G + lane] = s0;
         sc[SC_G + lane + 32] = s1;
-        sc[SC_B + lane] = b0;
-        sc[SC_B + lane + 32] = b1;
+        sc[SC_B + lane] = b0c;
+        sc[SC_B + lane + 32] = b1c;
         __syncwarp();  // every lane's scalars before lane 0's arrive publishes them
         if (lane == 0) {
           sc[SC_GMAX] = gmax;
