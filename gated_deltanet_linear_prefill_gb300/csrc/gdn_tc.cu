@@ -28,8 +28,9 @@
 //   O^T   = S~^T Q^T + (U' diag(s/lambda))^T M^T
 //   S~^T += (U' diag(s/lambda))^T K
 // S~^T and U' diag(s/lambda) (bf16 hi + lo) are A operands read straight from
-// TMEM. Operand precision: T and U' s carry about 16 significant bits (hi +
-// lo); S~ and W enter as bf16; every accumulation is fp32. Decays, norms and
+// TMEM. Operand precision: T_b and U' s carry about 16 significant bits (hi +
+// lo) where they feed the state; S~, W, M and the U' s of the intra-chunk
+// output term enter as bf16; every accumulation is fp32. Decays, norms and
 // the 64x64 unit-lower-triangular inverse run on CUDA cores in fp32, the
 // inverse's block merges on the warp-level tensor cores (three-term tf32).
 //
@@ -79,7 +80,7 @@ enum {
   B_WCONV0, B_WCONV1,             // W'^T of chunk c converted to bf16 (c % 2)
   B_P1_DONE0, B_P1_DONE1,         // chunk prepared (c % 2)
   B_T_READY0, B_T_READY1,         // T_b / T_w of chunk c written (c % 2)
-  B_S_READY, B_UP_DONE, B_WFREE0, B_WFREE1, B_UOPS_READY, B_STATE_DONE, B_O_DONE, B_EPI_DONE,
+  B_U_DONE, B_S_READY, B_UP_DONE, B_WFREE0, B_WFREE1, B_UOPS_READY, B_STATE_DONE, B_O_DONE, B_EPI_DONE,
   B_MFREE0, B_MFREE1, B_CSF0, B_CSF1, B_CSF2,
   B_DRAIN1, B_DRAIN2, kNumBars
 };
@@ -130,8 +131,8 @@ struct TcLayout {
   static constexpr uint32_t RING0 = 0;                     // K/Q slots x3
   static constexpr uint32_t V0 = 3 * SLOT_BYTES;           // V slots x2
   static constexpr uint32_t M0 = V0 + 2 * V_BYTES;         // M (bf16 64x64) x2
-  static constexpr uint32_t STG = M0 + 2 * 8192u;          // output staging (one pass)
-  static constexpr uint32_t TB = STG + 8192u;              // fp32 T, then T_b hi / lo
+  static constexpr uint32_t STG = M0 + 2 * 8192u;          // output staging, two tiles
+  static constexpr uint32_t TB = STG + 2 * 8192u;          // fp32 T, then T_b hi / lo
   static constexpr uint32_t TW = TB + SCR_BYTES;           // T_w bf16
   static constexpr uint32_t WT0 = TW + 8192u;              // fp32 A, then W'^T bf16, x2
   static constexpr bool NEED_ZERO = (DK == 64) || (DV == 64);
@@ -222,10 +223,13 @@ __device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float
 //     lane, each row of A read as float4 broadcasts;
 //  2. T_{b+1,b} = -D_{b+1} (A_{b+1,b} D_b) inside both 32x32 diagonal blocks;
 //  3. T_21 = -T_22 (A_21 T_11) for the lower-left 32x32 block.
-// Steps 2 and 3 run on the warp-level tensor cores (three-term tf32). Their
-// intermediate products are parked in T's upper triangle, which nothing reads
-// as T. Blocks above the diagonal are not otherwise written. 256 threads
-// (8 warps); ends with every T entry visible to all of them.
+// Steps 2 and 3 run on the warp-level tensor cores (three-term tf32), one
+// 16x8 tile per warp and product. Their intermediate products are parked in
+// T's upper triangle, which nothing reads as T; blocks above the diagonal are
+// not otherwise written. A warp that reads a parked tile either wrote it
+// itself or waits for its writer on a pair barrier (ids 3-6), so only three
+// barriers span all 256 threads (8 warps). Ends with every T entry visible to
+// all of them.
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ T,
                                                  int wa) {
   const int wq = wa >> 5, ln = wa & 31;
@@ -250,41 +254,36 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, fl
     for (int i = 0; i < 16; ++i) T[(b + i) * LDF + b + l] = t[i];
   }
   named_bar_sync(1, 256);
-  // Steps 2 and 3 as four passes of "c = X * Y over nk8 k-steps, store +-c",
-  // one tile per warp (warps 4-7 sit out the two step-2 passes):
-  //   pass 0: A_{b+1,b} D_b                      -> parked in block (b, b+1)
-  //   pass 1: -D_{b+1} (pass 0)                  -> T_{b+1,b}
-  //   pass 2: A_{rb, cb..1} T_{cb..1, cb}        -> parked in the upper right
-  //   pass 3: -T_{rb, 2..rb} (pass 2)            -> T_{rb,cb}
-  // with b = 32 (wq >> 1) in step 2 and (rb, cb) = (2 + (wq >> 2), (wq >> 1) & 1) in step 3.
-  const int h8 = 8 * (wq & 1);
-#pragma unroll
-  for (int pass = 0; pass < 4; ++pass) {
-    const bool step2 = pass < 2;
-    if (!step2 || wq < 4) {
-      const int b = 32 * (wq >> 1), rb = 2 + (wq >> 2), cb = (wq >> 1) & 1;
-      const float* X;
-      const float* Y;
-      int xr, xc, yr, yc, nk8, sr, sc;
-      float sgn;
-      if (pass == 0) {
-        X = A; xr = b + 16; xc = b; Y = T; yr = b; yc = b + h8; nk8 = 2; sr = b; sc = b + 16 + h8; sgn = 1.f;
-      } else if (pass == 1) {
-        X = T; xr = b + 16; xc = b + 16; Y = T; yr = b; yc = b + 16 + h8; nk8 = 2; sr = b + 16; sc = b + h8;
-        sgn = -1.f;
-      } else if (pass == 2) {
-        X = A; xr = 16 * rb; xc = 16 * cb; Y = T; yr = 16 * cb; yc = 16 * cb + h8; nk8 = 2 * (2 - cb);
-        sr = 16 * (rb - 2); sc = 32 + 16 * cb + h8; sgn = 1.f;
-      } else {
-        X = T; xr = 16 * rb; xc = 32; Y = T; yr = 0; yc = 32 + 16 * cb + h8; nk8 = 2 * (rb - 1);
-        sr = 16 * rb; sc = 16 * cb + h8; sgn = -1.f;
-      }
-      float c[4] = {};
-      mma_tile(X, xr, xc, Y, yr, yc, nk8, c, ln);
-      store_tile(T, sr, sc, c, sgn, ln);
-    }
-    named_bar_sync(1, 256);
+  const int h8 = 8 * (wq & 1);  // which 8 columns of a 16-wide block this warp takes
+  if (wq < 4) {
+    // step 2 in the 32x32 diagonal block at b: P = A_{b+1,b} D_b (parked at block (b, b+1)),
+    // then T_{b+1,b} = -D_{b+1} P; the warp reads back only its own P columns
+    const int b = 32 * (wq >> 1);
+    float c[4] = {}, d[4] = {};
+    mma_tile(A, b + 16, b, T, b, b + h8, 2, c, ln);
+    store_tile(T, b, b + 16 + h8, c, 1.f, ln);
+    __syncwarp();
+    mma_tile(T, b + 16, b + 16, T, b, b + 16 + h8, 2, d, ln);
+    store_tile(T, b + 16, b + h8, d, -1.f, ln);
   }
+  named_bar_sync(1, 256);
+  {
+    // step 3 for row block rb in {2, 3}, column block cb in {0, 1}:
+    // Z_rb = A_{rb, cb..1} T_{cb..1, cb} (parked in row block rb - 2 of the upper right),
+    // then T_{rb,cb} = -T_{rb, 2..rb} Z_{2..rb}; row block 3 also needs row block 2's Z
+    const int rb = 2 + (wq >> 2), cb = (wq >> 1) & 1;
+    float c[4] = {}, d[4] = {};
+    mma_tile(A, 16 * rb, 16 * cb, T, 16 * cb, 16 * cb + h8, 2 * (2 - cb), c, ln);
+    store_tile(T, 16 * (rb - 2), 32 + 16 * cb + h8, c, 1.f, ln);
+    if (rb == 2)
+      named_bar_arrive(3 + (wq & 3), 64);
+    else
+      named_bar_sync(3 + (wq & 3), 64);
+    __syncwarp();
+    mma_tile(T, 16 * rb, 32, T, 0, 32 + 16 * cb + h8, 2 * (rb - 1), d, ln);
+    store_tile(T, 16 * rb, 16 * cb + h8, d, -1.f, ln);
+  }
+  named_bar_sync(1, 256);
 }
 
 // Shared words of the MISC block: the TMEM base, the abort flag, the status
@@ -535,13 +534,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
         for (int k = 0; k < 4; ++k)
           mma_ss(tmem + TM_W, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
+        mma_commit(&bars[B_W_DONE]);  // W'^T may be converted while U is still running
         const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
         const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(sbase + L::TB, 16, 1024);
 #pragma unroll 1
         for (int kk = 0; kk < 8; ++kk)  // T_b hi, then lo
           mma_ss(tmem + TM_R, sdesc_add(dva, (kk & 3) * 2048u), sdesc_add(dtb, (kk >> 2) * 8192u + (kk & 3) * 32u),
                  id_w, kk != 0);
-        mma_commit(&bars[B_W_DONE]);
+        mma_commit(&bars[B_U_DONE]);
         mma_commit(&bars[B_VE0 + par]);
         if (last) break;
       }
@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0;; ++c) {
         const int par = c & 1;
         if (!wait(B_P1_DONE0 + par, (c >> 1) & 1, 4) || !wait(B_WCONV0 + par, (c >> 1) & 1, 4) ||
-            !wait(B_S_READY, c & 1, 4)) {
+            !wait(B_U_DONE, c & 1, 4) || !wait(B_S_READY, c & 1, 4)) {
           break;
         }
         tc_fence_after();
@@ -592,11 +592,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kk = 0; kk < 8; ++kk)  // hi (kk < 4), then lo
           mma_ts(tmem + TM_S, tmem + TM_UH + kk * 8u, sdesc_add(dkn, (kk & 3) * 2048u), id_st, 1);
         mma_commit(&bars[B_STATE_DONE]);
-        // O^T += (U' s)^T M^T : B = M K-major [i][j]
+        // O^T += (U' s)^T M^T : B = M K-major [i][j]; the hi part of U' s only, since
+        // this term reaches the output alone (M itself is bf16)
         const uint64_t dm = sdesc(sbase + L::M0 + par * 8192u, 16, 1024);
 #pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, (kk & 3) * 32u), id_pu, 1);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, kk * 32u), id_pu, 1);
         mma_commit(&bars[B_O_DONE]);
         mma_commit(&bars[B_KQE0 + c % 3]);
         mma_commit(&bars[B_MFREE0 + par]);
@@ -656,7 +657,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0;; ++c) {
         const int par = c & 1;
         bool ok = wait(B_FULL0 + c % 3, (c / 3) & 1, 8);
-        // M / staging, W'^T / A and the chunk scalars of this parity were released by chunk c-2 / c-3
+        // M, W'^T / A and the chunk scalars of this parity were released by chunk c-2 / c-3
         if (ok && c >= 2) ok = wait(B_MFREE0 + par, ((c >> 1) + 1) & 1, 8);
         if (ok && c >= 2) ok = wait(B_WFREE0 + par, ((c >> 1) + 1) & 1, 8);
         if (ok && c >= 3) ok = wait(B_CSF0 + c % 3, ((c / 3) + 1) & 1, 8);
@@ -732,8 +733,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        // T_b / T_w of chunk c-1 have been read by its W and U products
-        ok = c < 1 || wait(B_W_DONE, (c - 1) & 1, 9);
+        // T_b / T_w of chunk c-1 have been read by its W and U products (the solve
+        // overwrites them); A is complete once every thread passes this barrier
+        ok = c < 1 || wait(B_U_DONE, (c - 1) & 1, 9);
         if (named_bar_or(1, 256, !ok || *abort_flag)) break;
         // ---- T = (I + A)^-1
         solve_unit_lower(Abuf, Tbuf, wa);
@@ -811,6 +813,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const size_t osz = p.out_f32 ? 4 : 2;
     const int pieces = (int)(DV * osz / 16);  // 16-byte pieces of one output row
     const int pshift = __ffs(pieces) - 1;
+    uint32_t npass = 0;  // epilogue passes so far (selects the staging tile)
 #pragma unroll 1
     for (int c = -1;; ++c) {
       bool more = len > 0 && c < 0;
@@ -881,22 +884,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_bar_sync(2, 128);
         if (wb == 0) mbar_arrive(&bars[B_S_READY]);
       }
+      if (more) {
+        // ---- W'^T of chunk c+1: TMEM -> bf16 MN-major [d_k][j] (over its A scratch), for
+        // warp 2's U' product, ahead of chunk c's epilogue so that the U' product of
+        // chunk c+1 runs while the outputs of chunk c are written
+        const int cn = c + 1, pn = cn & 1;
+        bool ok = wait(B_W_DONE, cn & 1, 15);
+        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        tc_fence_after();
+        const uint32_t wt = sbase + L::WT0 + pn * L::SCR_BYTES;
+#pragma unroll 1
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t w[32];
+          tmem_ld32(tmem + lane_off + TM_W + 32 * hb, w);
+          tmem_ld_wait();
+          if (wb < DK) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(wt + sw128(wb, 4 * hb + q),
+                           pack_bf16(__uint_as_float(w[8 * q + 0]), __uint_as_float(w[8 * q + 1])),
+                           pack_bf16(__uint_as_float(w[8 * q + 2]), __uint_as_float(w[8 * q + 3])),
+                           pack_bf16(__uint_as_float(w[8 * q + 4]), __uint_as_float(w[8 * q + 5])),
+                           pack_bf16(__uint_as_float(w[8 * q + 6]), __uint_as_float(w[8 * q + 7])));
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(2, 128);
+        if (wb == 0) {
+          mbar_arrive(&bars[B_W_FREE]);
+          mbar_arrive(&bars[B_WCONV0 + pn]);
+        }
+      }
       if (c >= 0) {
         // ---- epilogue: out_i = co_i O^T_i, staged in shared memory and written by tensor
-        // stores (32 bf16 or 16 fp32 rows per pass); a pass that would run past the chunk's
-        // rows is copied out row by row instead
+        // stores (32 bf16 or 16 fp32 rows per pass). The passes alternate between two
+        // staging tiles, so a pass waits only for the store of two passes before. A pass
+        // that would run past the chunk's rows is copied out row by row instead.
         const ChunkScalars& cs = cscal[c % 3];
         bool ok = wait(B_O_DONE, c & 1, 13);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
-        uint8_t* stage = sm + L::STG;
         const int m = cs.m;
         const long long t0 = cs.t0;
         const int PT = p.out_f32 ? 16 : 32;
 #pragma unroll 1
-        for (int p0 = 0; p0 < m; p0 += PT) {
-          // the previous pass's (or chunk's) store has read the staging rows
-          if (wb == 0) bulk_wait_read();
+        for (int p0 = 0; p0 < m; p0 += PT, ++npass) {
+          uint8_t* stage = sm + L::STG + (npass & 1) * 8192u;
+          // the store that last used this tile has read it (one store group per pass)
+          if (wb == 0) bulk_wait_read_1();
           named_bar_sync(2, 128);
           uint32_t oa[16], ob[16];
           tmem_ld16(tmem + lane_off + TM_O + p0, oa);
@@ -928,10 +964,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           named_bar_sync(2, 128);
           const int rows = m - p0 < PT ? m - p0 : PT;
           if (rows == PT) {
-            if (wb == 0) {
-              tma_store_3d(&tm.o, stage, 0, h, (int)(t0 + p0));
-              bulk_commit();
-            }
+            if (wb == 0) tma_store_3d(&tm.o, stage, 0, h, (int)(t0 + p0));
           } else {
             for (int idx = wb; idx < (rows << pshift); idx += 128) {
               const int r = idx >> pshift, pc = idx & (pieces - 1);
@@ -940,6 +973,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               *reinterpret_cast<uint4*>(dst + pc * 16) = x;
             }
           }
+          if (wb == 0) bulk_commit();  // empty for a copied pass
         }
         tc_fence_before();
         named_bar_sync(2, 128);
@@ -947,37 +981,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (wb == 0) {
           mbar_arrive(&bars[B_EPI_DONE]);
           mbar_arrive(&bars[B_CSF0 + c % 3]);
-        }
-      }
-      if (more) {
-        // ---- W'^T of chunk c+1: TMEM -> bf16 MN-major [d_k][j] (over its A scratch), for
-        // warp 2's U' product; done here so the chunk preparation does not wait for W'
-        const int cn = c + 1, pn = cn & 1;
-        bool ok = wait(B_W_DONE, cn & 1, 15);
-        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
-        tc_fence_after();
-        const uint32_t wt = sbase + L::WT0 + pn * L::SCR_BYTES;
-#pragma unroll 1
-        for (int hb = 0; hb < 2; ++hb) {
-          uint32_t w[32];
-          tmem_ld32(tmem + lane_off + TM_W + 32 * hb, w);
-          tmem_ld_wait();
-          if (wb < DK) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_shared_v4(wt + sw128(wb, 4 * hb + q),
-                           pack_bf16(__uint_as_float(w[8 * q + 0]), __uint_as_float(w[8 * q + 1])),
-                           pack_bf16(__uint_as_float(w[8 * q + 2]), __uint_as_float(w[8 * q + 3])),
-                           pack_bf16(__uint_as_float(w[8 * q + 4]), __uint_as_float(w[8 * q + 5])),
-                           pack_bf16(__uint_as_float(w[8 * q + 6]), __uint_as_float(w[8 * q + 7])));
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(2, 128);
-        if (wb == 0) {
-          mbar_arrive(&bars[B_W_FREE]);
-          mbar_arrive(&bars[B_WCONV0 + pn]);
         }
       }
       if (!more) break;

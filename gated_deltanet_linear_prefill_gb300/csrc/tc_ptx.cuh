@@ -86,6 +86,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrives at a named barrier without waiting: the producer half of a
+// producer / consumer pair (the consumer calls named_bar_sync with the same
+// count). The producer's earlier shared-memory writes are visible to the
+// consumer once its named_bar_sync returns.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 // Named barrier that also ORs a predicate over the participating threads, so
 // that every one of them takes the same branch afterwards.
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
@@ -124,6 +131,11 @@ __device__ __forceinline__ void bulk_commit() {
 // Waits until every committed bulk store of this thread has read its source.
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed bulk store of this thread but the most recent
+// one has read its source.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {
