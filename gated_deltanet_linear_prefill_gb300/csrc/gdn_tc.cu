@@ -32,7 +32,8 @@
 // lo) where they feed the state; S~, W, M and the U' s of the intra-chunk
 // output term enter as bf16; every accumulation is fp32. Decays, norms and
 // the 64x64 unit-lower-triangular inverse run on CUDA cores in fp32, the
-// inverse's block merges on the warp-level tensor cores (three-term tf32).
+// inverse's block merges on the warp-level tensor cores (tf32 operands, fp32
+// accumulation; the merged blocks carry about 11 significant bits).
 //
 // Warp roles (512 threads): warp 0 scans the gates, sizes the chunks and loads
 // K/Q/V tiles by TMA (128-byte swizzle) into a 3-deep K/Q ring and a 2-deep V
@@ -103,7 +104,6 @@ constexpr int SC_T0 = 202;     // first row (int64, two words)
 // Per-chunk values WG-A hands to WG-B (three buffers, chunk % 3).
 struct ChunkScalars {
   float co[64];  // scale r^q_i e^{G_i - G_m} lambda: output weight of row i (0 past m)
-  float s[64];   // e^{G_m - G_j} r^k_j / lambda: weight of u'_j (0 past m)
   long long t0;  // first row of the chunk
   float mu_next; // mu after the chunk
   int m, last, pad[3];
@@ -114,6 +114,7 @@ struct PrepScalars {
   float r[64];     // r^k_j
   float tw[64];    // column scale of T_w
   float beta[64];
+  float s[64];     // e^{G_m - G_j} r^k_j / lambda: weight of u'_j (0 past m), the row scale of T_b, T_w
 };
 
 constexpr int LDF = 68;  // row stride (floats) of the fp32 64x64 scratch of the solve
@@ -153,18 +154,15 @@ struct Tmaps {
   CUtensorMap o;  // out [T, h_v, d_v]: box d_v x 1 head x 32 rows (bf16) or 16 rows (fp32)
 };
 
+// v, or 0 when `zero` (a block above the diagonal, whose T entries are parked products).
+__device__ __forceinline__ float zero_row(float v, bool zero) { return zero ? 0.f : v; }
+
 // ---------------------------------------------------------------- the solve
 // Warp-level tensor-core tiles for the block merges: mma.sync m16n8k8 with
-// tf32 operands, each fp32 operand split as hi + lo (both tf32) and the
-// product taken as hi*hi + hi*lo + lo*hi, which keeps close to fp32 accuracy.
-// Fragment layout (lane = 4 g + t): A rows g, g+8 x columns t, t+4; B rows
-// t, t+4 x column g; C rows g, g+8 x columns 2t, 2t+1.
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  // hi keeps the sign, exponent and top 10 mantissa bits; lo = x - hi is exact in fp32
-  // and enters the MMA as tf32 (its own low bits dropped: about 2^-21 of x)
-  hi = __float_as_uint(x) & 0xffffe000u;
-  lo = __float_as_uint(x - __uint_as_float(hi));
-}
+// tf32 operands taken straight from the fp32 values in shared memory (the
+// tensor cores read the top 19 bits), fp32 accumulation. Every T entry itself
+// stays fp32. Fragment layout (lane = 4 g + t): A rows g, g+8 x columns t, t+4;
+// B rows t, t+4 x column g; C rows g, g+8 x columns 2t, 2t+1.
 __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -174,41 +172,28 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 // c[16 x 8] += X[xr.., xc + k) * Y[yr + k, yc..) over k in [0, 8 nk8), nk8 <= 4, fp32 smem
-// with row stride LDF. Every operand is loaded and split before the MMAs, and the three
-// partial products accumulate separately, so the steps overlap.
+// with row stride LDF. Every operand is loaded before the first product.
 __device__ __forceinline__ void mma_tile(const float* X, int xr, int xc, const float* Y, int yr,
                                          int yc, int nk8, float (&c)[4], int lane) {
   const int g = lane >> 2, t = lane & 3;
   const float* x0 = X + (xr + g) * LDF + xc + t;
   const float* x1 = x0 + 8 * LDF;
   const float* y0 = Y + (yr + t) * LDF + yc + g;
-  float xa[4][4], yb[4][2];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const bool on = k < nk8;
-    xa[k][0] = on ? x0[8 * k] : 0.f;
-    xa[k][1] = on ? x1[8 * k] : 0.f;
-    xa[k][2] = on ? x0[8 * k + 4] : 0.f;
-    xa[k][3] = on ? x1[8 * k + 4] : 0.f;
-    yb[k][0] = on ? y0[8 * k * LDF] : 0.f;
-    yb[k][1] = on ? y0[(8 * k + 4) * LDF] : 0.f;
-  }
-  float c1[4] = {}, c2[4] = {};
+  uint32_t xa[4][4], yb[4][2];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if (k < nk8) {
-      uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) split_tf32(xa[k][e], ah[e], al[e]);
-      split_tf32(yb[k][0], bh[0], bl[0]);
-      split_tf32(yb[k][1], bh[1], bl[1]);
-      mma_tf32(c, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
-      mma_tf32(c1, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
-      mma_tf32(c2, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+      xa[k][0] = __float_as_uint(x0[8 * k]);
+      xa[k][1] = __float_as_uint(x1[8 * k]);
+      xa[k][2] = __float_as_uint(x0[8 * k + 4]);
+      xa[k][3] = __float_as_uint(x1[8 * k + 4]);
+      yb[k][0] = __float_as_uint(y0[8 * k * LDF]);
+      yb[k][1] = __float_as_uint(y0[(8 * k + 4) * LDF]);
     }
   }
 #pragma unroll
-  for (int e = 0; e < 4; ++e) c[e] += c1[e] + c2[e];
+  for (int k = 0; k < 4; ++k)
+    if (k < nk8) mma_tf32(c, xa[k][0], xa[k][1], xa[k][2], xa[k][3], yb[k][0], yb[k][1]);
 }
 __device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float (&c)[4], float sgn,
                                            int lane) {
@@ -220,11 +205,11 @@ __device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float
 // T = (I + A)^-1 for the strictly-lower 64x64 A (fp32, stride LDF), in 16x16
 // blocks (the blocked order of the open-jev-fast README's GDN kernel):
 //  1. the four diagonal blocks D_b by forward substitution, one column per
-//     lane, each row of A read as float4 broadcasts;
+//     lane (two blocks per warp), each row of A read as float4 broadcasts;
 //  2. T_{b+1,b} = -D_{b+1} (A_{b+1,b} D_b) inside both 32x32 diagonal blocks;
 //  3. T_21 = -T_22 (A_21 T_11) for the lower-left 32x32 block.
-// Steps 2 and 3 run on the warp-level tensor cores (three-term tf32), one
-// 16x8 tile per warp and product. Their intermediate products are parked in
+// Steps 2 and 3 run on the warp-level tensor cores (tf32 operands, fp32
+// accumulation), one 16x8 tile per warp and product. Their intermediate products are parked in
 // T's upper triangle, which nothing reads as T; blocks above the diagonal are
 // not otherwise written. A warp that reads a parked tile either wrote it
 // itself or waits for its writer on a pair barrier (ids 3-6), so only three
@@ -233,8 +218,9 @@ __device__ __forceinline__ void store_tile(float* M, int r0, int c0, const float
 __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ T,
                                                  int wa) {
   const int wq = wa >> 5, ln = wa & 31;
-  if (wq < 4 && ln < 16) {
-    const int b = 16 * wq, l = ln;  // lane l owns column l of D_wq
+  if (wq < 2) {
+    // warp wq inverts blocks 2 wq (lanes 0-15) and 2 wq + 1 (lanes 16-31)
+    const int b = 32 * wq + 16 * (ln >> 4), l = ln & 15;  // lane owns column l of its block
     float t[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -351,10 +337,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     *reinterpret_cast<uint32_t*>(sm + L::MISC + MISC_UNIT) = (uint32_t)unit;
     mbar_init_fence();
   }
-  if (L::NEED_ZERO) {
+  if (L::NEED_ZERO)
     for (int i = tid; i < 8192 / 16; i += kTcThreads) st_shared_v4(sbase + L::ZERO + i * 16, 0, 0, 0, 0);
-    fence_proxy_async_smem();
-  }
+  for (int i = tid; i < 2 * 8192 / 16; i += kTcThreads) st_shared_v4(sbase + L::M0 + i * 16, 0, 0, 0, 0);
+  fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm.q);
     tma_prefetch_desc(&tm.k);
@@ -608,9 +594,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 3) {
     // ================================================================ q norms
-    // Sum of squares of each raw q row (lane and lane + 32), straight from the tile,
+    // r^q_i from the diagonal of Q Q^T, 16 rows at a time on the warp-level tensor
+    // cores (bf16 products are exact in fp32), straight from the swizzled tile and
     // off the path of the chunk preparation (r^q only weights the output rows).
     if (len > 0) {
+      const int g = lane >> 2, t = lane & 3;
+      // ldmatrix rows: matrices 0 / 1 are rows 0-7 / 8-15 of k 0-7, 2 / 3 the same of k 8-15
+      const uint32_t lr = (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1)), lk = (uint32_t)(lane >> 4);
 #pragma unroll 1
       for (int c = 0;; ++c) {
         bool ok = true;
@@ -618,27 +608,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         float* sc = slot_sc(c);
-        const uint32_t r0 = slot_kq(c) + 8192u + (uint32_t)lane * 128u, r1 = r0 + 32u * 128u;
-        float acc[8] = {};
-#pragma unroll 2
-        for (int k = 0; k < 8 * L::NKA; ++k) {
-          // the row's 16-byte pieces in any order (the swizzle only permutes them)
-          const uint32_t off = (uint32_t)(k >> 3) * 16384u + (uint32_t)(((k + lane) & 7) * 16);
-          uint32_t x[4], y[4];
-          ld_shared_v4(r0 + off, x[0], x[1], x[2], x[3]);
-          ld_shared_v4(r1 + off, y[0], y[1], y[2], y[3]);
+        const uint32_t qa = slot_kq(c) + 8192u;  // Q atom 0 (atom a at + 16384 a)
+#pragma unroll 1
+        for (int rb = 0; rb < 4; ++rb) {
+          const uint32_t r = 16u * rb + lr;
+          float d0[4] = {}, d1[4] = {};  // columns 0-7 and 8-15 of the 16 x 16 block
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = bf16_lo_f(x[e]), b = bf16_hi_f(x[e]), cc = bf16_lo_f(y[e]), d = bf16_hi_f(y[e]);
-            acc[e & 1] = fmaf(a, a, acc[e & 1]);
-            acc[2 + (e & 1)] = fmaf(b, b, acc[2 + (e & 1)]);
-            acc[4 + (e & 1)] = fmaf(cc, cc, acc[4 + (e & 1)]);
-            acc[6 + (e & 1)] = fmaf(d, d, acc[6 + (e & 1)]);
+          for (int s = 0; s < 4 * L::NKA; ++s) {
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(qa + (uint32_t)(s >> 2) * 16384u + sw128(r, 2u * (s & 3) + lk), a0, a1, a2, a3);
+            mma_bf16_16816(d0, a0, a1, a2, a3, a0, a2);  // B = rows 0-7 of the block
+            mma_bf16_16816(d1, a0, a1, a2, a3, a1, a3);  // B = rows 8-15
+          }
+          if (t == (g >> 1)) {  // this lane holds (g, g) and (g + 8, g + 8)
+            const float q0 = (g & 1) ? d0[1] : d0[0], q1 = (g & 1) ? d1[3] : d1[2];
+            sc[SC_RQ + 16 * rb + g] = p.l2norm ? 1.0f / sqrtf(q0 + 1e-6f) : 1.f;
+            sc[SC_RQ + 16 * rb + g + 8] = p.l2norm ? 1.0f / sqrtf(q1 + 1e-6f) : 1.f;
           }
         }
-        const float s0 = acc[0] + acc[1] + acc[2] + acc[3], s1 = acc[4] + acc[5] + acc[6] + acc[7];
-        sc[SC_RQ + lane] = p.l2norm ? 1.0f / sqrtf(s0 + 1e-6f) : 1.f;
-        sc[SC_RQ + lane + 32] = p.l2norm ? 1.0f / sqrtf(s1 + 1e-6f) : 1.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_RQ0 + c % 3]);
         if (sc_int(sc, SC_FLAGS) & 1) break;
@@ -691,7 +678,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ps->r[i] = ri;
           ps->beta[i] = bi;
           ps->tw[i] = live ? -bi * ri * exp2f((Gi + sc[SC_NULOG]) * kLog2e) : 0.f;
-          cs.s[i] = live ? ri * exp2f((Gm - Gi - lamlog) * kLog2e) : 0.f;
+          ps->s[i] = live ? ri * exp2f((Gm - Gi - lamlog) * kLog2e) : 0.f;
         } else if (!krow && hf == 0) {
           // output weights
           cs.co[i] = i < m ? p.scale * sc[SC_RQ + i] * exp2f((Gi - Gm + lamlog) * kLog2e) : 0.f;
@@ -704,7 +691,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_bar_sync(1, 256);
         if (wa == 0) mbar_arrive(&bars[B_KQ_FREE]);  // [K;Q] K^T is in registers
-        if (krow) {
+        // A above the block diagonal (rows 0-31, columns 32-63) is never read, and M there is
+        // always zero (cleared once at the start): those two warps have nothing to write
+        const bool upper = hf == 1 && (Ln & 63) < 32;
+        if (krow && !upper) {
           // A_ij = beta_i r_i r_j e^{G_i - G_j} k_i.k_j  (j < i < m), fp32 into the scratch
           const float cia = i < m ? ps->beta[i] * ps->r[i] * exp2f((Gi - gmax) * kLog2e) : 0.f;
 #pragma unroll
@@ -718,7 +708,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               a4[e] = (j0 + e < i) ? (cia * __uint_as_float(v[4 * q + e])) * dd[e] : 0.f;
             *reinterpret_cast<float4*>(&Abuf[i * LDF + j0]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
           }
-        } else {
+        } else if (!krow && !upper) {
           // M_ij = q_i.k_j  (j <= i), bf16 K-major [i][j]
           const uint32_t mrow = sbase + L::M0 + par * 8192u;
 #pragma unroll
@@ -742,15 +732,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---- T_b = T diag(beta) as bf16 hi + lo; T_w = T diag(tw)
         {
           const int ti = wa & 63, qq = wa >> 6;  // row ti, columns [16 qq, 16 qq + 16)
+          // row ti carries the state-update weight s_ti (so U' and W' come out of their
+          // products already multiplied by diag(s / lambda))
+          const float si = zero_row(ps->s[ti], qq > (ti >> 4));
           float t[16];
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const float4 x = *reinterpret_cast<const float4*>(&Tbuf[ti * LDF + 16 * qq + 4 * k4]);
-            const bool zero = qq > (ti >> 4);  // block above the diagonal
-            t[4 * k4 + 0] = zero ? 0.f : x.x;
-            t[4 * k4 + 1] = zero ? 0.f : x.y;
-            t[4 * k4 + 2] = zero ? 0.f : x.z;
-            t[4 * k4 + 3] = zero ? 0.f : x.w;
+            t[4 * k4 + 0] = si * x.x;
+            t[4 * k4 + 1] = si * x.y;
+            t[4 * k4 + 2] = si * x.z;
+            t[4 * k4 + 3] = si * x.w;
           }
           named_bar_sync(1, 256);  // every thread has read T before it is overwritten
           const uint32_t tb = sbase + L::TB;
@@ -818,7 +810,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int c = -1;; ++c) {
       bool more = len > 0 && c < 0;
       if (c >= 0) {
-        // ---- U'^T -> (U' diag(s/lambda))^T as bf16 hi / lo A operands
+        // ---- (U' diag(s/lambda))^T -> bf16 hi / lo A operands
         const ChunkScalars& cs = cscal[c % 3];
         bool ok = wait(B_P1_DONE0 + (c & 1), (c >> 1) & 1, 12) && wait(B_UP_DONE, c & 1, 12);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
@@ -830,17 +822,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_ld_wait();
           uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 s4 = *reinterpret_cast<const float4*>(&cs.s[hb * 32 + q * 4]);
-            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float x0 = __uint_as_float(u[q * 4 + 2 * e]) * sv[2 * e];
-              const float x1 = __uint_as_float(u[q * 4 + 2 * e + 1]) * sv[2 * e + 1];
-              const uint32_t hh = pack_bf16(x0, x1);
-              hi[q * 2 + e] = hh;
-              lo[q * 2 + e] = pack_bf16(x0 - bf16_lo_f(hh), x1 - bf16_hi_f(hh));
-            }
+          for (int x = 0; x < 16; ++x) {
+            const float x0 = __uint_as_float(u[2 * x]), x1 = __uint_as_float(u[2 * x + 1]);
+            const uint32_t hh = pack_bf16(x0, x1);
+            hi[x] = hh;
+            lo[x] = pack_bf16(x0 - bf16_lo_f(hh), x1 - bf16_hi_f(hh));
           }
           tmem_st16(tmem + lane_off + TM_UH + hb * 16, hi);
           tmem_st16(tmem + lane_off + TM_UL + hb * 16, lo);

@@ -286,6 +286,26 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
                : "memory");
 }
 
+// Four 8x8 b16 matrices from shared memory: lane l gives the address of row
+// (l & 7) of matrix (l >> 3); d[m] then holds row l >> 2, columns 2 (l & 3)
+// and 2 (l & 3) + 1 of matrix m.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& d0, uint32_t& d1, uint32_t& d2,
+                                            uint32_t& d3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+               : "r"(addr)
+               : "memory");
+}
+// d[16 x 8] += A[16 x 16] B[16 x 8], bf16 operands, fp32 accumulators (warp-level).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128-byte-swizzled region whose base is 1024-byte aligned.
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
