@@ -695,18 +695,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // always zero (cleared once at the start): those two warps have nothing to write
         const bool upper = hf == 1 && (Ln & 63) < 32;
         if (krow && !upper) {
-          // A_ij = beta_i r_i r_j e^{G_i - G_j} k_i.k_j  (j < i < m), fp32 into the scratch
+          // A_ij = beta_i r_i r_j e^{G_i - G_j} k_i.k_j, fp32 into the scratch (0 in rows and
+          // columns past m). The solve reads only j < i, so entries on and above the diagonal
+          // are stored as computed, unmasked.
           const float cia = i < m ? ps->beta[i] * ps->r[i] * exp2f((Gi - gmax) * kLog2e) : 0.f;
+          const float2 ci2 = make_float2(cia, cia);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const int j0 = 32 * hf + 4 * q;
             const float4 d4 = *reinterpret_cast<const float4*>(&ps->d[j0]);
-            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-            float a4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              a4[e] = (j0 + e < i) ? (cia * __uint_as_float(v[4 * q + e])) * dd[e] : 0.f;
-            *reinterpret_cast<float4*>(&Abuf[i * LDF + j0]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+            const float2 a01 = __fmul2_rn(__fmul2_rn(ci2, make_float2(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]))),
+                                          make_float2(d4.x, d4.y));
+            const float2 a23 = __fmul2_rn(__fmul2_rn(ci2, make_float2(__uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]))),
+                                          make_float2(d4.z, d4.w));
+            *reinterpret_cast<float4*>(&Abuf[i * LDF + j0]) = make_float4(a01.x, a01.y, a23.x, a23.y);
           }
         } else if (!krow && !upper) {
           // M_ij = q_i.k_j  (j <= i), bf16 K-major [i][j]
@@ -735,14 +737,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // row ti carries the state-update weight s_ti (so U' and W' come out of their
           // products already multiplied by diag(s / lambda))
           const float si = zero_row(ps->s[ti], qq > (ti >> 4));
-          float t[16];
+          const float2 si2 = make_float2(si, si);
+          float2 t[8];
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const float4 x = *reinterpret_cast<const float4*>(&Tbuf[ti * LDF + 16 * qq + 4 * k4]);
-            t[4 * k4 + 0] = si * x.x;
-            t[4 * k4 + 1] = si * x.y;
-            t[4 * k4 + 2] = si * x.z;
-            t[4 * k4 + 3] = si * x.w;
+            t[2 * k4] = __fmul2_rn(si2, make_float2(x.x, x.y));
+            t[2 * k4 + 1] = __fmul2_rn(si2, make_float2(x.z, x.w));
           }
           named_bar_sync(1, 256);  // every thread has read T before it is overwritten
           const uint32_t tb = sbase + L::TB;
@@ -753,15 +754,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float4 bb = *reinterpret_cast<const float4*>(&ps->beta[j0 + 4]);
             const float4 wa4 = *reinterpret_cast<const float4*>(&ps->tw[j0]);
             const float4 wb4 = *reinterpret_cast<const float4*>(&ps->tw[j0 + 4]);
-            const float bt[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
-            const float wt8[8] = {wa4.x, wa4.y, wa4.z, wa4.w, wb4.x, wb4.y, wb4.z, wb4.w};
+            const float2 bt[4] = {make_float2(ba.x, ba.y), make_float2(ba.z, ba.w), make_float2(bb.x, bb.y),
+                                  make_float2(bb.z, bb.w)};
+            const float2 wt[4] = {make_float2(wa4.x, wa4.y), make_float2(wa4.z, wa4.w), make_float2(wb4.x, wb4.y),
+                                  make_float2(wb4.z, wb4.w)};
             uint32_t hi4[4], lo4[4], w4[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float x0 = t[8 * q + 2 * e] * bt[2 * e], x1 = t[8 * q + 2 * e + 1] * bt[2 * e + 1];
-              hi4[e] = pack_bf16(x0, x1);
-              lo4[e] = pack_bf16(x0 - bf16_lo_f(hi4[e]), x1 - bf16_hi_f(hi4[e]));
-              w4[e] = pack_bf16(t[8 * q + 2 * e] * wt8[2 * e], t[8 * q + 2 * e + 1] * wt8[2 * e + 1]);
+              const float2 x = __fmul2_rn(t[4 * q + e], bt[e]);
+              hi4[e] = pack_bf16(x.x, x.y);
+              lo4[e] = pack_bf16_2(bf16_residual(x, hi4[e]));
+              const float2 w = __fmul2_rn(t[4 * q + e], wt[e]);
+              w4[e] = pack_bf16(w.x, w.y);
             }
             const uint32_t off = sw128(ti, 2 * qq + q);
             st_shared_v4(tb + off, hi4[0], hi4[1], hi4[2], hi4[3]);
@@ -823,10 +827,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            const float x0 = __uint_as_float(u[2 * x]), x1 = __uint_as_float(u[2 * x + 1]);
-            const uint32_t hh = pack_bf16(x0, x1);
-            hi[x] = hh;
-            lo[x] = pack_bf16(x0 - bf16_lo_f(hh), x1 - bf16_hi_f(hh));
+            const float2 x2 = make_float2(__uint_as_float(u[2 * x]), __uint_as_float(u[2 * x + 1]));
+            hi[x] = pack_bf16(x2.x, x2.y);
+            lo[x] = pack_bf16_2(bf16_residual(x2, hi[x]));
           }
           tmem_st16(tmem + lane_off + TM_UH + hb * 16, hi);
           tmem_st16(tmem + lane_off + TM_UL + hb * 16, lo);
@@ -938,12 +941,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int t4 = 0; t4 < 8; ++t4) {
               const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
-              __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stage) + (4 * t4) * DV + wb;
+              uint16_t* st = reinterpret_cast<uint16_t*>(stage) + (4 * t4) * DV + wb;
               const uint32_t* o4 = t4 < 4 ? &oa[4 * t4] : &ob[4 * t4 - 16];
-              st[0] = __float2bfloat16_rn(c4.x * __uint_as_float(o4[0]));
-              st[DV] = __float2bfloat16_rn(c4.y * __uint_as_float(o4[1]));
-              st[2 * DV] = __float2bfloat16_rn(c4.z * __uint_as_float(o4[2]));
-              st[3 * DV] = __float2bfloat16_rn(c4.w * __uint_as_float(o4[3]));
+              const uint32_t y01 = pack_bf16_2(__fmul2_rn(make_float2(c4.x, c4.y),
+                                                          make_float2(__uint_as_float(o4[0]), __uint_as_float(o4[1]))));
+              const uint32_t y23 = pack_bf16_2(__fmul2_rn(make_float2(c4.z, c4.w),
+                                                          make_float2(__uint_as_float(o4[2]), __uint_as_float(o4[3]))));
+              st[0] = (uint16_t)y01;
+              st[DV] = (uint16_t)(y01 >> 16);
+              st[2 * DV] = (uint16_t)y23;
+              st[3 * DV] = (uint16_t)(y23 >> 16);
             }
           }
           fence_proxy_async_smem();

@@ -271,6 +271,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_lo_f(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16_2(float2 x) { return pack_bf16(x.x, x.y); }
+// x minus the two bf16 values packed in h (exact in fp32): the part a bf16 pair drops.
+__device__ __forceinline__ float2 bf16_residual(float2 x, uint32_t h) {
+  return __ffma2_rn(make_float2(bf16_lo_f(h), bf16_hi_f(h)), make_float2(-1.f, -1.f), x);
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
