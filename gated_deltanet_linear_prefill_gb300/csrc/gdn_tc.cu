@@ -73,7 +73,8 @@ constexpr uint32_t kTmemCols = 512;
 
 // Barrier indices (arrival count 1 each)
 enum {
-  B_FULL0 = 0, B_FULL1, B_FULL2,  // chunk tiles + gate scalars landed (slot c % 3)
+  B_FULL0 = 0, B_FULL1, B_FULL2,  // chunk K/Q tiles + gate scalars landed (slot c % 3)
+  B_VFULL0, B_VFULL1,             // chunk V tile landed (slot c % 2)
   B_KQE0, B_KQE1, B_KQE2,         // K/Q slot released (chunk c's last MMA done)
   B_VE0, B_VE1,                   // V slot released (slot c % 2)
   B_RQ0, B_RQ1, B_RQ2,            // q norms of slot c % 3 written
@@ -370,8 +371,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Scans the gates of the next 64 rows, ends the chunk early if the log-decay
     // span would pass kMaxSpan, keeps the state-scale bookkeeping, and requests
     // the chunk's tiles once its ring slots are free. It never waits for data.
-    const uint32_t tx_bytes = (uint32_t)(2 * L::NKA + L::NVA) * 8192u;
-    int issued = 0;
+    const uint32_t kq_bytes = (uint32_t)(2 * L::NKA) * 8192u, v_bytes = (uint32_t)L::NVA * 8192u;
+    int kq_issued = 0, v_issued = 0;  // chunks whose K / Q and V loads were requested
     if (len > 0) {
       int64_t start = 0;
       float logmu = 0.f;
@@ -431,10 +432,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool last = start + m >= len;
         const float b0c = b0, b1c = b1;
         if (!last) load_gates(start + m);  // the next chunk's gates, in flight while this one waits
-        // ring slots: K/Q of chunk c-3 and V of chunk c-2 released
+        // the K / Q ring slot of chunk c-3 was released
         bool ok = true;
         if (c >= 3) ok = wait(B_KQE0 + c % 3, ((c / 3) + 1) & 1, 0);
-        if (ok && c >= 2) ok = wait(B_VE0 + (c & 1), ((c >> 1) + 1) & 1, 0);
         if (!ok) break;
         float* sc = slot_sc(c);
         sc[SC_G + lane] = s0;
@@ -453,22 +453,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           sc[SC_M] = __int_as_float(m);
           sc[SC_FLAGS] = __int_as_float((last ? 1 : 0) | (eager ? 2 : 0));
           *reinterpret_cast<long long*>(&sc[SC_T0]) = (long long)(bos + start);
-          // the arrive publishes the scalars; the tiles complete the phase
+          // the arrive publishes the scalars; the K / Q tiles complete the phase
           const int row = (int)(bos + start);
           uint64_t* full = &bars[B_FULL0 + c % 3];
-          mbar_arrive_expect_tx(full, tx_bytes);
-          const uint32_t kq = slot_kq(c), vv = slot_v(c);
+          mbar_arrive_expect_tx(full, kq_bytes);
+          const uint32_t kq = slot_kq(c);
 #pragma unroll 1
-          for (int a = 0; a < 2 * L::NKA + L::NVA; ++a) {  // K, Q per atom column, then V
-            const bool isv = a >= 2 * L::NKA;
-            const int ac = isv ? a - 2 * L::NKA : (a >> 1);
-            const CUtensorMap* map = isv ? &tm.v : ((a & 1) ? &tm.q : &tm.k);
-            uint8_t* dst = isv ? sm + (vv - sbase) + ac * 8192 : sm + (kq - sbase) + ac * 16384 + (a & 1) * 8192;
-            tma_load_3d(dst, map, full, 64 * ac, isv ? h : hq, row);
-          }
+          for (int a = 0; a < 2 * L::NKA; ++a)  // K, Q per atom column
+            tma_load_3d(sm + (kq - sbase) + (a >> 1) * 16384 + (a & 1) * 8192, (a & 1) ? &tm.q : &tm.k, full,
+                        64 * (a >> 1), hq, row);
         }
         __syncwarp();
-        issued = c + 1;
+        kq_issued = c + 1;
+        // V has its own ring (two slots, released by chunk c-2's U product) and barrier, so
+        // the K / Q tiles above never wait for it
+        if (c >= 2) ok = wait(B_VE0 + (c & 1), ((c >> 1) + 1) & 1, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          const int row = (int)(bos + start);
+          uint64_t* vfull = &bars[B_VFULL0 + (c & 1)];
+          mbar_arrive_expect_tx(vfull, v_bytes);
+          const uint32_t vv = slot_v(c);
+#pragma unroll 1
+          for (int a = 0; a < L::NVA; ++a) tma_load_3d(sm + (vv - sbase) + a * 8192, &tm.v, vfull, 64 * a, h, row);
+        }
+        __syncwarp();
+        v_issued = c + 1;
         if (last) break;
         start += m;
         logmu = eager ? 0.f : loglam;
@@ -476,9 +486,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     // let every requested tile land before the CTA can exit (on the normal path
     // they were all consumed and these return at once)
-    if (lane == 0)
-      for (int c = issued - 3 < 0 ? 0 : issued - 3; c < issued; ++c)
+    if (lane == 0) {
+      for (int c = kq_issued - 3 < 0 ? 0 : kq_issued - 3; c < kq_issued; ++c)
         wait(B_FULL0 + c % 3, (c / 3) & 1, kDrainWait);
+      for (int c = v_issued - 2 < 0 ? 0 : v_issued - 2; c < v_issued; ++c)
+        wait(B_VFULL0 + (c & 1), (c >> 1) & 1, kDrainWait);
+    }
   } else if (warp == 1) {
     // ================================================================ state-independent MMAs
     // [K;Q] K^T of chunk c+1 as soon as its tiles are in and WG-A has read chunk c's;
@@ -521,6 +534,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int k = 0; k < 4; ++k)
           mma_ss(tmem + TM_W, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
         mma_commit(&bars[B_W_DONE]);  // W'^T may be converted while U is still running
+        if (!wait(B_VFULL0 + par, (c >> 1) & 1, 10)) break;
+        tc_fence_after();
         const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
         const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(sbase + L::TB, 16, 1024);
 #pragma unroll 1
