@@ -938,45 +938,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // the store that last used this tile has read it (one store group per pass)
           if (wb == 0) bulk_wait_read_1();
           named_bar_sync(2, 128);
-          uint32_t oa[16], ob[16];
-          tmem_ld16(tmem + lane_off + TM_O + p0, oa);
-          if (PT == 32) tmem_ld16(tmem + lane_off + TM_O + p0 + 16, ob);
-          tmem_ld_wait();
-          if (live && p.out_f32) {
+          if (p.out_f32) {
+            uint32_t oa[16];
+            tmem_ld16(tmem + lane_off + TM_O + p0, oa);
+            tmem_ld_wait();
+            if (live) {
 #pragma unroll
-            for (int t4 = 0; t4 < 4; ++t4) {
-              const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
-              float* st = reinterpret_cast<float*>(stage) + (4 * t4) * DV + wb;
-              st[0] = c4.x * __uint_as_float(oa[4 * t4]);
-              st[DV] = c4.y * __uint_as_float(oa[4 * t4 + 1]);
-              st[2 * DV] = c4.z * __uint_as_float(oa[4 * t4 + 2]);
-              st[3 * DV] = c4.w * __uint_as_float(oa[4 * t4 + 3]);
+              for (int t4 = 0; t4 < 4; ++t4) {
+                const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
+                float* st = reinterpret_cast<float*>(stage) + (4 * t4) * DV + wb;
+                st[0] = c4.x * __uint_as_float(oa[4 * t4]);
+                st[DV] = c4.y * __uint_as_float(oa[4 * t4 + 1]);
+                st[2 * DV] = c4.z * __uint_as_float(oa[4 * t4 + 2]);
+                st[3 * DV] = c4.w * __uint_as_float(oa[4 * t4 + 3]);
+              }
             }
-          } else if (live) {
+          } else {
+            // bf16: each thread takes consecutive row pairs of its 16-lane blocks (16 x 256b
+            // loads) and writes 8x8 blocks transposed into row-major tiles of 64 columns
+            // (128-byte swizzle, so the eight rows of a block hit distinct banks); the tile
+            // row is the lane index
+            const int qd = wb >> 5, t = lane & 3;
+            uint32_t a[16], b[16];
+            tmem_ld16x256b_x4(tmem + ((uint32_t)(32 * qd) << 16) + TM_O + p0, a);
+            tmem_ld16x256b_x4(tmem + ((uint32_t)(32 * qd + 16) << 16) + TM_O + p0, b);
+            tmem_ld_wait();
+            if (32 * qd < DV) {
+              float2 co2[4];
 #pragma unroll
-            for (int t4 = 0; t4 < 8; ++t4) {
-              const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
-              uint16_t* st = reinterpret_cast<uint16_t*>(stage) + (4 * t4) * DV + wb;
-              const uint32_t* o4 = t4 < 4 ? &oa[4 * t4] : &ob[4 * t4 - 16];
-              const uint32_t y01 = pack_bf16_2(__fmul2_rn(make_float2(c4.x, c4.y),
-                                                          make_float2(__uint_as_float(o4[0]), __uint_as_float(o4[1]))));
-              const uint32_t y23 = pack_bf16_2(__fmul2_rn(make_float2(c4.z, c4.w),
-                                                          make_float2(__uint_as_float(o4[2]), __uint_as_float(o4[3]))));
-              st[0] = (uint16_t)y01;
-              st[DV] = (uint16_t)(y01 >> 16);
-              st[2 * DV] = (uint16_t)y23;
-              st[3 * DV] = (uint16_t)(y23 >> 16);
+              for (int r = 0; r < 4; ++r) co2[r] = *reinterpret_cast<const float2*>(&cs.co[p0 + 8 * r + 2 * t]);
+              const uint32_t tile = sbase + (uint32_t)(stage - sm) + (uint32_t)(qd >> 1) * 4096u;
+#pragma unroll
+              for (int hs = 0; hs < 4; ++hs) {  // lane half (hs >> 1) and 8-lane block (hs & 1)
+                const uint32_t* x = (hs >> 1) ? b : a;
+                const int o = 2 * (hs & 1);
+                uint32_t pk[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                  pk[r] = pack_bf16_2(__fmul2_rn(co2[r], make_float2(__uint_as_float(x[4 * r + o]),
+                                                                      __uint_as_float(x[4 * r + o + 1]))));
+                const uint32_t chunk = (uint32_t)(4 * (qd & 1) + hs);
+                stmatrix_x4_trans(tile + sw128((uint32_t)lane, chunk), pk[0], pk[1], pk[2], pk[3]);
+              }
             }
           }
           fence_proxy_async_smem();
           named_bar_sync(2, 128);
           const int rows = m - p0 < PT ? m - p0 : PT;
           if (rows == PT) {
-            if (wb == 0) tma_store_3d(&tm.o, stage, 0, h, (int)(t0 + p0));
+            if (wb == 0) {
+              if (p.out_f32) {
+                tma_store_3d(&tm.o, stage, 0, h, (int)(t0 + p0));
+              } else {
+#pragma unroll
+                for (int tl = 0; tl < DV / 64; ++tl) tma_store_3d(&tm.o, stage + tl * 4096, 64 * tl, h, (int)(t0 + p0));
+              }
+            }
           } else {
             for (int idx = wb; idx < (rows << pshift); idx += 128) {
               const int r = idx >> pshift, pc = idx & (pieces - 1);
-              const uint4 x = *reinterpret_cast<const uint4*>(stage + (size_t)r * DV * osz + pc * 16);
+              const uint32_t src = p.out_f32 ? (uint32_t)(r * DV * 4 + pc * 16)
+                                             : (uint32_t)((pc >> 3) * 4096) + sw128((uint32_t)r, (uint32_t)(pc & 7));
+              const uint4 x = *reinterpret_cast<const uint4*>(stage + src);
               char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + h) * DV) * osz;
               *reinterpret_cast<uint4*>(dst + pc * 16) = x;
             }
@@ -1047,19 +1070,20 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t T, int H, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// out [T, H, D] (bf16 or fp32) for tensor stores: box = D x 1 head x 32 rows (bf16) or 16 rows
-// (fp32), unswizzled, i.e. the row-major staging tile of one epilogue pass.
+// out [T, H, D] for tensor stores: bf16 as 64 columns x 1 head x 32 rows with 128-byte swizzle
+// (one staging tile per 64 columns of an epilogue pass); fp32 as D x 1 x 16 rows, unswizzled.
 bool encode_out(CUtensorMap* m, void* base, int64_t T, int H, int D, bool f32) {
   auto fn = get_encode();
   if (!fn) return false;
   const cuuint64_t es = f32 ? 4 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es};
-  cuuint32_t box[3] = {(cuuint32_t)D, 1, f32 ? 16u : 32u};
+  cuuint32_t box[3] = {f32 ? (cuuint32_t)D : 64u, 1, f32 ? 16u : 32u};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int DK, int DV>

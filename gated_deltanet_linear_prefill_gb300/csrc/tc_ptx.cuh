@@ -291,6 +291,26 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_
                : "memory");
 }
 
+// 16 lanes x 32 columns of 32-bit values in four 8-column steps: thread 4 g + t
+// gets, for step r, v[4r], v[4r+1] = lane (lane of taddr) + g, columns 8r + 2t and
+// 8r + 2t + 1, and v[4r+2], v[4r+3] = lane + 8 + g, the same columns.
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+// Four 8x8 b16 matrices to shared memory, transposed: register m of lane 4 g + t
+// holds the pair that lands in rows 2t and 2t + 1, column g, of matrix m; lane
+// 8 m + j gives the address of row j of matrix m (16 bytes).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                                  uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0),
+               "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
 // Four 8x8 b16 matrices from shared memory: lane l gives the address of row
 // (l & 7) of matrix (l >> 3); d[m] then holds row l >> 2, columns 2 (l & 3)
 // and 2 (l & 3) + 1 of matrix m.
