@@ -922,23 +922,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (c >= 0) {
         // ---- epilogue: out_i = co_i O^T_i, staged in shared memory and written by tensor
-        // stores (32 bf16 or 16 fp32 rows per pass). The passes alternate between two
-        // staging tiles, so a pass waits only for the store of two passes before. A pass
-        // that would run past the chunk's rows is copied out row by row instead.
+        // stores. bf16: the whole chunk at once, as two 64-column tiles of 64 rows (128-byte
+        // swizzle), one store each; fp32: passes of 16 rows alternating between two tiles.
+        // A chunk (or pass) shorter than the tile is copied out row by row instead, since a
+        // store of the full tile would run into the next sequence's rows.
         const ChunkScalars& cs = cscal[c % 3];
         bool ok = wait(B_O_DONE, c & 1, 13);
+        if (wb == 0) bulk_wait_read();  // the staging tiles are free again
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
         const int m = cs.m;
         const long long t0 = cs.t0;
-        const int PT = p.out_f32 ? 16 : 32;
+        mu = cs.mu_next;
+        if (!p.out_f32) {
+          // each thread takes consecutive row pairs of its 16-lane blocks (16 x 256b loads)
+          // and writes 8x8 blocks transposed into the row-major tiles (the eight rows of a
+          // block hit distinct banks under the swizzle); a tile row is 32 half + lane
+          const int qd = wb >> 5, t = lane & 3;
+          const uint32_t tile = sbase + L::STG + (uint32_t)(qd >> 1) * 8192u;
 #pragma unroll 1
-        for (int p0 = 0; p0 < m; p0 += PT, ++npass) {
-          uint8_t* stage = sm + L::STG + (npass & 1) * 8192u;
-          // the store that last used this tile has read it (one store group per pass)
-          if (wb == 0) bulk_wait_read_1();
-          named_bar_sync(2, 128);
-          if (p.out_f32) {
+          for (int half = 0; half < 2 && 32 * half < m; ++half) {
+            const int p0 = 32 * half;
+            uint32_t a[16], b[16];
+            tmem_ld16x256b_x4(tmem + ((uint32_t)(32 * qd) << 16) + TM_O + p0, a);
+            tmem_ld16x256b_x4(tmem + ((uint32_t)(32 * qd + 16) << 16) + TM_O + p0, b);
+            tmem_ld_wait();
+            if (32 * qd < DV) {
+              float2 co2[4];
+#pragma unroll
+              for (int r = 0; r < 4; ++r) co2[r] = *reinterpret_cast<const float2*>(&cs.co[p0 + 8 * r + 2 * t]);
+#pragma unroll
+              for (int hs = 0; hs < 4; ++hs) {  // lane half (hs >> 1) and 8-lane block (hs & 1)
+                const uint32_t* x = (hs >> 1) ? b : a;
+                const int o = 2 * (hs & 1);
+                uint32_t pk[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                  pk[r] = pack_bf16_2(__fmul2_rn(co2[r], make_float2(__uint_as_float(x[4 * r + o]),
+                                                                      __uint_as_float(x[4 * r + o + 1]))));
+                stmatrix_x4_trans(tile + sw128((uint32_t)(p0 + lane), (uint32_t)(4 * (qd & 1) + hs)), pk[0], pk[1],
+                                  pk[2], pk[3]);
+              }
+            }
+          }
+          tc_fence_before();
+          fence_proxy_async_smem();
+          named_bar_sync(2, 128);  // tiles written, O and the chunk's scalars read
+          if (wb == 0) {
+            mbar_arrive(&bars[B_EPI_DONE]);
+            mbar_arrive(&bars[B_CSF0 + c % 3]);
+          }
+          if (m == 64) {
+            if (wb == 0) {
+#pragma unroll
+              for (int tl = 0; tl < DV / 64; ++tl)
+                tma_store_3d(&tm.o, sm + L::STG + tl * 8192, 64 * tl, h, (int)t0);
+              bulk_commit();
+            }
+          } else {
+            for (int idx = wb; idx < (m << pshift); idx += 128) {
+              const int r = idx >> pshift, pc = idx & (pieces - 1);
+              const uint4 x = *reinterpret_cast<const uint4*>(
+                  sm + L::STG + (pc >> 3) * 8192 + sw128((uint32_t)r, (uint32_t)(pc & 7)));
+              char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + r) * p.h_v + h) * DV) * osz;
+              *reinterpret_cast<uint4*>(dst + pc * 16) = x;
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int p0 = 0; p0 < m; p0 += 16, ++npass) {
+            uint8_t* stage = sm + L::STG + (npass & 1) * 8192u;
+            // the store that last used this tile has read it (one store group per pass)
+            if (wb == 0) bulk_wait_read_1();
+            named_bar_sync(2, 128);
             uint32_t oa[16];
             tmem_ld16(tmem + lane_off + TM_O + p0, oa);
             tmem_ld_wait();
@@ -953,65 +1009,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 st[3 * DV] = c4.w * __uint_as_float(oa[4 * t4 + 3]);
               }
             }
-          } else {
-            // bf16: each thread takes consecutive row pairs of its 16-lane blocks (16 x 256b
-            // loads) and writes 8x8 blocks transposed into row-major tiles of 64 columns
-            // (128-byte swizzle, so the eight rows of a block hit distinct banks); the tile
-            // row is the lane index
-            const int qd = wb >> 5, t = lane & 3;
-            uint32_t a[16], b[16];
-            tmem_ld16x256b_x4(tmem + ((uint32_t)(32 * qd) << 16) + TM_O + p0, a);
-            tmem_ld16x256b_x4(tmem + ((uint32_t)(32 * qd + 16) << 16) + TM_O + p0, b);
-            tmem_ld_wait();
-            if (32 * qd < DV) {
-              float2 co2[4];
-#pragma unroll
-              for (int r = 0; r < 4; ++r) co2[r] = *reinterpret_cast<const float2*>(&cs.co[p0 + 8 * r + 2 * t]);
-              const uint32_t tile = sbase + (uint32_t)(stage - sm) + (uint32_t)(qd >> 1) * 4096u;
-#pragma unroll
-              for (int hs = 0; hs < 4; ++hs) {  // lane half (hs >> 1) and 8-lane block (hs & 1)
-                const uint32_t* x = (hs >> 1) ? b : a;
-                const int o = 2 * (hs & 1);
-                uint32_t pk[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                  pk[r] = pack_bf16_2(__fmul2_rn(co2[r], make_float2(__uint_as_float(x[4 * r + o]),
-                                                                      __uint_as_float(x[4 * r + o + 1]))));
-                const uint32_t chunk = (uint32_t)(4 * (qd & 1) + hs);
-                stmatrix_x4_trans(tile + sw128((uint32_t)lane, chunk), pk[0], pk[1], pk[2], pk[3]);
+            fence_proxy_async_smem();
+            named_bar_sync(2, 128);
+            const int rows = m - p0 < 16 ? m - p0 : 16;
+            if (rows == 16) {
+              if (wb == 0) tma_store_3d(&tm.o, stage, 0, h, (int)(t0 + p0));
+            } else {
+              for (int idx = wb; idx < (rows << pshift); idx += 128) {
+                const int r = idx >> pshift, pc = idx & (pieces - 1);
+                const uint4 x = *reinterpret_cast<const uint4*>(stage + r * DV * 4 + pc * 16);
+                char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + h) * DV) * osz;
+                *reinterpret_cast<uint4*>(dst + pc * 16) = x;
               }
             }
+            if (wb == 0) bulk_commit();  // empty for a copied pass
           }
-          fence_proxy_async_smem();
+          tc_fence_before();
           named_bar_sync(2, 128);
-          const int rows = m - p0 < PT ? m - p0 : PT;
-          if (rows == PT) {
-            if (wb == 0) {
-              if (p.out_f32) {
-                tma_store_3d(&tm.o, stage, 0, h, (int)(t0 + p0));
-              } else {
-#pragma unroll
-                for (int tl = 0; tl < DV / 64; ++tl) tma_store_3d(&tm.o, stage + tl * 4096, 64 * tl, h, (int)(t0 + p0));
-              }
-            }
-          } else {
-            for (int idx = wb; idx < (rows << pshift); idx += 128) {
-              const int r = idx >> pshift, pc = idx & (pieces - 1);
-              const uint32_t src = p.out_f32 ? (uint32_t)(r * DV * 4 + pc * 16)
-                                             : (uint32_t)((pc >> 3) * 4096) + sw128((uint32_t)r, (uint32_t)(pc & 7));
-              const uint4 x = *reinterpret_cast<const uint4*>(stage + src);
-              char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + h) * DV) * osz;
-              *reinterpret_cast<uint4*>(dst + pc * 16) = x;
-            }
+          if (wb == 0) {
+            mbar_arrive(&bars[B_EPI_DONE]);
+            mbar_arrive(&bars[B_CSF0 + c % 3]);
           }
-          if (wb == 0) bulk_commit();  // empty for a copied pass
-        }
-        tc_fence_before();
-        named_bar_sync(2, 128);
-        mu = cs.mu_next;
-        if (wb == 0) {
-          mbar_arrive(&bars[B_EPI_DONE]);
-          mbar_arrive(&bars[B_CSF0 + c % 3]);
         }
       }
       if (!more) break;
@@ -1070,15 +1088,15 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t T, int H, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// out [T, H, D] for tensor stores: bf16 as 64 columns x 1 head x 32 rows with 128-byte swizzle
-// (one staging tile per 64 columns of an epilogue pass); fp32 as D x 1 x 16 rows, unswizzled.
+// out [T, H, D] for tensor stores: bf16 as 64 columns x 1 head x 64 rows with 128-byte swizzle
+// (one staging tile per 64 columns of a chunk); fp32 as D x 1 x 16 rows, unswizzled.
 bool encode_out(CUtensorMap* m, void* base, int64_t T, int H, int D, bool f32) {
   auto fn = get_encode();
   if (!fn) return false;
   const cuuint64_t es = f32 ? 4 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es};
-  cuuint32_t box[3] = {f32 ? (cuuint32_t)D : 64u, 1, f32 ? 16u : 32u};
+  cuuint32_t box[3] = {f32 ? (cuuint32_t)D : 64u, 1, f32 ? 16u : 64u};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
