@@ -34,7 +34,7 @@ GDN_FLAG_SIMT = 0x2
 GDN_NOALLOC_MAX_SEQS = 16384  # include/gdn.h
 STATUS_NAMES = ["GDN_OK", "GDN_ERR_NULL", "GDN_ERR_SHAPE", "GDN_ERR_DTYPE", "GDN_ERR_ALIGN",
                 "GDN_ERR_SEQLENS", "GDN_ERR_STATE_INDEX", "GDN_ERR_ALIAS", "GDN_ERR_WORKSPACE",
-                "GDN_ERR_ARCH", "GDN_ERR_CUDA", "GDN_ERR_DEVICE_TIMEOUT"]
+                "GDN_ERR_ARCH", "GDN_ERR_CUDA", "GDN_ERR_DEVICE_TIMEOUT", "GDN_ERR_PARENT"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -97,6 +97,10 @@ def load_library(build_if_missing: bool = True):
         lib.gdn_prefill_varlen.restype = ctypes.c_int
         lib.gdn_prefill_varlen_noalloc.argtypes = [P] * 10 + [ctypes.POINTER(GdnDesc), P]
         lib.gdn_prefill_varlen_noalloc.restype = ctypes.c_int
+        lib.gdn_tree_workspace_bytes.argtypes = [ctypes.POINTER(GdnDesc)]
+        lib.gdn_tree_workspace_bytes.restype = ctypes.c_size_t
+        lib.gdn_prefill_tree.argtypes = [P] * 11 + [ctypes.POINTER(GdnDesc), P]
+        lib.gdn_prefill_tree.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.POINTER(GdnDesc), P]
         lib.gdn_get_device_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -166,6 +170,20 @@ def gdn_prefill_varlen_noalloc(q, k, v, g, beta, cu_seqlens, initial_state, stat
                                               ctypes.byref(desc), _stream_handle(stream)))
 
 
+def gdn_tree_workspace_bytes(desc: GdnDesc) -> int:
+    return int(load_library().gdn_tree_workspace_bytes(ctypes.byref(desc)))
+
+
+def gdn_prefill_tree(q, k, v, g, beta, cu_seqlens, parent, initial_state, state_index, out,
+                     final_state, desc: GdnDesc, stream=None) -> int:
+    """The C tree entry point with tensors for pointers; returns the gdn_status code."""
+    lib = load_library()
+    return int(lib.gdn_prefill_tree(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                    _ptr(cu_seqlens), _ptr(parent), _ptr(initial_state),
+                                    _ptr(state_index), _ptr(out), _ptr(final_state),
+                                    ctypes.byref(desc), _stream_handle(stream)))
+
+
 def gdn_get_device_status(desc: GdnDesc, stream=None) -> int:
     """Synchronises the stream and returns the device status word's code."""
     return int(load_library().gdn_get_device_status(ctypes.byref(desc), _stream_handle(stream)))
@@ -227,6 +245,39 @@ def prefill_varlen(q, k, v, g, beta, cu_seqlens, *, initial_state=None, state_in
                             final_state, desc, stream)
     if rc != GDN_OK:
         raise GdnError(rc, "gdn_prefill_varlen")
+    if check_device:
+        rc = gdn_get_device_status(desc, stream)
+        if rc != GDN_OK:
+            raise GdnError(rc, "device status")
+    return out, final_state
+
+
+def prefill_tree(q, k, v, g, beta, cu_seqlens, parent, *, initial_state=None, state_index=None,
+                 out=None, final_state=None, out_dtype=None, max_seqlen: int = 0,
+                 scale: float = 0.0, flags: int = 0, workspace=None, stream=None,
+                 check_device: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """A prefix tree of packed sequences in one launch (see include/gdn.h):
+    sequence n continues from the final state of sequence parent[n] (int32 [N],
+    parent[n] in [-1, n); -1 starts from initial_state[state_index[n]] or zero).
+    Returns (out [T, h_v, d_v], final_state [N, h_v, d_k, d_v] fp32)."""
+    dev = q.device
+    if out is None:
+        out = torch.empty(v.shape, dtype=out_dtype or torch.bfloat16, device=dev)
+    N = int(cu_seqlens.numel()) - 1
+    if final_state is None:
+        final_state = torch.empty((N, v.shape[1], q.shape[2], v.shape[2]), dtype=torch.float32,
+                                  device=dev)
+    desc = make_desc(q, v, g, cu_seqlens, out_dtype=out.dtype, initial_state=initial_state,
+                     max_seqlen=max_seqlen, scale=scale, flags=flags)
+    if workspace is None:
+        need = gdn_tree_workspace_bytes(desc)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    desc.workspace = workspace.data_ptr()
+    desc.workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = gdn_prefill_tree(q, k, v, g, beta, cu_seqlens, parent, initial_state, state_index, out,
+                          final_state, desc, stream)
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_prefill_tree")
     if check_device:
         rc = gdn_get_device_status(desc, stream)
         if rc != GDN_OK:

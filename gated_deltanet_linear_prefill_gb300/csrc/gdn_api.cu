@@ -17,15 +17,26 @@ constexpr int kBins = 4096;  // sequences are ordered by chunk count, capped her
 // One block. Resets the status word, checks what only the device can see, and
 // writes the sequence order (most chunks first) by a counting sort on the
 // chunk count. The order only steers scheduling; results do not depend on it.
+//
+// A tree launch (p.parent set) also checks parent[n] in [-1, n), clears the
+// ready flags and the work counter, and orders the roots (parent -1) longest
+// first followed by every other sequence in index order: a parent then always
+// precedes its children, as the tree kernel's in-order unit counter needs.
 __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_t* order) {
   __shared__ int hist[kBins];
   __shared__ int warp_tot[kPrepThreads / 32];
+  __shared__ int n_roots;
   const int tid = threadIdx.x;
+  const bool tree = p.parent != nullptr;
   if (tid == 0) {
     p.status->code = 0u;
     p.status->detail = 0u;
     p.status->units_done = 0u;
+    p.status->next_unit = 0u;
+    n_roots = 0;
   }
+  if (tree)
+    for (int64_t u = tid; u < (int64_t)p.num_seqs * p.h_v; u += kPrepThreads) p.ready[u] = 0u;
   for (int b = tid; b < kBins; b += kPrepThreads) hist[b] = 0;
   __syncthreads();
 
@@ -38,6 +49,12 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_
     if (p.initial_state && p.state_index) {
       const int32_t s = p.state_index[n];
       if (s < -1 || s >= p.num_state_slots) report(p.status, GDN_ERR_STATE_INDEX, (uint32_t)n);
+    }
+    if (tree) {
+      const int32_t pa = p.parent[n];
+      if (pa < -1 || pa >= n) report(p.status, GDN_ERR_PARENT, (uint32_t)n);
+      if (tree_parent(p, n) >= 0) continue;  // ordered after the roots, below
+      atomicAdd(&n_roots, 1);
     }
     int64_t bos, eos;
     seq_bounds(p, n, bos, eos);
@@ -84,12 +101,36 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_
   }
   __syncthreads();
   for (int n = tid; n < N; n += kPrepThreads) {
+    if (tree && tree_parent(p, n) >= 0) continue;
     int64_t bos, eos;
     seq_bounds(p, n, bos, eos);
     int64_t nc = (eos - bos + kChunk - 1) / kChunk;
     const int bin = (int)(nc < kBins - 1 ? nc : kBins - 1);
     const int pos = atomicAdd(&hist[bin], 1);
     order[pos] = n;
+  }
+  if (!tree) return;
+  // the other sequences after the roots, in index order (a block-wide scan per pass)
+  int base = n_roots;
+  for (int n0 = 0; n0 < N; n0 += kPrepThreads) {
+    const int n = n0 + tid;
+    const int f = (n < N && tree_parent(p, n) >= 0) ? 1 : 0;
+    int incl = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    __syncthreads();  // warp_tot is free again
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kPrepThreads / 32; ++w) {
+      if (w < warp) before += warp_tot[w];
+      total += warp_tot[w];
+    }
+    if (f) order[base + before + incl - 1] = n;
+    base += total;
   }
 }
 
@@ -158,6 +199,11 @@ extern "C" size_t gdn_workspace_bytes(const gdn_desc* desc) {
   return gdn::workspace_bytes(desc->num_seqs);
 }
 
+extern "C" size_t gdn_tree_workspace_bytes(const gdn_desc* desc) {
+  if (!desc || desc->num_seqs < 0 || desc->h_v < 1) return 0;
+  return gdn::tree_workspace_bytes(desc->num_seqs, desc->h_v);
+}
+
 extern "C" const char* gdn_status_string(gdn_status s) {
   switch (s) {
     case GDN_OK: return "GDN_OK";
@@ -172,6 +218,7 @@ extern "C" const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_ARCH: return "GDN_ERR_ARCH: the current device is not sm_103";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA runtime call failed";
     case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+    case GDN_ERR_PARENT: return "GDN_ERR_PARENT: a parent index outside [-1, n) (device check)";
   }
   return "unknown gdn_status";
 }
@@ -180,7 +227,8 @@ extern "C" const char* gdn_status_string(gdn_status s) {
 static gdn_status validate(const void* q, const void* k, const void* v, const void* g,
                            const void* beta, const int32_t* cu_seqlens,
                            const float* initial_state, const int32_t* state_index, void* out,
-                           float* final_state, const gdn_desc* d, Params& p) {
+                           float* final_state, const gdn_desc* d, Params& p,
+                           const int32_t* parent = nullptr) {
   if (!d) return GDN_ERR_NULL;
   const int64_t T = d->total_tokens;
   const int N = d->num_seqs;
@@ -199,7 +247,7 @@ static gdn_status validate(const void* q, const void* k, const void* v, const vo
     return GDN_ERR_WORKSPACE;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(initial_state, 16) || !aligned(final_state, 16) || !aligned(g, 4) ||
-      !aligned(beta, 4) || !aligned(cu_seqlens, 4) || !aligned(state_index, 4))
+      !aligned(beta, 4) || !aligned(cu_seqlens, 4) || !aligned(state_index, 4) || !aligned(parent, 4))
     return GDN_ERR_ALIGN;
 
   const size_t gsz = d->gate_dtype == GDN_F32 ? 4 : 2;
@@ -211,10 +259,12 @@ static gdn_status validate(const void* q, const void* k, const void* v, const vo
   const size_t fsb = final_state ? sb * (size_t)N : 0;
   const size_t cub = sizeof(int32_t) * (size_t)(N + 1);
   const size_t sib = state_index ? sizeof(int32_t) * (size_t)N : 0;
+  const size_t pab = parent ? sizeof(int32_t) * (size_t)N : 0;
   const size_t wsb = d->workspace_bytes;
   struct R { const void* p; size_t n; } ins[] = {{q, qb}, {k, qb}, {v, vb}, {g, gb}, {beta, gb},
                                                  {cu_seqlens, cub}, {initial_state, isb},
-                                                 {state_index, sib}, {d->workspace, wsb}};
+                                                 {state_index, sib}, {d->workspace, wsb},
+                                                 {parent, pab}};
   for (const R& r : ins) {
     if (overlaps(out, ob, r.p, r.n)) return GDN_ERR_ALIAS;
     if (overlaps(final_state, fsb, r.p, r.n)) return GDN_ERR_ALIAS;
@@ -267,6 +317,56 @@ extern "C" gdn_status gdn_prefill_varlen(const void* q, const void* k, const voi
   const cudaError_t e = (desc->flags & GDN_FLAG_SIMT) ? launch_simt(p, s) : launch_tc(p, s);
   if (e != cudaSuccess) return GDN_ERR_CUDA;
   return GDN_OK;
+}
+
+namespace gdn {
+
+// Tree launch with no tokens at all: every sequence ends where it starts, so
+// final_state[n] is its root's starting state (one block per (sequence, head)).
+__global__ void gdn_tree_copy_kernel(Params p) {
+  const int n = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
+  int r = n;
+  for (int steps = 0; steps <= n; ++steps) {  // parents have smaller indices: the walk ends
+    const int pa = tree_parent(p, r);
+    if (pa < 0) break;
+    r = pa;
+  }
+  const int64_t slot = state_slot(p, r);
+  const size_t sz = (size_t)p.d_k * p.d_v;
+  const float* src = slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + h) * sz : nullptr;
+  float* dst = p.final_state + ((size_t)n * p.h_v + h) * sz;
+  for (size_t i = threadIdx.x; i < sz; i += blockDim.x) dst[i] = src ? src[i] : 0.f;
+}
+
+}  // namespace gdn
+
+extern "C" gdn_status gdn_prefill_tree(const void* q, const void* k, const void* v, const void* g,
+                                       const void* beta, const int32_t* cu_seqlens,
+                                       const int32_t* parent, const float* initial_state,
+                                       const int32_t* state_index, void* out, float* final_state,
+                                       const gdn_desc* desc, void* stream) {
+  if (!desc) return GDN_ERR_NULL;
+  if (!parent || !final_state) return GDN_ERR_NULL;
+  if (desc->flags & GDN_FLAG_SIMT) return GDN_ERR_SHAPE;
+  if (desc->num_seqs > 0 && desc->h_v >= 1 && desc->workspace &&
+      desc->workspace_bytes < gdn::tree_workspace_bytes(desc->num_seqs, desc->h_v))
+    return GDN_ERR_WORKSPACE;
+  Params p;
+  const gdn_status st = validate(q, k, v, g, beta, cu_seqlens, initial_state, state_index, out,
+                                 final_state, desc, p, parent);
+  if (st != GDN_OK) return st;
+  if (p.num_seqs == 0) return GDN_OK;
+  p.parent = parent;
+  p.ready = (uint32_t*)((char*)desc->workspace + gdn::tree_flags_offset(p.num_seqs));
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_prep(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (p.total_tokens == 0) {
+    const long long units = (long long)p.num_seqs * p.h_v;
+    if (units > 0x7fffffffLL) return GDN_ERR_SHAPE;
+    gdn::gdn_tree_copy_kernel<<<(unsigned)units, 256, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
+  return launch_tc(p, s) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 extern "C" gdn_status gdn_get_device_status(const gdn_desc* desc, void* stream) {

@@ -18,10 +18,11 @@ constexpr int kChunk = 64;
 //   [0, 256)           Status: the device status word and diagnostics
 //   [256, 256 + 4*N)   the sequence order, longest first (int32)
 struct Status {
-  uint32_t code;      // first gdn_status a kernel reported (0 = none)
-  uint32_t detail;    // the sequence or unit it concerns
+  uint32_t code;       // first gdn_status a kernel reported (0 = none)
+  uint32_t detail;     // the sequence or unit it concerns
   uint32_t units_done;
-  uint32_t pad[61];
+  uint32_t next_unit;  // tree launches: work counter (units are taken in order)
+  uint32_t pad[60];
 };
 static_assert(sizeof(Status) == 256, "status block is 256 bytes");
 
@@ -31,6 +32,14 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline size_t workspace_bytes(int num_seqs) {
   return kOrderOffset + round_up(sizeof(int32_t) * (size_t)(num_seqs > 0 ? num_seqs : 1), 256);
+}
+
+// A tree launch adds, after the work list, one ready flag (uint32) per
+// (sequence, value head): set once that unit's final state is written.
+inline size_t tree_flags_offset(int num_seqs) { return workspace_bytes(num_seqs); }
+inline size_t tree_workspace_bytes(int num_seqs, int h_v) {
+  const size_t units = (size_t)(num_seqs > 0 ? num_seqs : 1) * (size_t)(h_v > 0 ? h_v : 1);
+  return tree_flags_offset(num_seqs) + round_up(sizeof(uint32_t) * units, 256);
 }
 
 // Everything a kernel needs, passed by value.
@@ -46,7 +55,9 @@ struct Params {
   void* out;
   float* final_state;
   Status* status;
-  const int32_t* order;  // sequences, longest first
+  const int32_t* order;  // sequences, longest first (tree launches: parents before children)
+  const int32_t* parent; // tree launches only (else NULL): parent[n] in [-1, n)
+  uint32_t* ready;       // tree launches only: ready flag per (sequence, value head)
   int64_t total_tokens;
   int num_seqs;
   int max_seqlen;
@@ -75,6 +86,14 @@ __device__ __forceinline__ void seq_bounds(const Params& p, int n, int64_t& bos,
   e = e < b ? b : (e > p.total_tokens ? p.total_tokens : e);
   bos = b;
   eos = e;
+}
+
+// Parent of sequence n in a tree launch, or -1 (no parent, not a tree launch, or
+// an index outside [-1, n), which the prep kernel reports).
+__device__ __forceinline__ int tree_parent(const Params& p, int n) {
+  if (!p.parent) return -1;
+  const int32_t pa = p.parent[n];
+  return (pa >= 0 && pa < n) ? pa : -1;
 }
 
 // Initial-state slot of sequence n, or -1 for a zero state (an out-of-range

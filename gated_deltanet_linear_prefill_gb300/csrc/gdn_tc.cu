@@ -275,7 +275,7 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, fl
 
 // Shared words of the MISC block: the TMEM base, the abort flag, the status
 // pointer and the unit, so that the slow path of a wait needs only addresses.
-constexpr uint32_t MISC_TMEM = 0, MISC_ABORT = 4, MISC_STATUS = 8, MISC_UNIT = 16;
+constexpr uint32_t MISC_TMEM = 0, MISC_ABORT = 4, MISC_STATUS = 8, MISC_UNIT = 16, MISC_WORK = 20;
 constexpr uint32_t kDrainWait = 0x8000u;  // site flag: a drain (ignores abort, shorter limit)
 
 // Slow path of every mbarrier wait: polls (each poll may park the thread until
@@ -318,7 +318,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   PrepScalars* ps = reinterpret_cast<PrepScalars*>(sm + L::PS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.x;
+  // A tree launch takes units in order from a counter, so that a unit's parent
+  // unit (earlier in the work list) already belongs to a running CTA.
+  int* tree_unit = reinterpret_cast<int*>(sm + L::MISC + MISC_WORK);
+  if (p.parent) {
+    if (tid == 0) *tree_unit = (int)atomicAdd(&p.status->next_unit, 1u);
+    __syncthreads();
+  }
+  const int unit = p.parent ? *tree_unit : (int)blockIdx.x;
   const int n = p.order[unit / p.h_v];
   const int h = unit % p.h_v;
   if (n < 0 || n >= p.num_seqs) {  // never expected: the prep kernel writes a permutation
@@ -805,10 +812,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int wb = tid - 384;  // == TMEM lane == d_v index
     const uint32_t lane_off = (uint32_t)((wb & ~31) << 16);
     const bool live = wb < DV;
-    // initial state -> S~^T in TMEM (lane d_v, column d_k), mu = 1
-    {
+    // initial state -> S~^T in TMEM (lane d_v, column d_k), mu = 1; in a tree launch a
+    // child's comes from its parent's final state, once the parent's unit has released it
+    bool ok_all = true;
+    const int par = tree_parent(p, n);
+    if (par >= 0) {
+      bool ok = true;
+      if (wb == 0) {
+        ok = wait_flag(&p.ready[(size_t)par * p.h_v + h], kWaitLimitNs);
+        if (!ok && !*abort_flag) {
+          *abort_flag = 1;
+          report(p.status, GDN_ERR_DEVICE_TIMEOUT, (uint32_t)unit * 16u + 5u);
+        }
+      }
+      if (named_bar_or(2, 128, !ok)) ok_all = false;
+    }
+    if (ok_all) {
       const int64_t slot = state_slot(p, n);
-      const float* s0 = slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + h) * DK * DV : nullptr;
+      const float* s0 = par >= 0 ? p.final_state + ((size_t)par * p.h_v + h) * DK * DV
+                                 : (slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + h) * DK * DV : nullptr);
 #pragma unroll 1
       for (int xb = 0; xb < DK / 32; ++xb) {
         uint32_t v[32];
@@ -820,7 +842,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_st_wait();
     }
     float mu = 1.f;
-    bool ok_all = true;
     const size_t osz = p.out_f32 ? 4 : 2;
     const int pieces = (int)(DV * osz / 16);  // 16-byte pieces of one output row
     const int pshift = __ffs(pieces) - 1;
@@ -1035,8 +1056,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!more) break;
     }
     if (wb == 0) bulk_wait_all();
-    // final state S = mu S~ (every MMA on S~ finished before the last O_DONE)
-    if (ok_all && !*abort_flag && p.final_state) {
+    // final state S = mu S~ (every MMA on S~ finished before the last O_DONE); the
+    // decision is taken once for the whole group, which then may meet at a barrier
+    const bool fin = p.final_state != nullptr && !named_bar_or(2, 128, !ok_all || *abort_flag);
+    if (fin) {
       tc_fence_after();
       float* fs = p.final_state + ((size_t)n * p.h_v + h) * DK * DV;
 #pragma unroll 1
@@ -1048,6 +1071,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int x = 0; x < 32; ++x) fs[(size_t)(xb * 32 + x) * DV + wb] = mu * __uint_as_float(v[x]);
         }
+      }
+      if (p.parent) {
+        // tree launch: the children of this unit may start from its final state
+        named_bar_sync(2, 128);  // every thread's stores before the release
+        if (wb == 0) release_flag(&p.ready[(size_t)n * p.h_v + h]);
       }
     }
   }

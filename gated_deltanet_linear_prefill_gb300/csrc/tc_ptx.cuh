@@ -69,6 +69,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
   return ok != 0;
 }
 
+// Polls a global flag written by another CTA (acquire at GPU scope) until it is
+// non-zero or `limit_ns` has passed; false on timeout.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint64_t limit_ns) {
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) return false;
+    __nanosleep(256);
+  }
+}
+// Sets a global flag for other CTAs after every earlier write of the calling
+// thread, and of the threads that met it at a barrier before, is visible.
+__device__ __forceinline__ void release_flag(uint32_t* flag) {
+  __threadfence();
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
+}
+
 // Volatile shared-memory word access by address.
 __device__ __forceinline__ uint32_t ld_shared_volatile_u32(uint32_t addr) {
   uint32_t v;

@@ -67,7 +67,8 @@ typedef enum {
   GDN_ERR_WORKSPACE = 8,      /* workspace NULL, misaligned or smaller than gdn_workspace_bytes */
   GDN_ERR_ARCH = 9,           /* the current device is not sm_103 */
   GDN_ERR_CUDA = 10,          /* a CUDA runtime call failed (launch, query, copy) */
-  GDN_ERR_DEVICE_TIMEOUT = 11 /* device: a bounded wait gave up */
+  GDN_ERR_DEVICE_TIMEOUT = 11, /* device: a bounded wait gave up */
+  GDN_ERR_PARENT = 12          /* device: a parent index outside [-1, n) (gdn_prefill_tree) */
 } gdn_status;
 
 /* Flags. */
@@ -186,6 +187,45 @@ gdn_status gdn_prefill_varlen_noalloc(const void* q, const void* k, const void* 
                                       const int32_t* cu_seqlens, const float* initial_state,
                                       const int32_t* state_index, void* out, float* final_state,
                                       const gdn_desc* desc, void* stream);
+
+/*
+ * Bytes of device workspace gdn_prefill_tree needs for this descriptor (0 for a
+ * NULL desc): the status word, the work list, a work counter and one ready flag
+ * per (sequence, value head). Like gdn_workspace_bytes, it needs no
+ * initialisation and is rewritten by every call.
+ */
+size_t gdn_tree_workspace_bytes(const gdn_desc* desc);
+
+/*
+ * A prefix tree of sequences in one launch: sequence n continues from the final
+ * state of sequence parent[n], computed by the same call.
+ *
+ * Where it comes from: System1-Omni PR #186 ("Purpose and summary") runs short
+ * continuations from a prefix's state; the open-jev-fast README (Phase 2 item
+ * 2, "Prefix tree") hands a long prompt's final recurrent state to each
+ * candidate, and its project page draws the two-level tree of the example
+ * request (shared context, question branches, candidate tails). With
+ * gdn_prefill_varlen such a tree takes one call per level; here the levels run
+ * in one launch, and a child's value head starts its state step as soon as its
+ * parent's final state for that head is written (its chunk preparation, which
+ * does not depend on the state, starts earlier still).
+ *
+ * Arguments are those of gdn_prefill_varlen plus
+ *  parent [N] int32, device: parent[n] in [-1, n). A sequence with parent -1 starts
+ *         from initial_state[state_index[n]] (or zero) exactly as in
+ *         gdn_prefill_varlen; any other starts from final_state[parent[n]].
+ * final_state is required (it carries the states handed from parent to child) and
+ * desc->workspace must hold gdn_tree_workspace_bytes(desc) bytes. A parent index
+ * outside [-1, n) sets GDN_ERR_PARENT in the device status word (the outputs are
+ * then unspecified); a child whose parent never finishes gives up after a bounded
+ * wait with GDN_ERR_DEVICE_TIMEOUT. The tensor-core kernel only: GDN_FLAG_SIMT
+ * returns GDN_ERR_SHAPE. Asynchronous on `stream`, no allocation, no host
+ * synchronisation.
+ */
+gdn_status gdn_prefill_tree(const void* q, const void* k, const void* v, const void* g,
+                            const void* beta, const int32_t* cu_seqlens, const int32_t* parent,
+                            const float* initial_state, const int32_t* state_index, void* out,
+                            float* final_state, const gdn_desc* desc, void* stream);
 
 /*
  * Synchronises `stream`, then returns the device status word the last call on

@@ -139,3 +139,56 @@ def run_workload(w, kind: str = "recurrent", **kw):
     fn = recurrent if kind == "recurrent" else chunked
     return fn(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state, w.state_index,
               scale=w.scale, **kw)
+
+
+
+def tree(q, k, v, g, beta, cu_seqlens, parent, initial_state=None, state_index=None, **kw):
+    """A prefix tree of sequences: sequence n starts from the final state of
+    sequence parent[n] (parent[n] in [-1, n)); a sequence with parent -1 starts
+    from initial_state[state_index[n]] (or zero) as in ``recurrent``.
+
+    This is the hand-off the open-jev-fast README describes for long prompts
+    (Phase 2 item 2, "Prefix tree": the prefix's final recurrent state goes to
+    each candidate) and System1-Omni PR #186 runs as compact prefix
+    continuations ("Purpose and summary"). Written out without any rounding at
+    the hand-off: each sequence's rows are the tail of its full root-to-node
+    path (the replicated layout the README uses for linear attention), run by
+    the fp64 recurrence from the root's starting state.
+    Returns (out [T, h_v, d_v], final [N, h_v, d_k, d_v]).
+    """
+    q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
+    cu = _i64(cu_seqlens)
+    par = _i64(parent)
+    s0 = _f32(initial_state)
+    sidx = _i64(state_index)
+    N = cu.size - 1
+    T, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    if par is None or par.size != N:
+        raise ValueError("parent needs one entry per sequence")
+    out = np.zeros((T, h_v, d_v), dtype=np.float64)
+    fs = np.zeros((N, h_v, d_k, d_v), dtype=np.float64)
+    for n in range(N):
+        path = [n]
+        while int(par[path[-1]]) >= 0:
+            p_ = int(par[path[-1]])
+            if p_ >= path[-1]:
+                raise ValueError(f"parent[{path[-1]}] = {p_} is not below {path[-1]}")
+            path.append(p_)
+        if int(par[path[-1]]) < -1:
+            raise ValueError(f"parent[{path[-1]}] = {int(par[path[-1]])} is below -1")
+        path.reverse()
+        root = path[0]
+        rows = np.concatenate([np.arange(int(cu[m]), int(cu[m + 1])) for m in path])
+        if s0 is not None:
+            slot = root if sidx is None else int(sidx[root])
+            start = s0[slot][None] if slot >= 0 else None
+        else:
+            start = None
+        o_p, f_p = _run("recurrent", q[rows], k[rows], v[rows], g[rows], beta[rows],
+                        np.array([0, rows.size], dtype=np.int64), start,
+                        None if start is None else np.array([0], dtype=np.int64), **kw)
+        b, e = int(cu[n]), int(cu[n + 1])
+        out[b:e] = o_p[rows.size - (e - b):]
+        fs[n] = f_p[0]
+    return out, fs

@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_prefill_varlen_noalloc",
-        "gdn_get_device_status", "gdn_status_string"])
+        "gdn_tree_workspace_bytes", "gdn_prefill_tree", "gdn_get_device_status",
+        "gdn_status_string"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -151,3 +152,50 @@ def test_valid_call_without_a_device_reports_cuda_or_arch():
     d = base_desc()
     rc = call(d)
     assert rc in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
+
+
+def call_tree(desc, parent=FAKE * 500, **ptrs):
+    if torch.cuda.is_available():
+        pytest.skip("fake-pointer validation calls run only without a device")
+    lib = gdn.load_library()
+    T = desc.total_tokens if desc else 100
+    qb = max(T, 1) * 16 * 128 * 2
+    base = dict(q=FAKE, k=FAKE + 4 * qb, v=FAKE + 8 * qb, g=FAKE + 16 * qb, beta=FAKE + 18 * qb,
+                cu=FAKE + 20 * qb, init=None, sidx=None, out=FAKE + 32 * qb, fs=FAKE * 600)
+    base.update(ptrs)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_prefill_tree(P(base["q"]), P(base["k"]), P(base["v"]), P(base["g"]),
+                                P(base["beta"]), P(base["cu"]), P(parent), P(base["init"]),
+                                P(base["sidx"]), P(base["out"]), P(base["fs"]),
+                                ctypes.byref(desc) if desc is not None else None, None)
+
+
+def test_tree_workspace_size():
+    lib = gdn.load_library()
+    assert lib.gdn_tree_workspace_bytes(None) == 0
+    d = base_desc(num_seqs=10)
+    need = gdn.gdn_tree_workspace_bytes(d)
+    assert need >= gdn.gdn_workspace_bytes(d) + 4 * 10 * 32 and need % 256 == 0
+
+
+def test_tree_host_checks():
+    need = gdn.gdn_tree_workspace_bytes(base_desc())
+    assert call_tree(None) == E["GDN_ERR_NULL"]
+    assert call_tree(base_desc(workspace_bytes=need), parent=None) == E["GDN_ERR_NULL"]
+    assert call_tree(base_desc(workspace_bytes=need), fs=None) == E["GDN_ERR_NULL"]
+    assert call_tree(base_desc(workspace_bytes=need, flags=gdn.GDN_FLAG_SIMT)) == E["GDN_ERR_SHAPE"]
+    # the varlen workspace is not enough for the ready flags
+    small = gdn.gdn_workspace_bytes(base_desc())
+    assert small < need
+    assert call_tree(base_desc(workspace_bytes=small)) == E["GDN_ERR_WORKSPACE"]
+    assert call_tree(base_desc(workspace_bytes=need), parent=FAKE * 500 + 2) == E["GDN_ERR_ALIGN"]
+    # the output overlapping the parent list
+    d = base_desc(workspace_bytes=need)
+    out = FAKE + 32 * 100 * 16 * 128 * 2
+    assert call_tree(d, parent=out + 64) == E["GDN_ERR_ALIAS"]
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path only")
+def test_valid_tree_call_without_a_device_reports_cuda_or_arch():
+    d = base_desc(workspace_bytes=gdn.gdn_tree_workspace_bytes(base_desc()))
+    assert call_tree(d) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
