@@ -399,6 +399,114 @@ def run_gdn(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_tree_bench(args):
+    """Latency of the two-level prefix tree of config 3 (one shared prompt, 3
+    question branches, 7 candidate tails; 11 nodes), three ways on one GPU:
+    one gdn_prefill_tree launch; three gdn_prefill_varlen calls, one per level,
+    each handing its final states to the next; and one call over the 7 full
+    root-to-leaf paths (the replicated layout). Inputs resident on the device;
+    each variant is timed over `steps` calls after `warmup`, with CUDA events
+    on the launching stream. Prints one JSON line."""
+    import gated_deltanet_linear_prefill_gb300 as gdn
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --tree needs a CUDA device")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    t = workloads.tree_config()
+    rows = t.rows
+    parent = torch.tensor([-1] + [0] * len(t.branch_lens) + [1 + b for b in t.leaf_parent],
+                          dtype=torch.int32)
+    n_nodes = int(parent.numel())
+    d = rows.to(device)
+    par = parent.to(device)
+    stream = torch.cuda.current_stream(device)
+    out = torch.empty(d.v.shape, dtype=d.out_dtype, device=device)
+    fs = torch.empty((n_nodes, d.h_v, d.d_k, d.d_v), dtype=torch.float32, device=device)
+    desc = gdn.make_desc(d.q, d.v, d.g, d.cu_seqlens, out_dtype=d.out_dtype)
+    ws = torch.empty(max(256, gdn.gdn_tree_workspace_bytes(desc)), dtype=torch.uint8, device=device)
+    desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
+
+    def tree_call():
+        rc = gdn.gdn_prefill_tree(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, par, None, None, out, fs,
+                                  desc, stream)
+        if rc != gdn.GDN_OK:
+            raise gdn.GdnError(rc, "gdn_prefill_tree")
+
+    # level by level
+    nb, nl = len(t.branch_lens), len(t.leaf_lens)
+    levels = [workloads.take_rows(rows, [[t.segment("prefix")]], "prefix"),
+              workloads.take_rows(rows, [[t.segment("branch", b)] for b in range(nb)], "branches"),
+              workloads.take_rows(rows, [[t.segment("leaf", l)] for l in range(nl)], "leaves")]
+    lv = [x.to(device) for x in levels]
+    lv_out = [torch.empty(x.v.shape, dtype=x.out_dtype, device=device) for x in lv]
+    lv_fs = [torch.empty((x.num_seqs, x.h_v, x.d_k, x.d_v), dtype=torch.float32, device=device)
+             for x in lv]
+    lv_sidx = [None, torch.zeros(nb, dtype=torch.int32, device=device),
+               torch.tensor(t.leaf_parent, dtype=torch.int32, device=device)]
+    lv_init = [None, lv_fs[0], lv_fs[1]]
+    lv_desc = []
+    for i, x in enumerate(lv):
+        dd = gdn.make_desc(x.q, x.v, x.g, x.cu_seqlens, out_dtype=x.out_dtype,
+                           initial_state=lv_init[i])
+        w_ = torch.empty(max(256, gdn.gdn_workspace_bytes(dd)), dtype=torch.uint8, device=device)
+        dd.workspace, dd.workspace_bytes = w_.data_ptr(), w_.numel()
+        lv_desc.append((dd, w_))
+
+    def level_calls():
+        for i, x in enumerate(lv):
+            rc = gdn.gdn_prefill_varlen(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, lv_init[i],
+                                        lv_sidx[i], lv_out[i], lv_fs[i], lv_desc[i][0], stream)
+            if rc != gdn.GDN_OK:
+                raise gdn.GdnError(rc, "gdn_prefill_varlen")
+
+    # replicated full paths
+    pw = workloads.take_rows(rows, [[t.segment("prefix"), t.segment("branch", t.leaf_parent[l]),
+                                     t.segment("leaf", l)] for l in range(nl)], "paths").to(device)
+    p_out = torch.empty(pw.v.shape, dtype=pw.out_dtype, device=device)
+    p_fs = torch.empty((pw.num_seqs, pw.h_v, pw.d_k, pw.d_v), dtype=torch.float32, device=device)
+    p_desc = gdn.make_desc(pw.q, pw.v, pw.g, pw.cu_seqlens, out_dtype=pw.out_dtype)
+    p_ws = torch.empty(max(256, gdn.gdn_workspace_bytes(p_desc)), dtype=torch.uint8, device=device)
+    p_desc.workspace, p_desc.workspace_bytes = p_ws.data_ptr(), p_ws.numel()
+
+    def path_call():
+        rc = gdn.gdn_prefill_varlen(pw.q, pw.k, pw.v, pw.g, pw.beta, pw.cu_seqlens, None, None,
+                                    p_out, p_fs, p_desc, stream)
+        if rc != gdn.GDN_OK:
+            raise gdn.GdnError(rc, "gdn_prefill_varlen")
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(device)
+        ts = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    us_tree, us_levels, us_paths = timed(tree_call), timed(level_calls), timed(path_call)
+    rc = gdn.gdn_get_device_status(desc, stream)
+    if rc != gdn.GDN_OK:
+        raise gdn.GdnError(rc, "device status")
+    T = int(rows.q.shape[0])
+    line = {
+        "metric": "GDN prefix-tree prefill latency (config 3 tree, one launch)",
+        "value": us_tree, "unit": "us per tree", "higher_is_better": False, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+        "variants_us": {"tree_one_launch": us_tree, "three_level_calls": us_levels,
+                        "replicated_full_paths": us_paths},
+        "gpu_launches": {"tree_one_launch": 2, "three_level_calls": 6, "replicated_full_paths": 2},
+        "config": {"workload": "cfg3_prefix_tree", "nodes": n_nodes, "tokens": T,
+                   "replicated_path_tokens": int(pw.q.shape[0]), "h_qk": d.h_qk, "h_v": d.h_v,
+                   "d": d.d_k, "timing": "median of per-call CUDA events, inputs resident"},
+    }
+    print(json.dumps(line))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,7 +520,12 @@ def main(argv=None):
                     help="time only the first K sequences of the batch (small profiling case)")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="seconds of untimed steps while the clock sampler warms up")
+    ap.add_argument("--tree", action="store_true",
+                    help="time the config 3 prefix tree (one launch vs level by level vs full paths)")
     args = ap.parse_args(argv)
+    if args.tree:
+        run_tree_bench(args)
+        return
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
