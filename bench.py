@@ -507,6 +507,103 @@ def run_tree_bench(args):
     print(json.dumps(line))
 
 
+def run_latency_bench(args):
+    """Per-call latency of the small, launch-bound workloads (inputs resident):
+    config 0, config 1 (one 539-token prompt, 32 value heads), a batch of seven
+    65-96-token candidate paths (two chunks each), and the config 3 prefix tree
+    in one launch. Each is timed as plain launches and as a CUDA graph replay
+    (the call captured once), median of `steps` calls after `warmup`, with
+    CUDA events on the launching stream. Prints one JSON line."""
+    import gated_deltanet_linear_prefill_gb300 as gdn
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --latency needs a CUDA device")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+
+    def varlen_case(w):
+        d = w.to(device)
+        out = torch.empty(d.v.shape, dtype=d.out_dtype, device=device)
+        fs = torch.empty((d.num_seqs, d.h_v, d.d_k, d.d_v), dtype=torch.float32, device=device)
+        desc = gdn.make_desc(d.q, d.v, d.g, d.cu_seqlens, out_dtype=d.out_dtype,
+                             initial_state=d.initial_state, max_seqlen=w.max_seqlen)
+        ws = torch.empty(max(256, gdn.gdn_workspace_bytes(desc)), dtype=torch.uint8, device=device)
+        desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
+        keep = (d, out, fs, ws)
+
+        def call():
+            rc = gdn.gdn_prefill_varlen(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, d.initial_state,
+                                        d.state_index, out, fs, desc, stream)
+            if rc != gdn.GDN_OK:
+                raise gdn.GdnError(rc, "gdn_prefill_varlen")
+        return call, keep, int(w.q.shape[0])
+
+    def tree_case():
+        t = workloads.tree_config()
+        d = t.rows.to(device)
+        par = torch.tensor([-1] + [0] * len(t.branch_lens) + [1 + b for b in t.leaf_parent],
+                           dtype=torch.int32, device=device)
+        out = torch.empty(d.v.shape, dtype=d.out_dtype, device=device)
+        fs = torch.empty((d.num_seqs, d.h_v, d.d_k, d.d_v), dtype=torch.float32, device=device)
+        desc = gdn.make_desc(d.q, d.v, d.g, d.cu_seqlens, out_dtype=d.out_dtype)
+        ws = torch.empty(max(256, gdn.gdn_tree_workspace_bytes(desc)), dtype=torch.uint8,
+                         device=device)
+        desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
+        keep = (d, par, out, fs, ws)
+
+        def call():
+            rc = gdn.gdn_prefill_tree(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, par, None, None,
+                                      out, fs, desc, stream)
+            if rc != gdn.GDN_OK:
+                raise gdn.GdnError(rc, "gdn_prefill_tree")
+        return call, keep, int(t.rows.q.shape[0])
+
+    rng = np.random.default_rng(5)
+    short = workloads.random_workload([int(x) for x in rng.integers(65, 97, 7)], h_qk=16, h_v=32,
+                                      d_k=128, d_v=128, seed=5)
+    cases = {"cfg0_tiny_T128_d64": varlen_case(workloads.config(0)),
+             "cfg1_single_T539": varlen_case(workloads.config(1)),
+             "short_paths_7x65to96": varlen_case(short),
+             "cfg3_prefix_tree_one_launch": tree_case()}
+
+    def med(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                fn()
+        stream.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    res = {}
+    for name, (call, keep, tokens) in cases.items():
+        plain = med(call)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            call()  # the library's one-time set-up happens outside the capture
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                call()
+        def replay(g=g):
+            with torch.cuda.stream(stream):
+                g.replay()
+        graph = med(replay)
+        res[name] = {"tokens": tokens, "us_per_call": plain, "us_per_graph_replay": graph}
+    line = {"metric": "GDN prefill latency of small workloads (per call, one GB300)",
+            "value": res["cfg1_single_T539"]["us_per_graph_replay"], "unit": "us per call",
+            "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "dtype": "bf16", "data": "synthetic", "cases": res,
+            "config": {"workload": "cfg1_single_T539 (value); all cases under 'cases'",
+                       "timing": "median of per-call CUDA events, inputs resident"}}
+    print(json.dumps(line))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,7 +619,12 @@ def main(argv=None):
                     help="seconds of untimed steps while the clock sampler warms up")
     ap.add_argument("--tree", action="store_true",
                     help="time the config 3 prefix tree (one launch vs level by level vs full paths)")
+    ap.add_argument("--latency", action="store_true",
+                    help="per-call latency of configs 0, 1, short two-chunk paths and the config 3 tree")
     args = ap.parse_args(argv)
+    if args.latency:
+        run_latency_bench(args)
+        return
     if args.tree:
         run_tree_bench(args)
         return
