@@ -19,7 +19,10 @@
 // spans more than kMaxSpan, which keeps every factorised exponential in fp32
 // range for any finite gate.
 //
-// One CTA owns one (sequence, value head) chain and walks its chunks in order.
+// One CTA per SM stays resident and takes (sequence, value head) units in turn
+// from a counter (longest first), walking each unit's chunks in order; the
+// chunks of successive units form one stream through the pipeline, so it does
+// not drain between units.
 // All dense products run on tcgen05 in the "d-major" orientation, where the
 // 128 TMEM lanes index d_v (or d_k) so every MMA has M = 128:
 //   [K;Q] K^T                    KK^T (lanes 0-63) and QK^T (lanes 64-127)
@@ -45,6 +48,8 @@
 // CTA reports GDN_ERR_DEVICE_TIMEOUT and unwinds.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "gdn_internal.cuh"
 #include "tc_ptx.cuh"
@@ -99,15 +104,25 @@ constexpr int SC_NULOG = 196;  // log of the W' weight applied to e^{G_j}
 constexpr int SC_RMW = 197;    // factor applied to the stored state first (1 unless eager)
 constexpr int SC_MUNEXT = 198; // mu after this chunk
 constexpr int SC_M = 199;      // rows (int)
-constexpr int SC_FLAGS = 200;  // bit 0: last chunk of the sequence; bit 1: eager
+constexpr int SC_FLAGS = 200;  // F_* bits below
 constexpr int SC_T0 = 202;     // first row (int64, two words)
+constexpr int SC_N = 204;      // the chunk's sequence (int)
+constexpr int SC_H = 205;      // the chunk's value head (int)
+// chunk flags
+constexpr int F_ULAST = 1;     // last chunk of its (sequence, head) unit
+constexpr int F_EAGER = 2;     // the stored state is rescaled before this chunk
+constexpr int F_UFIRST = 4;    // first chunk of its unit: the state starts over
+constexpr int F_SLAST = 8;     // last chunk this CTA processes
 
 // Per-chunk values WG-A hands to WG-B (three buffers, chunk % 3).
 struct ChunkScalars {
   float co[64];  // scale r^q_i e^{G_i - G_m} lambda: output weight of row i (0 past m)
   long long t0;  // first row of the chunk
   float mu_next; // mu after the chunk
-  int m, last, pad[3];
+  int m;         // rows
+  int slast;     // the last chunk this CTA processes
+  int n, h;      // the chunk's (sequence, value head) unit
+  int pad;
 };
 // WG-A private per-chunk values.
 struct PrepScalars {
@@ -318,31 +333,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   PrepScalars* ps = reinterpret_cast<PrepScalars*>(sm + L::PS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // A tree launch takes units in order from a counter, so that a unit's parent
-  // unit (earlier in the work list) already belongs to a running CTA.
-  int* tree_unit = reinterpret_cast<int*>(sm + L::MISC + MISC_WORK);
-  if (p.parent) {
-    if (tid == 0) *tree_unit = (int)atomicAdd(&p.status->next_unit, 1u);
-    __syncthreads();
-  }
-  const int unit = p.parent ? *tree_unit : (int)blockIdx.x;
-  const int n = p.order[unit / p.h_v];
-  const int h = unit % p.h_v;
-  if (n < 0 || n >= p.num_seqs) {  // never expected: the prep kernel writes a permutation
-    if (tid == 0) report(p.status, GDN_ERR_SEQLENS, (uint32_t)unit);
-    return;
-  }
-  const int hq = h / (p.h_v / p.h_qk);
-  int64_t bos, eos;
-  seq_bounds(p, n, bos, eos);
-  const int64_t len = eos - bos;
+  // The CTA stays resident and takes (sequence, head) units in order from a counter
+  // (the work list is longest first; in a tree launch parents come before children),
+  // running their chunks as one stream so that the pipeline does not drain between
+  // units. Thread 0 takes the first unit here; the producer takes the rest.
+  const int total_units = p.num_seqs * p.h_v;
+  int* first_unit = reinterpret_cast<int*>(sm + L::MISC + MISC_WORK);
+  if (tid == 0) *first_unit = (int)atomicAdd(&p.status->next_unit, 1u);
 
   // ---- setup
   if (tid == 0) {
     for (int b = 0; b < kNumBars; ++b) mbar_init(&bars[b], 1u);
     *abort_flag = 0;
     *reinterpret_cast<Status**>(sm + L::MISC + MISC_STATUS) = p.status;
-    *reinterpret_cast<uint32_t*>(sm + L::MISC + MISC_UNIT) = (uint32_t)unit;
+    *reinterpret_cast<uint32_t*>(sm + L::MISC + MISC_UNIT) = (uint32_t)blockIdx.x;
     mbar_init_fence();
   }
   if (L::NEED_ZERO)
@@ -360,6 +364,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_ptr;
+  const bool any = *first_unit < total_units;  // this CTA has at least one unit
 
   auto slot_kq = [&](int c) { return sbase + L::RING0 + (uint32_t)(c % 3) * L::SLOT_BYTES; };
   auto slot_v = [&](int c) { return sbase + L::V0 + (uint32_t)(c & 1) * L::V_BYTES; };
@@ -380,7 +385,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the chunk's tiles once its ring slots are free. It never waits for data.
     const uint32_t kq_bytes = (uint32_t)(2 * L::NKA) * 8192u, v_bytes = (uint32_t)L::NVA * 8192u;
     int kq_issued = 0, v_issued = 0;  // chunks whose K / Q and V loads were requested
-    if (len > 0) {
+    int cur = *first_unit, g = 0;     // the unit in hand; chunks emitted so far
+    // the next unit is taken one unit ahead, so that a chunk knows whether it is the CTA's last
+    auto take_unit = [&]() {
+      int u = 0;
+      if (lane == 0) u = (int)atomicAdd(&p.status->next_unit, 1u);
+      return __shfl_sync(0xffffffffu, u, 0);
+    };
+    int nxt = cur < total_units ? take_unit() : total_units;
+    bool ok = true;
+#pragma unroll 1
+    while (ok && cur < total_units) {
+      int n = p.order[cur / p.h_v];
+      if (n < 0 || n >= p.num_seqs) {  // never expected: the prep kernel writes a permutation
+        if (lane == 0) report(p.status, GDN_ERR_SEQLENS, (uint32_t)cur);
+        n = 0;
+      }
+      const int h = cur % p.h_v, hq = h / (p.h_v / p.h_qk);
+      int64_t bos, eos;
+      seq_bounds(p, n, bos, eos);
+      const int64_t len = eos - bos;  // 0: one chunk of no rows carries the unit's state through
       int64_t start = 0;
       float logmu = 0.f;
       float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
@@ -398,7 +422,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       load_gates(0);
 #pragma unroll 1
-      for (int c = 0;; ++c) {
+      for (int cu = 0;; ++cu, ++g) {
         const int mv = (int)(len - start < kChunk ? len - start : kChunk);
         // inclusive prefix sums and prefix max / min (the chunk start, 0, included)
         float s0 = g0, s1 = g1;
@@ -420,11 +444,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
             wmin = fminf(wmin, __shfl_xor_sync(0xffffffffu, wmin, o));
           }
-          if (wmax - wmin <= kMaxSpan || m == 1) break;
+          if (wmax - wmin <= kMaxSpan || m <= 1) break;
           m = (m + 1) >> 1;
         }
         // rows past m: no decay, no write
-        const float Gm = __shfl_sync(0xffffffffu, (m - 1) < 32 ? s0 : s1, (m - 1) & 31);
+        const float Gm = m > 0 ? __shfl_sync(0xffffffffu, (m - 1) < 32 ? s0 : s1, (m - 1) & 31) : 0.f;
         if (lane >= m) { s0 = Gm; b0 = 0.f; }
         if (lane + 32 >= m) { s1 = Gm; b1 = 0.f; }
         float gmax = fmaxf(lane < m ? s0 : -3.0e38f, lane + 32 < m ? s1 : -3.0e38f);
@@ -436,19 +460,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const float loglam = logmu + Gm;
         const bool eager = fabsf(loglam) > kMaxLogScale;
-        const bool last = start + m >= len;
+        const bool ulast = start + m >= len;
+        const bool slast = ulast && nxt >= total_units;
         const float b0c = b0, b1c = b1;
-        if (!last) load_gates(start + m);  // the next chunk's gates, in flight while this one waits
-        // the K / Q ring slot of chunk c-3 was released
-        bool ok = true;
-        if (c >= 3) ok = wait(B_KQE0 + c % 3, ((c / 3) + 1) & 1, 0);
+        if (!ulast) load_gates(start + m);  // the next chunk's gates, in flight while this one waits
+        // the K / Q ring slot of chunk g-3 was released
+        if (g >= 3) ok = wait(B_KQE0 + g % 3, ((g / 3) + 1) & 1, 0);
         if (!ok) break;
-        float* sc = slot_sc(c);
+        float* sc = slot_sc(g);
         sc[SC_G + lane] = s0;
         sc[SC_G + lane + 32] = s1;
         sc[SC_B + lane] = b0c;
         sc[SC_B + lane + 32] = b1c;
         __syncwarp();  // every lane's scalars before lane 0's arrive publishes them
+        const int row = (int)(bos + start);
         if (lane == 0) {
           sc[SC_GMAX] = gmax;
           sc[SC_GMIN] = gmin;
@@ -458,38 +483,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           sc[SC_RMW] = eager ? exp2f(loglam * kLog2e) : 1.f;
           sc[SC_MUNEXT] = eager ? 1.f : exp2f(loglam * kLog2e);
           sc[SC_M] = __int_as_float(m);
-          sc[SC_FLAGS] = __int_as_float((last ? 1 : 0) | (eager ? 2 : 0));
+          sc[SC_FLAGS] = __int_as_float((ulast ? F_ULAST : 0) | (eager ? F_EAGER : 0) |
+                                        (cu == 0 ? F_UFIRST : 0) | (slast ? F_SLAST : 0));
           *reinterpret_cast<long long*>(&sc[SC_T0]) = (long long)(bos + start);
-          // the arrive publishes the scalars; the K / Q tiles complete the phase
-          const int row = (int)(bos + start);
-          uint64_t* full = &bars[B_FULL0 + c % 3];
+          sc[SC_N] = __int_as_float(n);
+          sc[SC_H] = __int_as_float(h);
+          // the arrive publishes the scalars; the K / Q tiles complete the phase (a chunk of
+          // no rows at the end of the tensor reads zeros)
+          uint64_t* full = &bars[B_FULL0 + g % 3];
           mbar_arrive_expect_tx(full, kq_bytes);
-          const uint32_t kq = slot_kq(c);
+          const uint32_t kq = slot_kq(g);
 #pragma unroll 1
           for (int a = 0; a < 2 * L::NKA; ++a)  // K, Q per atom column
             tma_load_3d(sm + (kq - sbase) + (a >> 1) * 16384 + (a & 1) * 8192, (a & 1) ? &tm.q : &tm.k, full,
                         64 * (a >> 1), hq, row);
         }
         __syncwarp();
-        kq_issued = c + 1;
-        // V has its own ring (two slots, released by chunk c-2's U product) and barrier, so
+        kq_issued = g + 1;
+        // V has its own ring (two slots, released by chunk g-2's U product) and barrier, so
         // the K / Q tiles above never wait for it
-        if (c >= 2) ok = wait(B_VE0 + (c & 1), ((c >> 1) + 1) & 1, 0);
+        if (g >= 2) ok = wait(B_VE0 + (g & 1), ((g >> 1) + 1) & 1, 0);
         if (!ok) break;
         if (lane == 0) {
-          const int row = (int)(bos + start);
-          uint64_t* vfull = &bars[B_VFULL0 + (c & 1)];
+          uint64_t* vfull = &bars[B_VFULL0 + (g & 1)];
           mbar_arrive_expect_tx(vfull, v_bytes);
-          const uint32_t vv = slot_v(c);
+          const uint32_t vv = slot_v(g);
 #pragma unroll 1
           for (int a = 0; a < L::NVA; ++a) tma_load_3d(sm + (vv - sbase) + a * 8192, &tm.v, vfull, 64 * a, h, row);
         }
         __syncwarp();
-        v_issued = c + 1;
-        if (last) break;
+        v_issued = g + 1;
+        if (ulast) {
+          ++g;
+          break;
+        }
         start += m;
         logmu = eager ? 0.f : loglam;
       }
+      if (nxt >= total_units) break;
+      cur = nxt;
+      nxt = take_unit();
     }
     // let every requested tile land before the CTA can exit (on the normal path
     // they were all consumed and these return at once)
@@ -503,7 +536,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ================================================================ state-independent MMAs
     // [K;Q] K^T of chunk c+1 as soon as its tiles are in and WG-A has read chunk c's;
     // then W'^T = K^T T_w^T and U^T = V^T T_b^T of chunk c once WG-A has written T_b / T_w.
-    if (lane == 0 && len > 0) {
+    if (lane == 0 && any) {
       constexpr uint32_t id_kq = idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
       auto issue_kq = [&](int c) {
@@ -523,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
       for (int c = 0; run; ++c) {
         const int par = c & 1;
-        const bool last = sc_int(slot_sc(c), SC_FLAGS) & 1;
+        const bool last = sc_int(slot_sc(c), SC_FLAGS) & F_SLAST;
         if (!last) {
           if (!wait(B_FULL0 + (c + 1) % 3, ((c + 1) / 3) & 1, 2) || !wait(B_KQ_FREE, c & 1, 2)) break;
           tc_fence_after();
@@ -558,7 +591,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 2) {
     // ================================================================ state-dependent MMAs
-    if (lane == 0 && len > 0) {
+    if (lane == 0 && any) {
       constexpr uint32_t id_sw = idesc_bf16(128, 64, 0, 1);
       constexpr uint32_t id_qs = idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_st = idesc_bf16(128, DK, 0, 1);
@@ -571,7 +604,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const bool last = cscal[c % 3].last;  // read now: the buffer is reused after this chunk
+        const bool last = cscal[c % 3].slast;  // read now: the buffer is reused after this chunk
         const uint32_t kq = slot_kq(c);
         // U'^T += S~^T W'^T : A = S~^T (bf16, TMEM), B = W'^T MN-major [d_k][j]
         const uint64_t dwt = sdesc(sbase + L::WT0 + par * L::SCR_BYTES, 16, 1024);
@@ -619,7 +652,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // r^q_i from the diagonal of Q Q^T, 16 rows at a time on the warp-level tensor
     // cores (bf16 products are exact in fp32), straight from the swizzled tile and
     // off the path of the chunk preparation (r^q only weights the output rows).
-    if (len > 0) {
+    if (any) {
       const int g = lane >> 2, t = lane & 3;
       // ldmatrix rows: matrices 0 / 1 are rows 0-7 / 8-15 of k 0-7, 2 / 3 the same of k 8-15
       const uint32_t lr = (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1)), lk = (uint32_t)(lane >> 4);
@@ -650,7 +683,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_RQ0 + c % 3]);
-        if (sc_int(sc, SC_FLAGS) & 1) break;
+        if (sc_int(sc, SC_FLAGS) & F_SLAST) break;
       }
     }
   } else if (warp < 12) {
@@ -661,7 +694,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_off = (uint32_t)((Ln & ~31) << 16);
     const bool krow = Ln < 64;
     const int i = Ln & 63;
-    if (len > 0) {
+    if (any) {
 #pragma unroll 1
       for (int c = 0;; ++c) {
         const int par = c & 1;
@@ -677,7 +710,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float* sc = slot_sc(c);
         ChunkScalars& cs = cscal[c % 3];
         const int m = sc_int(sc, SC_M);
-        const bool last = sc_int(sc, SC_FLAGS) & 1;
+        const bool last = sc_int(sc, SC_FLAGS) & F_SLAST;
         const float gmax = sc[SC_GMAX], Gm = sc[SC_GM], lamlog = sc[SC_LAMLOG];
         const float Gi = sc[SC_G + i];
         uint32_t v[32];  // row Ln of [K;Q] K^T, columns [32 hf, 32 hf + 32)
@@ -708,7 +741,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             cs.t0 = *reinterpret_cast<const long long*>(&sc[SC_T0]);
             cs.mu_next = sc[SC_MUNEXT];
             cs.m = m;
-            cs.last = last ? 1 : 0;
+            cs.slast = last ? 1 : 0;
+            cs.n = sc_int(sc, SC_N);
+            cs.h = sc_int(sc, SC_H);
           }
         }
         named_bar_sync(1, 256);
@@ -812,25 +847,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int wb = tid - 384;  // == TMEM lane == d_v index
     const uint32_t lane_off = (uint32_t)((wb & ~31) << 16);
     const bool live = wb < DV;
-    // initial state -> S~^T in TMEM (lane d_v, column d_k), mu = 1; in a tree launch a
-    // child's comes from its parent's final state, once the parent's unit has released it
     bool ok_all = true;
-    const int par = tree_parent(p, n);
-    if (par >= 0) {
-      bool ok = true;
-      if (wb == 0) {
-        ok = wait_flag(&p.ready[(size_t)par * p.h_v + h], kWaitLimitNs);
-        if (!ok && !*abort_flag) {
-          *abort_flag = 1;
-          report(p.status, GDN_ERR_DEVICE_TIMEOUT, (uint32_t)unit * 16u + 5u);
+    // A unit's final state S = mu S~, once its last S~ update has finished; in a tree
+    // launch the unit's children may then start from it.
+    auto store_final = [&](int un, int uh, float umu) {
+      if (!p.final_state) return;
+      float* fs = p.final_state + ((size_t)un * p.h_v + uh) * DK * DV;
+#pragma unroll 1
+      for (int xb = 0; xb < DK / 32; ++xb) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + TM_S + xb * 32, v);
+        tmem_ld_wait();
+        if (live) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) fs[(size_t)(xb * 32 + x) * DV + wb] = umu * __uint_as_float(v[x]);
         }
       }
-      if (named_bar_or(2, 128, !ok)) ok_all = false;
-    }
-    if (ok_all) {
-      const int64_t slot = state_slot(p, n);
-      const float* s0 = par >= 0 ? p.final_state + ((size_t)par * p.h_v + h) * DK * DV
-                                 : (slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + h) * DK * DV : nullptr);
+      if (p.parent) {
+        named_bar_sync(2, 128);  // every thread's stores before the release
+        if (wb == 0) release_flag(&p.ready[(size_t)un * p.h_v + uh]);
+      }
+    };
+    // A unit's starting state -> S~^T in TMEM (lane d_v, column d_k), mu = 1: an
+    // initial-state slot or zero, or in a tree launch a child's parent's final state once
+    // the parent's unit has released it. False if that wait gave up.
+    auto load_initial = [&](int un, int uh) {
+      const int par = tree_parent(p, un);
+      if (par >= 0) {
+        bool ok = true;
+        if (wb == 0) {
+          ok = wait_flag(&p.ready[(size_t)par * p.h_v + uh], kWaitLimitNs);
+          if (!ok && !*abort_flag) {
+            *abort_flag = 1;
+            report(p.status, GDN_ERR_DEVICE_TIMEOUT, blockIdx.x * 16u + 5u);
+          }
+        }
+        if (named_bar_or(2, 128, !ok)) return false;
+      }
+      const int64_t slot = state_slot(p, un);
+      const float* s0 = par >= 0 ? p.final_state + ((size_t)par * p.h_v + uh) * DK * DV
+                                 : (slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + uh) * DK * DV : nullptr);
 #pragma unroll 1
       for (int xb = 0; xb < DK / 32; ++xb) {
         uint32_t v[32];
@@ -840,15 +896,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_st32(tmem + lane_off + TM_S + xb * 32, v);
       }
       tmem_st_wait();
-    }
-    float mu = 1.f;
+      return true;
+    };
+    int un_c = 0, uh_c = 0;  // the unit of the chunk whose state step ran last,
+    float mu_c = 1.f;        // and mu after it
+    int clast = -1;
     const size_t osz = p.out_f32 ? 4 : 2;
     const int pieces = (int)(DV * osz / 16);  // 16-byte pieces of one output row
     const int pshift = __ffs(pieces) - 1;
     uint32_t npass = 0;  // epilogue passes so far (selects the staging tile)
 #pragma unroll 1
     for (int c = -1;; ++c) {
-      bool more = len > 0 && c < 0;
+      bool more = any && c < 0;
       if (c >= 0) {
         // ---- (U' diag(s/lambda))^T -> bf16 hi / lo A operands
         const ChunkScalars& cs = cscal[c % 3];
@@ -877,7 +936,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive(&bars[B_R_FREE]);
           mbar_arrive(&bars[B_UOPS_READY]);
         }
-        more = !cs.last;
+        more = !cs.slast;
+        un_c = cs.n;
+        uh_c = cs.h;
+        mu_c = cs.mu_next;
+        clast = c;
       }
       if (more) {
         // ---- S~ -> bf16 A operand for chunk c+1 (first applying its decay when eager)
@@ -887,7 +950,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ok && c >= 0) ok = wait(B_STATE_DONE, c & 1, 11);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
-        const bool eager = sc_int(sc, SC_FLAGS) & 2;
+        if (sc_int(sc, SC_FLAGS) & F_UFIRST) {
+          // chunk cn starts a unit: the one that ended with chunk c is complete
+          if (c >= 0) store_final(un_c, uh_c, mu_c);
+          if (!load_initial(sc_int(sc, SC_N), sc_int(sc, SC_H))) { ok_all = false; break; }
+        }
+        const bool eager = sc_int(sc, SC_FLAGS) & F_EAGER;
         const float rmw = sc[SC_RMW];
 #pragma unroll 1
         for (int xb = 0; xb < DK / 32; ++xb) {
@@ -954,7 +1022,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const int m = cs.m;
         const long long t0 = cs.t0;
-        mu = cs.mu_next;
         if (!p.out_f32) {
           // each thread takes consecutive row pairs of its 16-lane blocks (16 x 256b loads)
           // and writes 8x8 blocks transposed into the row-major tiles (the eight rows of a
@@ -997,7 +1064,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (wb == 0) {
 #pragma unroll
               for (int tl = 0; tl < DV / 64; ++tl)
-                tma_store_3d(&tm.o, sm + L::STG + tl * 8192, 64 * tl, h, (int)t0);
+                tma_store_3d(&tm.o, sm + L::STG + tl * 8192, 64 * tl, cs.h, (int)t0);
               bulk_commit();
             }
           } else {
@@ -1005,7 +1072,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const int r = idx >> pshift, pc = idx & (pieces - 1);
               const uint4 x = *reinterpret_cast<const uint4*>(
                   sm + L::STG + (pc >> 3) * 8192 + sw128((uint32_t)r, (uint32_t)(pc & 7)));
-              char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + r) * p.h_v + h) * DV) * osz;
+              char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + r) * p.h_v + cs.h) * DV) * osz;
               *reinterpret_cast<uint4*>(dst + pc * 16) = x;
             }
           }
@@ -1034,12 +1101,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             named_bar_sync(2, 128);
             const int rows = m - p0 < 16 ? m - p0 : 16;
             if (rows == 16) {
-              if (wb == 0) tma_store_3d(&tm.o, stage, 0, h, (int)(t0 + p0));
+              if (wb == 0) tma_store_3d(&tm.o, stage, 0, cs.h, (int)(t0 + p0));
             } else {
               for (int idx = wb; idx < (rows << pshift); idx += 128) {
                 const int r = idx >> pshift, pc = idx & (pieces - 1);
                 const uint4 x = *reinterpret_cast<const uint4*>(stage + r * DV * 4 + pc * 16);
-                char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + h) * DV) * osz;
+                char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + cs.h) * DV) * osz;
                 *reinterpret_cast<uint4*>(dst + pc * 16) = x;
               }
             }
@@ -1056,27 +1123,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!more) break;
     }
     if (wb == 0) bulk_wait_all();
-    // final state S = mu S~ (every MMA on S~ finished before the last O_DONE); the
+    // the last unit's final state (every MMA on S~ finished before the last O_DONE); the
     // decision is taken once for the whole group, which then may meet at a barrier
-    const bool fin = p.final_state != nullptr && !named_bar_or(2, 128, !ok_all || *abort_flag);
-    if (fin) {
+    if (!named_bar_or(2, 128, !ok_all || *abort_flag || clast < 0)) {
       tc_fence_after();
-      float* fs = p.final_state + ((size_t)n * p.h_v + h) * DK * DV;
-#pragma unroll 1
-      for (int xb = 0; xb < DK / 32; ++xb) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + TM_S + xb * 32, v);
-        tmem_ld_wait();
-        if (live) {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) fs[(size_t)(xb * 32 + x) * DV + wb] = mu * __uint_as_float(v[x]);
-        }
-      }
-      if (p.parent) {
-        // tree launch: the children of this unit may start from its final state
-        named_bar_sync(2, 128);  // every thread's stores before the release
-        if (wb == 0) release_flag(&p.ready[(size_t)n * p.h_v + h]);
-      }
+      store_final(un_c, uh_c, mu_c);
     }
   }
   tc_fence_before();
@@ -1132,6 +1183,25 @@ bool encode_out(CUtensorMap* m, void* base, int64_t T, int H, int D, bool f32) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+cudaError_t sm_count(int* out) {
+  static std::mutex mu;
+  static int cached[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cached[dev] = n > 0 ? n : 1;
+  }
+  *out = cached[dev];
+  return cudaSuccess;
+}
+
 template <int DK, int DV>
 cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   using L = TcLayout<DK, DV>;
@@ -1145,7 +1215,13 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long long units = (long long)p.num_seqs * p.h_v;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  gdn_tc_kernel<DK, DV><<<(unsigned)units, kTcThreads, L::DYN_SMEM, stream>>>(p, tm);
+  // one resident CTA per SM (the kernel's shared memory and TMEM fill an SM), each
+  // taking units until the work list is exhausted
+  int sms = 0;
+  e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  const long long grid = units < sms ? units : sms;
+  gdn_tc_kernel<DK, DV><<<(unsigned)grid, kTcThreads, L::DYN_SMEM, stream>>>(p, tm);
   return cudaGetLastError();
 }
 
