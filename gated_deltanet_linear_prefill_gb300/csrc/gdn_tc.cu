@@ -318,7 +318,9 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint32_t m
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int DK, int DV>
+// OF32: fp32 output (else bf16), a template parameter so that each kernel holds
+// only its own epilogue.
+template <int DK, int DV, bool OF32>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gdn_tc_kernel(const Params p, const __grid_constant__ Tmaps tm) {
   using L = TcLayout<DK, DV>;
@@ -901,7 +903,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int un_c = 0, uh_c = 0;  // the unit of the chunk whose state step ran last,
     float mu_c = 1.f;        // and mu after it
     int clast = -1;
-    const size_t osz = p.out_f32 ? 4 : 2;
+    constexpr size_t osz = OF32 ? 4 : 2;
     const int pieces = (int)(DV * osz / 16);  // 16-byte pieces of one output row
     const int pshift = __ffs(pieces) - 1;
     uint32_t npass = 0;  // epilogue passes so far (selects the staging tile)
@@ -1022,7 +1024,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const int m = cs.m;
         const long long t0 = cs.t0;
-        if (!p.out_f32) {
+        if constexpr (!OF32) {
           // each thread takes consecutive row pairs of its 16-lane blocks (16 x 256b loads)
           // and writes 8x8 blocks transposed into the row-major tiles (the eight rows of a
           // block hit distinct banks under the swizzle); a tile row is 32 half + lane
@@ -1202,7 +1204,7 @@ cudaError_t sm_count(int* out) {
   return cudaSuccess;
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool OF32>
 cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   using L = TcLayout<DK, DV>;
   Tmaps tm;
@@ -1211,7 +1213,7 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
       !encode_rows(&tm.v, p.v, p.total_tokens, p.h_v, DV) ||
       !encode_out(&tm.o, p.out, p.total_tokens, p.h_v, DV, p.out_f32 != 0))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV>), (int)L::DYN_SMEM);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV, OF32>), (int)L::DYN_SMEM);
   if (e != cudaSuccess) return e;
   const long long units = (long long)p.num_seqs * p.h_v;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -1221,7 +1223,7 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const long long grid = units < sms ? units : sms;
-  gdn_tc_kernel<DK, DV><<<(unsigned)grid, kTcThreads, L::DYN_SMEM, stream>>>(p, tm);
+  gdn_tc_kernel<DK, DV, OF32><<<(unsigned)grid, kTcThreads, L::DYN_SMEM, stream>>>(p, tm);
   return cudaGetLastError();
 }
 
@@ -1230,10 +1232,14 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
 cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
   if (p.total_tokens <= 0) return launch_simt(p, stream);  // only empty sequences: state copy
   if (p.total_tokens > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (p.d_k == 128 && p.d_v == 128) return launch_tc_dk<128, 128>(p, stream);
-  if (p.d_k == 64 && p.d_v == 64) return launch_tc_dk<64, 64>(p, stream);
-  if (p.d_k == 128 && p.d_v == 64) return launch_tc_dk<128, 64>(p, stream);
-  return launch_tc_dk<64, 128>(p, stream);
+  const bool f = p.out_f32 != 0;
+  if (p.d_k == 128 && p.d_v == 128)
+    return f ? launch_tc_dk<128, 128, true>(p, stream) : launch_tc_dk<128, 128, false>(p, stream);
+  if (p.d_k == 64 && p.d_v == 64)
+    return f ? launch_tc_dk<64, 64, true>(p, stream) : launch_tc_dk<64, 64, false>(p, stream);
+  if (p.d_k == 128 && p.d_v == 64)
+    return f ? launch_tc_dk<128, 64, true>(p, stream) : launch_tc_dk<128, 64, false>(p, stream);
+  return f ? launch_tc_dk<64, 128, true>(p, stream) : launch_tc_dk<64, 128, false>(p, stream);
 }
 
 }  // namespace gdn
