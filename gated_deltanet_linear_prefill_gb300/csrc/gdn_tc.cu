@@ -317,6 +317,41 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint32_t m
   }
 }
 
+// The rows of a chunk whose gates span more than kMaxSpan in log-decay: the window
+// of m rows is halved until the span of {0, G_0 .. G_{m-1}} fits (one row always
+// does). s0 / s1: the inclusive prefix sums G of rows lane and lane + 32. Returns
+// (m as int bits, max and min of G over the chosen rows). Out of line: only
+// decays far outside the usual range get here.
+__device__ __noinline__ float3 span_fit(float s0, float s1, int m, int lane) {
+#pragma unroll 1
+  for (;;) {
+    m = (m + 1) >> 1;
+    float wmax = fmaxf(lane < m ? s0 : -3.0e38f, lane + 32 < m ? s1 : -3.0e38f);
+    float wmin = fminf(lane < m ? s0 : 3.0e38f, lane + 32 < m ? s1 : 3.0e38f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+      wmin = fminf(wmin, __shfl_xor_sync(0xffffffffu, wmin, o));
+    }
+    if (m <= 1 || fmaxf(wmax, 0.f) - fminf(wmin, 0.f) <= kMaxSpan) return make_float3(__int_as_float(m), wmax, wmin);
+  }
+}
+
+// Waits (bounded) until the K / Q loads of the last three chunks and the V loads
+// of the last two that the producer requested have landed, before the CTA exits.
+__device__ __noinline__ void drain_loads(uint32_t bars, int kq_issued, int v_issued, uint32_t misc) {
+#pragma unroll 1
+  for (int c = kq_issued - 3 < 0 ? 0 : kq_issued - 3; c < kq_issued; ++c) {
+    const uint32_t bar = bars + 8u * (uint32_t)(B_FULL0 + c % 3), par = (uint32_t)((c / 3) & 1);
+    if (!mbar_try_wait(bar, par)) wait_slow(bar, par, misc, kDrainWait);
+  }
+#pragma unroll 1
+  for (int c = v_issued - 2 < 0 ? 0 : v_issued - 2; c < v_issued; ++c) {
+    const uint32_t bar = bars + 8u * (uint32_t)(B_VFULL0 + (c & 1)), par = (uint32_t)((c >> 1) & 1);
+    if (!mbar_try_wait(bar, par)) wait_slow(bar, par, misc, kDrainWait);
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 // OF32: fp32 output (else bf16), a template parameter so that each kernel holds
 // only its own epilogue.
@@ -412,14 +447,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
       auto load_gates = [&](int64_t st) {
         const int64_t avail = len - st;
-        g0 = g1 = b0 = b1 = 0.f;
-        if (lane < avail) {
-          g0 = load_gate(p.g, (bos + st + lane) * p.h_v + h, p.gate_f32);
-          b0 = load_gate(p.beta, (bos + st + lane) * p.h_v + h, p.gate_f32);
-        }
-        if (lane + 32 < avail) {
-          g1 = load_gate(p.g, (bos + st + lane + 32) * p.h_v + h, p.gate_f32);
-          b1 = load_gate(p.beta, (bos + st + lane + 32) * p.h_v + h, p.gate_f32);
+        const int64_t i0 = (bos + st + lane) * p.h_v + h, i1 = i0 + 32 * (int64_t)p.h_v;
+        const bool in0 = lane < avail, in1 = lane + 32 < avail;
+        if (p.gate_f32) {
+          const float* gg = reinterpret_cast<const float*>(p.g);
+          const float* bb = reinterpret_cast<const float*>(p.beta);
+          g0 = in0 ? gg[i0] : 0.f;
+          b0 = in0 ? bb[i0] : 0.f;
+          g1 = in1 ? gg[i1] : 0.f;
+          b1 = in1 ? bb[i1] : 0.f;
+        } else {
+          const __nv_bfloat16* gg = reinterpret_cast<const __nv_bfloat16*>(p.g);
+          const __nv_bfloat16* bb = reinterpret_cast<const __nv_bfloat16*>(p.beta);
+          g0 = in0 ? __bfloat162float(gg[i0]) : 0.f;
+          b0 = in0 ? __bfloat162float(bb[i0]) : 0.f;
+          g1 = in1 ? __bfloat162float(gg[i1]) : 0.f;
+          b1 = in1 ? __bfloat162float(bb[i1]) : 0.f;
         }
       };
       load_gates(0);
@@ -434,25 +477,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane >= o) { s0 += u0; s1 += u1; }
         }
         s1 += __shfl_sync(0xffffffffu, s0, 31);
-        // rows of the chunk: the window, halved while the span of {0, G_0 .. G_{m-1}}
-        // passes kMaxSpan (only decays far outside the usual range get here)
+        // rows of the chunk: the window, halved (out of line, only for decays far outside
+        // the usual range) while the span of {0, G_0 .. G_{m-1}} passes kMaxSpan
         int m = mv;
-#pragma unroll 1
-        for (;;) {
-          float wmax = fmaxf(fmaxf(lane < m ? s0 : 0.f, lane + 32 < m ? s1 : 0.f), 0.f);
-          float wmin = fminf(fminf(lane < m ? s0 : 0.f, lane + 32 < m ? s1 : 0.f), 0.f);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-            wmin = fminf(wmin, __shfl_xor_sync(0xffffffffu, wmin, o));
-          }
-          if (wmax - wmin <= kMaxSpan || m <= 1) break;
-          m = (m + 1) >> 1;
-        }
-        // rows past m: no decay, no write
-        const float Gm = m > 0 ? __shfl_sync(0xffffffffu, (m - 1) < 32 ? s0 : s1, (m - 1) & 31) : 0.f;
-        if (lane >= m) { s0 = Gm; b0 = 0.f; }
-        if (lane + 32 >= m) { s1 = Gm; b1 = 0.f; }
         float gmax = fmaxf(lane < m ? s0 : -3.0e38f, lane + 32 < m ? s1 : -3.0e38f);
         float gmin = fminf(lane < m ? s0 : 3.0e38f, lane + 32 < m ? s1 : 3.0e38f);
 #pragma unroll
@@ -460,6 +487,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
           gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
         }
+        if (m > 1 && fmaxf(gmax, 0.f) - fminf(gmin, 0.f) > kMaxSpan) {
+          const float3 f = span_fit(s0, s1, m, lane);
+          m = __float_as_int(f.x);
+          gmax = f.y;
+          gmin = f.z;
+        }
+        // rows past m: no decay, no write
+        const float Gm = m > 0 ? __shfl_sync(0xffffffffu, (m - 1) < 32 ? s0 : s1, (m - 1) & 31) : 0.f;
+        if (lane >= m) { s0 = Gm; b0 = 0.f; }
+        if (lane + 32 >= m) { s1 = Gm; b1 = 0.f; }
         const float loglam = logmu + Gm;
         const bool eager = fabsf(loglam) > kMaxLogScale;
         const bool ulast = start + m >= len;
@@ -528,12 +565,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     // let every requested tile land before the CTA can exit (on the normal path
     // they were all consumed and these return at once)
-    if (lane == 0) {
-      for (int c = kq_issued - 3 < 0 ? 0 : kq_issued - 3; c < kq_issued; ++c)
-        wait(B_FULL0 + c % 3, (c / 3) & 1, kDrainWait);
-      for (int c = v_issued - 2 < 0 ? 0 : v_issued - 2; c < v_issued; ++c)
-        wait(B_VFULL0 + (c & 1), (c >> 1) & 1, kDrainWait);
-    }
+    if (lane == 0) drain_loads(sbase + L::BARS, kq_issued, v_issued, sbase + L::MISC);
   } else if (warp == 1) {
     // ================================================================ state-independent MMAs
     // [K;Q] K^T of chunk c+1 as soon as its tiles are in and WG-A has read chunk c's;
