@@ -91,6 +91,7 @@ enum {
   B_MFREE0, B_MFREE1, B_CSF0, B_CSF1, B_CSF2,
   B_DRAIN1, B_DRAIN2, kNumBars
 };
+static_assert(kNumBars <= 127, "barrier indices fit the seven bits of a wait-list entry");
 
 // Gate scalars the producer writes next to each K/Q slot (floats).
 constexpr int SC_G = 0;        // G_i (rows past m repeat G_{m-1})
@@ -414,6 +415,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t bar = sbase + L::BARS + 8u * (uint32_t)b;
     return mbar_try_wait(bar, parity) || wait_slow(bar, parity, sbase + L::MISC, site);
   };
+  // A group of waits through one call site: `list` holds one byte per barrier (index
+  // in the low seven bits, parity in the top bit), 0xff after the last; the order of
+  // the entries does not matter.
+  auto wait_all = [&](uint64_t list, uint32_t site) {
+#pragma unroll 1
+    for (; (list & 0xffu) != 0xffu; list >>= 8) {
+      const uint32_t e = (uint32_t)list & 0xffu;
+      const uint32_t bar = sbase + L::BARS + 8u * (e & 0x7fu);
+      if (!mbar_try_wait(bar, e >> 7) && !wait_slow(bar, e >> 7, sbase + L::MISC, site)) return false;
+    }
+    return true;
+  };
+  // list entry for barrier b at parity `parity`, prepended to `list`
+  auto with = [](uint64_t list, int b, uint32_t parity) {
+    return (list << 8) | (uint64_t)((uint32_t)b | ((parity & 1u) << 7));
+  };
+  constexpr uint64_t kNone = 0xffu;  // an empty list
 
   if (warp == 0) {
     // ================================================================ producer
@@ -592,14 +610,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int par = c & 1;
         const bool last = sc_int(slot_sc(c), SC_FLAGS) & F_SLAST;
         if (!last) {
-          if (!wait(B_FULL0 + (c + 1) % 3, ((c + 1) / 3) & 1, 2) || !wait(B_KQ_FREE, c & 1, 2)) break;
+          if (!wait_all(with(with(kNone, B_FULL0 + (c + 1) % 3, ((c + 1) / 3) & 1), B_KQ_FREE, c & 1), 2)) break;
           tc_fence_after();
           issue_kq(c + 1);
         }
         // R and the W' accumulator were read by WG-B for chunk c-1
-        if (!wait(B_T_READY0 + par, (c >> 1) & 1, 10) ||
-            (c >= 1 && (!wait(B_R_FREE, (c - 1) & 1, 10) || !wait(B_W_FREE, (c - 1) & 1, 10))))
-          break;
+        uint64_t wl = with(kNone, B_T_READY0 + par, (c >> 1) & 1);
+        if (c >= 1) wl = with(with(wl, B_R_FREE, (c - 1) & 1), B_W_FREE, (c - 1) & 1);
+        if (!wait_all(wl, 10)) break;
         tc_fence_after();
         const uint32_t kq = slot_kq(c), vv = slot_v(c);
         const uint32_t lbo_k = (L::NKA == 2) ? 16384u : (sbase + L::ZERO - kq);
@@ -633,8 +651,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
       for (int c = 0;; ++c) {
         const int par = c & 1;
-        if (!wait(B_P1_DONE0 + par, (c >> 1) & 1, 4) || !wait(B_WCONV0 + par, (c >> 1) & 1, 4) ||
-            !wait(B_U_DONE, c & 1, 4) || !wait(B_S_READY, c & 1, 4)) {
+        if (!wait_all(with(with(with(with(kNone, B_P1_DONE0 + par, (c >> 1) & 1), B_WCONV0 + par, (c >> 1) & 1),
+                                 B_U_DONE, c & 1), B_S_READY, c & 1), 4)) {
           break;
         }
         tc_fence_after();
@@ -732,13 +750,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
       for (int c = 0;; ++c) {
         const int par = c & 1;
-        bool ok = wait(B_FULL0 + c % 3, (c / 3) & 1, 8);
-        // M, W'^T / A and the chunk scalars of this parity were released by chunk c-2 / c-3
-        if (ok && c >= 2) ok = wait(B_MFREE0 + par, ((c >> 1) + 1) & 1, 8);
-        if (ok && c >= 2) ok = wait(B_WFREE0 + par, ((c >> 1) + 1) & 1, 8);
-        if (ok && c >= 3) ok = wait(B_CSF0 + c % 3, ((c / 3) + 1) & 1, 8);
-        if (ok) ok = wait(B_RQ0 + c % 3, (c / 3) & 1, 8);
-        if (ok) ok = wait(B_KQ_DONE, c & 1, 8);
+        // the chunk's tiles, q norms and [K;Q] K^T; M, W'^T / A and the chunk scalars of this
+        // parity released by chunk c-2 / c-3
+        uint64_t wl = with(with(with(kNone, B_FULL0 + c % 3, (c / 3) & 1), B_RQ0 + c % 3, (c / 3) & 1),
+                           B_KQ_DONE, c & 1);
+        if (c >= 2) wl = with(with(wl, B_MFREE0 + par, ((c >> 1) + 1) & 1), B_WFREE0 + par, ((c >> 1) + 1) & 1);
+        if (c >= 3) wl = with(wl, B_CSF0 + c % 3, ((c / 3) + 1) & 1);
+        bool ok = wait_all(wl, 8);
         if (named_bar_or(1, 256, !ok || *abort_flag)) break;
         tc_fence_after();
         const float* sc = slot_sc(c);
@@ -945,7 +963,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (c >= 0) {
         // ---- (U' diag(s/lambda))^T -> bf16 hi / lo A operands
         const ChunkScalars& cs = cscal[c % 3];
-        bool ok = wait(B_P1_DONE0 + (c & 1), (c >> 1) & 1, 12) && wait(B_UP_DONE, c & 1, 12);
+        bool ok = wait_all(with(with(kNone, B_P1_DONE0 + (c & 1), (c >> 1) & 1), B_UP_DONE, c & 1), 12);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
 #pragma unroll 1
@@ -980,8 +998,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---- S~ -> bf16 A operand for chunk c+1 (first applying its decay when eager)
         const int cn = c + 1;
         const float* sc = slot_sc(cn);
-        bool ok = wait(B_FULL0 + cn % 3, (cn / 3) & 1, 11);
-        if (ok && c >= 0) ok = wait(B_STATE_DONE, c & 1, 11);
+        uint64_t wl = with(kNone, B_FULL0 + cn % 3, (cn / 3) & 1);
+        if (c >= 0) wl = with(wl, B_STATE_DONE, c & 1);
+        bool ok = wait_all(wl, 11);
         if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
         tc_fence_after();
         if (sc_int(sc, SC_FLAGS) & F_UFIRST) {
