@@ -318,6 +318,19 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint32_t m
   }
 }
 
+// A group of bounded waits through one call: `list` holds one byte per barrier (its
+// index from `bars` in the low seven bits, the parity in the top bit), 0xff after the
+// last. False when a wait gave up (see wait_slow).
+__device__ __noinline__ bool wait_list(uint64_t list, uint32_t bars, uint32_t misc, uint32_t site) {
+#pragma unroll 1
+  for (; (list & 0xffu) != 0xffu; list >>= 8) {
+    const uint32_t e = (uint32_t)list & 0xffu;
+    const uint32_t bar = bars + 8u * (e & 0x7fu);
+    if (!mbar_try_wait(bar, e >> 7) && !wait_slow(bar, e >> 7, misc, site)) return false;
+  }
+  return true;
+}
+
 // The rows of a chunk whose gates span more than kMaxSpan in log-decay: the window
 // of m rows is halved until the span of {0, G_0 .. G_{m-1}} fits (one row always
 // does). s0 / s1: the inclusive prefix sums G of rows lane and lane + 32. Returns
@@ -415,17 +428,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t bar = sbase + L::BARS + 8u * (uint32_t)b;
     return mbar_try_wait(bar, parity) || wait_slow(bar, parity, sbase + L::MISC, site);
   };
-  // A group of waits through one call site: `list` holds one byte per barrier (index
-  // in the low seven bits, parity in the top bit), 0xff after the last; the order of
-  // the entries does not matter.
+  // a group of waits (see wait_list); the order of the entries does not matter
   auto wait_all = [&](uint64_t list, uint32_t site) {
-#pragma unroll 1
-    for (; (list & 0xffu) != 0xffu; list >>= 8) {
-      const uint32_t e = (uint32_t)list & 0xffu;
-      const uint32_t bar = sbase + L::BARS + 8u * (e & 0x7fu);
-      if (!mbar_try_wait(bar, e >> 7) && !wait_slow(bar, e >> 7, sbase + L::MISC, site)) return false;
-    }
-    return true;
+    return wait_list(list, sbase + L::BARS, sbase + L::MISC, site);
   };
   // list entry for barrier b at parity `parity`, prepended to `list`
   auto with = [](uint64_t list, int b, uint32_t parity) {
