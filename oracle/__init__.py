@@ -192,3 +192,32 @@ def tree(q, k, v, g, beta, cu_seqlens, parent, initial_state=None, state_index=N
         out[b:e] = o_p[rows.size - (e - b):]
         fs[n] = f_p[0]
     return out, fs
+
+
+def gated_rmsnorm(o, z, weight, eps: float = EPS):
+    """Gated RMSNorm of the prefill output, in fp64.
+
+    For every row x = o[..., :] (one token and value head, d_v entries) and its
+    gate row z[..., :]:
+
+        y_j = w_j * x_j / sqrt(mean_j(x_j^2) + eps) * silu(z_j),
+        silu(z) = z / (1 + e^{-z}).
+
+    The open-jev-fast README lists "gated RMSNorm" among the six fused
+    element-wise kernels of its Phase 2 (item 1) and puts it behind the Gated
+    DeltaNet core; its item 4 reports that fusing it into that kernel was
+    measured and rejected. The README gives no formula: this is the textbook
+    RMS normalisation over the value dimension, a per-channel weight w [d_v]
+    shared by the value heads, and a SiLU gate, with no rounding before the
+    end (the caller rounds y to its storage type).
+    o, z: [..., d_v]; weight: [d_v]. Returns y [..., d_v] float64.
+    """
+    x = np.asarray(o, dtype=np.float64)
+    zz = np.asarray(z, dtype=np.float64)
+    w = np.asarray(weight, dtype=np.float64)
+    if zz.shape != x.shape or w.shape != x.shape[-1:]:
+        raise ValueError("z must match o, and weight must have d_v entries")
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    with np.errstate(over="ignore"):
+        silu = zz / (1.0 + np.exp(-zz))
+    return w * (x / np.sqrt(ms + float(eps))) * silu
