@@ -604,6 +604,107 @@ def run_latency_bench(args):
     print(json.dumps(line))
 
 
+def run_norm_bench(args):
+    """The gated RMSNorm that follows the prefill, on the 74-prompt batch's
+    output shape [62,875, 32, 128]: bf16 o, z and y, fp32 weight. One step =
+    one gdn_gated_rmsnorm call. o and z (1.03 GB) exceed the 129 MB L2."""
+    import gated_deltanet_linear_prefill_gb300 as gdn
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --gated-rmsnorm needs a CUDA device")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    gdn.load_library()
+    w = workloads.config(CONFIG_INDEX)
+    T, H, D = w.total_tokens, w.h_v, w.d_v
+    o_h, _ = workloads.norm_inputs(T, H, D, seed=21)  # stands in for the prefill's output
+    z_h, wt_h = workloads.norm_inputs(T, H, D, seed=22)
+    o, z, wt = o_h.to(device), z_h.to(device), wt_h.to(device)
+    y = torch.empty_like(o)
+    rows = T * H
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        rc = gdn.gdn_gated_rmsnorm(o, z, wt, y, rows, D, gdn.GDN_BF16, gdn.GDN_BF16, 1e-6, stream)
+        if rc != gdn.GDN_OK:
+            raise gdn.GdnError(rc, "gdn_gated_rmsnorm")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(0, os.path.join(ROOT, "gpurun_out", "clocks_norm.csv"))
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(32):
+            step()
+        torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(times) / len(times)
+    B = rows * D * (2 + 2 + 2) + D * 4  # read o and z, write y, read the weights
+    hbm_peak, _, peak_kind = measured_peaks()
+    achieved = B / (ms / 1e3) / 1e9
+
+    # end to end: pinned host o and z in, y out, each step
+    e2e_line = None
+    if not args.no_e2e:
+        ho, hz = o_h.pin_memory(), z_h.pin_memory()
+        hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+        def e2e_step():
+            o.copy_(ho, non_blocking=True)
+            z.copy_(hz, non_blocking=True)
+            step()
+            hy.copy_(y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        n_e2e = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_line = {"value": T * n_e2e / (e0.elapsed_time(e1) / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": int(2 * rows * D * 2), "d2h_bytes_per_step": int(rows * D * 2)}
+    line = {
+        "metric": "gated RMSNorm tokens/s at 1 GB300 and % of HBM roofline", "value": T / (ms / 1e3),
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "gated_rmsnorm_cfg2_output", "tokens": T, "h_v": H, "d_v": D,
+                   "o_z_y": "bf16", "weight": "fp32", "eps": 1e-6,
+                   "l2_flush": "none needed: o and z (%.2f GB) exceed the 129 MB L2" % (2 * rows * D * 2 / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": B},
+        "e2e": e2e_line, "gpu_launches": args.steps, "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        idx = np.random.default_rng(0).choice(rows, min(rows, 400_000), replace=False)
+        o2, z2 = o_h.reshape(rows, D)[idx].float().numpy(), z_h.reshape(rows, D)[idx].float().numpy()
+        w2 = wt_h.numpy()
+        tot, n = 0.0, 0
+        while tot < 10.0 and n < 50:
+            t0 = time.perf_counter()
+            oracle.gated_rmsnorm(o2, z2, w2, 1e-6)
+            tot += time.perf_counter() - t0
+            n += 1
+        line["cpu_baseline"] = {"value": n * idx.size / H / tot, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{idx.size} random rows of {D} (token-heads), fp64 numpy, "
+                                          f"{n} passes in {tot:.1f} s; tokens = rows / {H}"}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -621,7 +722,12 @@ def main(argv=None):
                     help="time the config 3 prefix tree (one launch vs level by level vs full paths)")
     ap.add_argument("--latency", action="store_true",
                     help="per-call latency of configs 0, 1, short two-chunk paths and the config 3 tree")
+    ap.add_argument("--gated-rmsnorm", action="store_true",
+                    help="time the gated RMSNorm on the 74-prompt batch's output shape")
     args = ap.parse_args(argv)
+    if args.gated_rmsnorm:
+        run_norm_bench(args)
+        return
     if args.latency:
         run_latency_bench(args)
         return

@@ -24,6 +24,7 @@ __all__ = [
     "GdnError", "GdnDesc", "GDN_OK", "GDN_BF16", "GDN_F32", "GDN_FLAG_NO_L2NORM", "GDN_FLAG_SIMT",
     "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_get_device_status",
     "gdn_status_string", "make_desc", "prefill_varlen", "library_path", "load_library",
+    "gdn_gated_rmsnorm", "gated_rmsnorm",
 ]
 
 ABI_VERSION = 1
@@ -34,7 +35,8 @@ GDN_FLAG_SIMT = 0x2
 GDN_NOALLOC_MAX_SEQS = 16384  # include/gdn.h
 STATUS_NAMES = ["GDN_OK", "GDN_ERR_NULL", "GDN_ERR_SHAPE", "GDN_ERR_DTYPE", "GDN_ERR_ALIGN",
                 "GDN_ERR_SEQLENS", "GDN_ERR_STATE_INDEX", "GDN_ERR_ALIAS", "GDN_ERR_WORKSPACE",
-                "GDN_ERR_ARCH", "GDN_ERR_CUDA", "GDN_ERR_DEVICE_TIMEOUT", "GDN_ERR_PARENT"]
+                "GDN_ERR_ARCH", "GDN_ERR_CUDA", "GDN_ERR_DEVICE_TIMEOUT", "GDN_ERR_PARENT",
+                "GDN_ERR_VALUE"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -101,6 +103,9 @@ def load_library(build_if_missing: bool = True):
         lib.gdn_tree_workspace_bytes.restype = ctypes.c_size_t
         lib.gdn_prefill_tree.argtypes = [P] * 11 + [ctypes.POINTER(GdnDesc), P]
         lib.gdn_prefill_tree.restype = ctypes.c_int
+        lib.gdn_gated_rmsnorm.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_float, P]
+        lib.gdn_gated_rmsnorm.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.POINTER(GdnDesc), P]
         lib.gdn_get_device_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -283,3 +288,36 @@ def prefill_tree(q, k, v, g, beta, cu_seqlens, parent, *, initial_state=None, st
         if rc != GDN_OK:
             raise GdnError(rc, "device status")
     return out, final_state
+
+
+def gdn_gated_rmsnorm(o, z, weight, y, rows: int, d_v: int, x_dtype: int, z_dtype: int, eps: float,
+                      stream=None) -> int:
+    """The C entry point with tensors for pointers; returns the gdn_status code."""
+    lib = load_library()
+    return int(lib.gdn_gated_rmsnorm(_ptr(o), _ptr(z), _ptr(weight), _ptr(y), int(rows), int(d_v),
+                                     int(x_dtype), int(z_dtype), float(eps), _stream_handle(stream)))
+
+
+def gated_rmsnorm(o, z, weight, *, eps: float = 1e-6, out=None, stream=None) -> torch.Tensor:
+    """Gated RMSNorm of the prefill output (see include/gdn.h):
+    y = weight * o / sqrt(mean(o^2 over d_v) + eps) * silu(z), per row of d_v.
+
+    o [..., d_v] bf16/fp32 (e.g. prefill_varlen's [T, h_v, d_v] output); z the
+    same shape, bf16/fp32; weight [d_v] fp32. out (default: new, o's shape and
+    type) may be o itself. Raises GdnError on a non-OK status."""
+    if out is None:
+        out = torch.empty_like(o)
+    d_v = int(o.shape[-1])
+    rows = o.numel() // d_v if d_v else 0
+    if tuple(z.shape) != tuple(o.shape) or tuple(out.shape) != tuple(o.shape) or out.dtype != o.dtype:
+        raise ValueError("z and out must have o's shape (and out o's dtype)")
+    if tuple(weight.shape) != (d_v,) or weight.dtype != torch.float32:
+        raise ValueError("weight must be fp32 with d_v entries")
+    for t in (o, z, weight, out):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    rc = gdn_gated_rmsnorm(o, z, weight, out, rows, d_v, _dtype_code(o.dtype), _dtype_code(z.dtype), eps,
+                           stream)
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_gated_rmsnorm")
+    return out

@@ -219,6 +219,7 @@ extern "C" const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA runtime call failed";
     case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
     case GDN_ERR_PARENT: return "GDN_ERR_PARENT: a parent index outside [-1, n) (device check)";
+    case GDN_ERR_VALUE: return "GDN_ERR_VALUE: an argument outside its range";
   }
   return "unknown gdn_status";
 }
@@ -432,4 +433,27 @@ extern "C" gdn_status gdn_prefill_varlen_noalloc(const void* q, const void* k, c
   d.workspace_bytes = kNoallocBytes;
   return gdn_prefill_varlen(q, k, v, g, beta, cu_seqlens, initial_state, state_index, out,
                             final_state, &d, stream);
+}
+
+extern "C" gdn_status gdn_gated_rmsnorm(const void* o, const void* z, const float* weight, void* y,
+                                        int64_t rows, int32_t d_v, gdn_dtype x_dtype, gdn_dtype z_dtype,
+                                        float eps, void* stream) {
+  if (rows < 0 || (d_v != 64 && d_v != 128 && d_v != 256)) return GDN_ERR_SHAPE;
+  if ((x_dtype != GDN_BF16 && x_dtype != GDN_F32) || (z_dtype != GDN_BF16 && z_dtype != GDN_F32))
+    return GDN_ERR_DTYPE;
+  if (!(eps > 0.f) || !(eps < 3.0e38f)) return GDN_ERR_VALUE;
+  if (rows == 0) return GDN_OK;
+  if (!o || !z || !weight || !y) return GDN_ERR_NULL;
+  if (!aligned(o, 16) || !aligned(z, 16) || !aligned(weight, 16) || !aligned(y, 16)) return GDN_ERR_ALIGN;
+  const size_t xb = (size_t)rows * (size_t)d_v * (x_dtype == GDN_F32 ? 4 : 2);
+  const size_t zb = (size_t)rows * (size_t)d_v * (z_dtype == GDN_F32 ? 4 : 2);
+  // y may be o itself (each entry is read before the same thread writes it), not a
+  // shifted view of it, and may not overlap z or the weights
+  if (y != o && overlaps(y, xb, o, xb)) return GDN_ERR_ALIAS;
+  if (overlaps(y, xb, z, zb) || overlaps(y, xb, weight, (size_t)d_v * 4)) return GDN_ERR_ALIAS;
+  const gdn_status arch = check_arch();
+  if (arch != GDN_OK) return arch;
+  const cudaError_t e = launch_gated_rmsnorm(o, z, weight, y, rows, d_v, x_dtype == GDN_F32, z_dtype == GDN_F32,
+                                             eps, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -112,5 +112,9 @@ cudaError_t set_smem_once(const void* kernel, int bytes);
 cudaError_t launch_prep(const Params& p, cudaStream_t stream);
 cudaError_t launch_simt(const Params& p, cudaStream_t stream);
 cudaError_t launch_tc(const Params& p, cudaStream_t stream);
+// Gated RMSNorm over `rows` rows of d_v (64, 128 or 256) entries; o and y bf16 or
+// fp32 (x_f32), z bf16 or fp32 (z_f32), w fp32 [d_v]; nothing is launched for rows <= 0.
+cudaError_t launch_gated_rmsnorm(const void* o, const void* z, const float* w, void* y, int64_t rows, int d_v,
+                                 bool x_f32, bool z_f32, float eps, cudaStream_t stream);
 
 }  // namespace gdn

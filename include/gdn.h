@@ -68,7 +68,8 @@ typedef enum {
   GDN_ERR_ARCH = 9,           /* the current device is not sm_103 */
   GDN_ERR_CUDA = 10,          /* a CUDA runtime call failed (launch, query, copy) */
   GDN_ERR_DEVICE_TIMEOUT = 11, /* device: a bounded wait gave up */
-  GDN_ERR_PARENT = 12          /* device: a parent index outside [-1, n) (gdn_prefill_tree) */
+  GDN_ERR_PARENT = 12,         /* device: a parent index outside [-1, n) (gdn_prefill_tree) */
+  GDN_ERR_VALUE = 13           /* an argument outside its range (gdn_gated_rmsnorm: eps) */
 } gdn_status;
 
 /* Flags. */
@@ -233,6 +234,34 @@ gdn_status gdn_prefill_tree(const void* q, const void* k, const void* v, const v
  * the synchronisation or the read failed.
  */
 gdn_status gdn_get_device_status(const gdn_desc* desc, void* stream);
+
+/*
+ * Gated RMSNorm of the prefill output, one row per token and value head:
+ *
+ *     y[r, j] = weight[j] * o[r, j] / sqrt(mean_j o[r, j]^2 + eps) * silu(z[r, j]),
+ *     silu(z) = z / (1 + exp(-z)),
+ *
+ * with every step in fp32 and one rounding to y's type (so a row's sum of squares
+ * must stay inside fp32: entries up to about 1e18 in magnitude). The open-jev-fast README
+ * lists the gated RMSNorm among the six fused element-wise kernels of a layer
+ * (Phase 2 item 1) that follow the Gated DeltaNet core, and reports fusing it into
+ * that core as measured and rejected (item 4). It gives no formula; this is the
+ * textbook RMS normalisation over the d_v entries of a row with a per-channel
+ * weight shared by the value heads and a SiLU gate.
+ *
+ *  o, y    [rows, d_v] (rows = tokens x value heads, e.g. the [T, h_v, d_v] output
+ *          of gdn_prefill_varlen), storage type x_dtype (GDN_BF16 or GDN_F32)
+ *  z       [rows, d_v] gate, storage type z_dtype (GDN_BF16 or GDN_F32)
+ *  weight  [d_v] fp32
+ *  d_v     64, 128 or 256; rows >= 0 (0 launches nothing and returns GDN_OK
+ *          whatever the pointers); eps > 0 and finite, else GDN_ERR_VALUE
+ *
+ * Every pointer is caller-owned device memory, 16-byte aligned (GDN_ERR_ALIGN).
+ * y may be o itself (in place) but may not overlap o otherwise, nor z or weight
+ * (GDN_ERR_ALIAS). Asynchronous on `stream`; no allocation, no workspace.
+ */
+gdn_status gdn_gated_rmsnorm(const void* o, const void* z, const float* weight, void* y, int64_t rows,
+                             int32_t d_v, gdn_dtype x_dtype, gdn_dtype z_dtype, float eps, void* stream);
 
 /* A static, human-readable name for a status code. */
 const char* gdn_status_string(gdn_status s);

@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_prefill_varlen_noalloc",
         "gdn_tree_workspace_bytes", "gdn_prefill_tree", "gdn_get_device_status",
-        "gdn_status_string"])
+        "gdn_status_string", "gdn_gated_rmsnorm"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -199,3 +199,36 @@ def test_tree_host_checks():
 def test_valid_tree_call_without_a_device_reports_cuda_or_arch():
     d = base_desc(workspace_bytes=gdn.gdn_tree_workspace_bytes(base_desc()))
     assert call_tree(d) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
+
+
+def call_norm(o=FAKE, z=FAKE * 8, w=FAKE * 16, y=FAKE * 24, rows=1000, d_v=128, xd=gdn.GDN_BF16,
+              zd=gdn.GDN_BF16, eps=1e-6):
+    if torch.cuda.is_available():
+        pytest.skip("fake-pointer validation calls run only without a device")
+    lib = gdn.load_library()
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_gated_rmsnorm(P(o), P(z), P(w), P(y), rows, d_v, xd, zd, eps, None)
+
+
+def test_gated_rmsnorm_host_checks():
+    assert call_norm(rows=-1) == E["GDN_ERR_SHAPE"]
+    for d_v in (0, 32, 96, 512):
+        assert call_norm(d_v=d_v) == E["GDN_ERR_SHAPE"]
+    assert call_norm(xd=3) == E["GDN_ERR_DTYPE"]
+    assert call_norm(zd=-1) == E["GDN_ERR_DTYPE"]
+    for eps in (0.0, -1e-6, float("inf"), float("nan")):
+        assert call_norm(eps=eps) == E["GDN_ERR_VALUE"]
+    # no rows: nothing to do, whatever the pointers
+    assert call_norm(rows=0, o=None, z=None, w=None, y=None) == E["GDN_OK"]
+    assert call_norm(o=None) == E["GDN_ERR_NULL"]
+    assert call_norm(w=None) == E["GDN_ERR_NULL"]
+    assert call_norm(y=FAKE * 24 + 8) == E["GDN_ERR_ALIGN"]
+    assert call_norm(w=FAKE * 16 + 4) == E["GDN_ERR_ALIGN"]
+    # y may be o itself, but not a shifted view of it, nor overlap z or the weights
+    assert call_norm(y=FAKE) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
+    assert call_norm(y=FAKE + 256) == E["GDN_ERR_ALIAS"]
+    assert call_norm(y=FAKE * 8 + 1024) == E["GDN_ERR_ALIAS"]
+    assert call_norm(w=FAKE * 24 + 512) == E["GDN_ERR_ALIAS"]
+    # fp32 o / y are twice as long: y right after a bf16-sized o overlaps an fp32 o
+    assert call_norm(y=FAKE + 1000 * 128 * 2, xd=gdn.GDN_F32) == E["GDN_ERR_ALIAS"]
+    assert call_norm() in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])

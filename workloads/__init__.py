@@ -299,3 +299,14 @@ def subset_sequences(w: Workload, seqs) -> Workload:
         sub.initial_state = w.initial_state
         sub.state_index = torch.tensor(slot, dtype=torch.int32)
     return sub
+
+
+def norm_inputs(T: int, h_v: int, d_v: int, *, seed: int, z_dtype=torch.bfloat16):
+    """Seeded inputs of the gated RMSNorm that follows the prefill: the output
+    gate z [T, h_v, d_v] ~ N(0, 2^2) (it spans SiLU's curved range and both
+    tails), stored in z_dtype, and a per-channel weight [d_v] fp32 ~ U(0.5, 1.5)
+    (RMSNorm weights sit near their initial value 1)."""
+    rng = np.random.default_rng(seed)
+    z = torch.from_numpy(_normal(rng, (T, h_v, d_v), sd=2.0)).to(z_dtype)
+    w = torch.from_numpy(rng.uniform(0.5, 1.5, d_v).astype(np.float32))
+    return z, w
