@@ -221,3 +221,76 @@ def gated_rmsnorm(o, z, weight, eps: float = EPS):
     with np.errstate(over="ignore"):
         silu = zz / (1.0 + np.exp(-zz))
     return w * (x / np.sqrt(ms + float(eps))) * silu
+
+
+def causal_conv_silu(x, conv_w, cu_seqlens, conv_bias=None, conv_state=None, state_index=None):
+    """Causal depthwise convolution over each packed sequence, then SiLU, in fp64.
+
+    The first step of the Gated DeltaNet input prep in the open-jev-fast README
+    (Phase 2 item 1: "causal conv, SiLU, q/k/v split, ..."; reference [6] is the
+    causal-conv1d kernel). For channel c and row t of a sequence that starts at
+    row b, with a window of K taps (conv_w [C, K], tap K-1 on the current row):
+
+        y[t, c] = bias[c] + sum_{j=0}^{K-1} conv_w[c, j] * x[t - (K-1) + j, c]
+        u[t, c] = silu(y[t, c]) = y / (1 + e^{-y})
+
+    where a row before b reads the sequence's carried window: conv_state
+    [slots, K-1, C] holds the K-1 rows that precede the sequence (oldest first),
+    slot state_index[n] (n itself if state_index is None; a negative index, or no
+    conv_state, means zeros). The README's prefix-tree item replicates each
+    candidate's whole path so that its convolution window sees the prefix's last
+    rows; carrying the window into a continuation gives the same rows.
+    Returns (u [T, C], final_state [N, K-1, C]): the K-1 last input rows of each
+    sequence, oldest first, reaching into its carried window when the sequence
+    is shorter than K-1.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(conv_w, dtype=np.float64)
+    cu = _i64(cu_seqlens)
+    T, C = x.shape
+    K = w.shape[1]
+    if w.shape[0] != C:
+        raise ValueError("conv_w must be [C, K]")
+    bias = np.zeros(C) if conv_bias is None else np.asarray(conv_bias, dtype=np.float64)
+    N = cu.size - 1
+    u = np.zeros((T, C))
+    final = np.zeros((N, K - 1, C))
+    for n in range(N):
+        b, e = int(cu[n]), int(cu[n + 1])
+        slot = -1
+        if conv_state is not None:
+            slot = n if state_index is None else int(np.asarray(state_index)[n])
+        carried = (np.asarray(conv_state, dtype=np.float64)[slot] if slot >= 0
+                   else np.zeros((K - 1, C)))
+        seq = np.concatenate([carried, x[b:e]], axis=0)  # rows -(K-1) .. len-1
+        for i in range(e - b):
+            y = bias + np.sum(w.T * seq[i:i + K], axis=0)
+            with np.errstate(over="ignore"):
+                u[b + i] = y / (1.0 + np.exp(-y))
+        final[n] = seq[seq.shape[0] - (K - 1):]
+    return u, final
+
+
+def gate_params(a, b, A_log, dt_bias):
+    """The per-head gates of the gated delta rule from their projections, in fp64:
+
+        g[t, h]    = -exp(A_log[h]) * softplus(a[t, h] + dt_bias[h]),
+        beta[t, h] = 1 / (1 + e^{-b[t, h]}),   softplus(x) = ln(1 + e^x).
+
+    The open-jev-fast README lists gate parameters as the last step of its GDN
+    input prep (Phase 2 item 1) but gives no formula. This is the reading taken
+    from the model its reference [5] defines ("Gated Delta Networks: Improving
+    Mamba2 with Delta Rule"), which keeps Mamba2's decay: a per-head rate
+    exp(A_log) times a softplus step, so that alpha = e^g lies in (0, 1), and a
+    sigmoid for the writing strength beta. a, b: [T, H]; A_log, dt_bias: [H].
+    Returns (g, beta).
+    """
+    a = np.asarray(a, dtype=np.float64)
+    bb = np.asarray(b, dtype=np.float64)
+    A = np.asarray(A_log, dtype=np.float64)
+    dt = np.asarray(dt_bias, dtype=np.float64)
+    softplus = np.logaddexp(0.0, a + dt)  # ln(e^0 + e^x)
+    g = -np.exp(A) * softplus
+    with np.errstate(over="ignore"):
+        beta = 1.0 / (1.0 + np.exp(-bb))
+    return g, beta
