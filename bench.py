@@ -705,6 +705,123 @@ def run_norm_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prep_bench(args):
+    """The GDN input prep on the 74-prompt batch: x [62,875, 8,192] bf16 (q | k | v
+    channels of 16 x 128, 16 x 128, 32 x 128), 4 conv taps, gate projections
+    [62,875, 32]. One step = one gdn_input_prep call (the conv + SiLU kernel and
+    the gate kernel). x (1.03 GB) exceeds the 129 MB L2."""
+    import gated_deltanet_linear_prefill_gb300 as gdn
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --input-prep needs a CUDA device")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    gdn.load_library()
+    w = workloads.config(CONFIG_INDEX)
+    h_qk, d_k, h_v, d_v, K = w.h_qk, w.d_k, w.h_v, w.d_v, 4
+    inp_h = workloads.prep_inputs(w.lengths.tolist(), h_qk=h_qk, d_k=d_k, h_v=h_v, d_v=d_v, K=K, seed=31)
+    inp = {n: (None if t is None else t.to(device)) for n, t in inp_h.items()}
+    T, C, N = w.total_tokens, 2 * h_qk * d_k + h_v * d_v, w.num_seqs
+    q = torch.empty((T, h_qk, d_k), dtype=torch.bfloat16, device=device)
+    k = torch.empty_like(q)
+    v = torch.empty((T, h_v, d_v), dtype=torch.bfloat16, device=device)
+    g = torch.empty((T, h_v), dtype=torch.float32, device=device)
+    beta = torch.empty_like(g)
+    cs = torch.empty((N, K - 1, C), dtype=torch.bfloat16, device=device)
+    d = gdn.GdnPrepDesc()
+    d.num_seqs, d.total_tokens, d.h_qk, d.h_v, d.d_k, d.d_v = N, T, h_qk, h_v, d_k, d_v
+    d.conv_width, d.num_state_slots = K, 0
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        rc = gdn.gdn_input_prep(inp["x"], inp["conv_w"], None, inp["cu_seqlens"], None, None, inp["a"], inp["b"],
+                                inp["A_log"], inp["dt_bias"], q, k, v, g, beta, cs, d, stream)
+        if rc != gdn.GDN_OK:
+            raise gdn.GdnError(rc, "gdn_input_prep")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clocks = ClockSampler(0, os.path.join(ROOT, "gpurun_out", "clocks_prep.csv"))
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(32):
+            step()
+        torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a_, b_ in ev:
+        a_.record(stream)
+        step()
+        b_.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    ms = sum(a_.elapsed_time(b_) for a_, b_ in ev) / len(ev)
+    B = (T * C * 2 * 2 + T * h_v * (2 * 2 + 4 * 2) + C * K * 4 + 2 * h_v * 4 + N * (K - 1) * C * 2
+         + (N + 1) * 4)
+    hbm_peak, _, peak_kind = measured_peaks()
+    achieved = B / (ms / 1e3) / 1e9
+    e2e_line = None
+    if not args.no_e2e:
+        hx, ha, hb = inp_h["x"].pin_memory(), inp_h["a"].pin_memory(), inp_h["b"].pin_memory()
+        hq, hk, hv = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, v))
+        hg, hbeta = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (g, beta))
+
+        def e2e_step():
+            inp["x"].copy_(hx, non_blocking=True)
+            inp["a"].copy_(ha, non_blocking=True)
+            inp["b"].copy_(hb, non_blocking=True)
+            step()
+            for h_, t_ in ((hq, q), (hk, k), (hv, v), (hg, g), (hbeta, beta)):
+                h_.copy_(t_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        n_e2e = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_line = {"value": T * n_e2e / (e0.elapsed_time(e1) / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": int(T * C * 2 + 2 * T * h_v * 2),
+                    "d2h_bytes_per_step": int(T * C * 2 + 2 * T * h_v * 4)}
+    line = {
+        "metric": "GDN input prep tokens/s at 1 GB300 and % of HBM roofline", "value": T / (ms / 1e3),
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "input_prep_cfg2", "tokens": T, "num_seqs": N, "channels": C, "conv_width": K,
+                   "h_qk": h_qk, "h_v": h_v, "d_k": d_k, "d_v": d_v, "x_qkv": "bf16", "gates": "fp32",
+                   "l2_flush": "none needed: x (%.2f GB) exceeds the 129 MB L2" % (T * C * 2 / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": B,
+                     "note": "bytes and time of the whole call (conv + SiLU kernel and gate kernel)"},
+        "e2e": e2e_line, "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        lens = w.lengths
+        cu = inp_h["cu_seqlens"].numpy().astype(np.int64)
+        n = int(np.argsort(lens)[len(lens) // 2])  # a median-length sequence
+        b0, e0_ = int(cu[n]), int(cu[n + 1])
+        xs = inp_h["x"][b0:e0_].float().numpy()
+        wc = inp_h["conv_w"].numpy()
+        tot, passes = 0.0, 0
+        while tot < 10.0 and passes < 50:
+            t0 = time.perf_counter()
+            oracle.causal_conv_silu(xs, wc, np.array([0, e0_ - b0]))
+            oracle.gate_params(inp_h["a"][b0:e0_].float().numpy(), inp_h["b"][b0:e0_].float().numpy(),
+                               inp_h["A_log"].numpy(), inp_h["dt_bias"].numpy())
+            tot += time.perf_counter() - t0
+            passes += 1
+        line["cpu_baseline"] = {"value": passes * (e0_ - b0) / tot, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"sequence {n} ({e0_ - b0} tokens, all {C} channels and {h_v} gate "
+                                          f"heads), fp64 numpy, {passes} passes in {tot:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -724,7 +841,12 @@ def main(argv=None):
                     help="per-call latency of configs 0, 1, short two-chunk paths and the config 3 tree")
     ap.add_argument("--gated-rmsnorm", action="store_true",
                     help="time the gated RMSNorm on the 74-prompt batch's output shape")
+    ap.add_argument("--input-prep", action="store_true",
+                    help="time the GDN input prep (conv + SiLU + split, gates) on the 74-prompt batch")
     args = ap.parse_args(argv)
+    if args.input_prep:
+        run_prep_bench(args)
+        return
     if args.gated_rmsnorm:
         run_norm_bench(args)
         return

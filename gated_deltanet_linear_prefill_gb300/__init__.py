@@ -24,7 +24,7 @@ __all__ = [
     "GdnError", "GdnDesc", "GDN_OK", "GDN_BF16", "GDN_F32", "GDN_FLAG_NO_L2NORM", "GDN_FLAG_SIMT",
     "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_get_device_status",
     "gdn_status_string", "make_desc", "prefill_varlen", "library_path", "load_library",
-    "gdn_gated_rmsnorm", "gated_rmsnorm",
+    "gdn_gated_rmsnorm", "gated_rmsnorm", "GdnPrepDesc", "gdn_input_prep", "input_prep",
 ]
 
 ABI_VERSION = 1
@@ -72,6 +72,21 @@ class GdnDesc(ctypes.Structure):
     ]
 
 
+class GdnPrepDesc(ctypes.Structure):
+    """Mirror of gdn_prep_desc (include/gdn.h)."""
+
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32),
+        ("total_tokens", ctypes.c_int64),
+        ("h_qk", ctypes.c_int32),
+        ("h_v", ctypes.c_int32),
+        ("d_k", ctypes.c_int32),
+        ("d_v", ctypes.c_int32),
+        ("conv_width", ctypes.c_int32),
+        ("num_state_slots", ctypes.c_int32),
+    ]
+
+
 def library_path() -> str:
     return os.path.join(_HERE, "libgdn.so")
 
@@ -106,6 +121,8 @@ def load_library(build_if_missing: bool = True):
         lib.gdn_gated_rmsnorm.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_float, P]
         lib.gdn_gated_rmsnorm.restype = ctypes.c_int
+        lib.gdn_input_prep.argtypes = [P] * 16 + [ctypes.POINTER(GdnPrepDesc), P]
+        lib.gdn_input_prep.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.POINTER(GdnDesc), P]
         lib.gdn_get_device_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -321,3 +338,49 @@ def gated_rmsnorm(o, z, weight, *, eps: float = 1e-6, out=None, stream=None) -> 
     if rc != GDN_OK:
         raise GdnError(rc, "gdn_gated_rmsnorm")
     return out
+
+
+def gdn_input_prep(x, conv_w, conv_bias, cu_seqlens, conv_state_in, state_index, a, b, A_log, dt_bias,
+                   q, k, v, g, beta, conv_state_out, desc: GdnPrepDesc, stream=None) -> int:
+    """The C entry point with tensors for pointers; returns the gdn_status code."""
+    lib = load_library()
+    return int(lib.gdn_input_prep(_ptr(x), _ptr(conv_w), _ptr(conv_bias), _ptr(cu_seqlens), _ptr(conv_state_in),
+                                  _ptr(state_index), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(q),
+                                  _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(conv_state_out),
+                                  ctypes.byref(desc), _stream_handle(stream)))
+
+
+def input_prep(x, conv_w, cu_seqlens, *, h_qk: int, d_k: int, h_v: int, d_v: int, conv_bias=None,
+               conv_state=None, state_index=None, a=None, b=None, A_log=None, dt_bias=None,
+               want_conv_state: bool = True, stream=None):
+    """GDN input prep (see include/gdn.h): causal depthwise conv + SiLU over the
+    packed rows x [T, C] bf16 (C = 2 h_qk d_k + h_v d_v), split into q, k [T, h_qk,
+    d_k] and v [T, h_v, d_v] bf16, and, when a is given, the gates g, beta
+    [T, h_v] fp32. conv_w [C, K] fp32; conv_state [slots, K-1, C] bf16.
+    Returns (q, k, v, g, beta, conv_state_out [N, K-1, C] bf16 or None); g and
+    beta are None without a. Raises GdnError on a non-OK status."""
+    dev = x.device
+    T = int(x.shape[0])
+    N = int(cu_seqlens.numel()) - 1
+    K = int(conv_w.shape[1])
+    C = int(x.shape[1])
+    q = torch.empty((T, h_qk, d_k), dtype=torch.bfloat16, device=dev)
+    k = torch.empty((T, h_qk, d_k), dtype=torch.bfloat16, device=dev)
+    v = torch.empty((T, h_v, d_v), dtype=torch.bfloat16, device=dev)
+    g = beta = None
+    if a is not None:
+        g = torch.empty((T, h_v), dtype=torch.float32, device=dev)
+        beta = torch.empty((T, h_v), dtype=torch.float32, device=dev)
+    cs = torch.empty((N, K - 1, C), dtype=torch.bfloat16, device=dev) if want_conv_state else None
+    d = GdnPrepDesc()
+    d.num_seqs, d.total_tokens = N, T
+    d.h_qk, d.h_v, d.d_k, d.d_v = h_qk, h_v, d_k, d_v
+    d.conv_width = K
+    d.num_state_slots = 0 if conv_state is None else int(conv_state.shape[0])
+    if C != 2 * h_qk * d_k + h_v * d_v or tuple(conv_w.shape) != (C, K):
+        raise ValueError("x must have 2 h_qk d_k + h_v d_v channels and conv_w must be [C, K]")
+    rc = gdn_input_prep(x, conv_w, conv_bias, cu_seqlens, conv_state, state_index, a, b, A_log, dt_bias,
+                        q, k, v, g, beta, cs, d, stream)
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_input_prep")
+    return q, k, v, g, beta, cs

@@ -457,3 +457,88 @@ extern "C" gdn_status gdn_gated_rmsnorm(const void* o, const void* z, const floa
                                              eps, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
+
+extern "C" gdn_status gdn_input_prep(const void* x, const float* conv_w, const float* conv_bias,
+                                     const int32_t* cu_seqlens, const void* conv_state_in,
+                                     const int32_t* state_index, const void* a, const void* b,
+                                     const float* A_log, const float* dt_bias, void* q, void* k, void* v,
+                                     float* g, float* beta, void* conv_state_out, const gdn_prep_desc* desc,
+                                     void* stream) {
+  if (!desc) return GDN_ERR_NULL;
+  const gdn_prep_desc& d = *desc;
+  if (d.num_seqs < 0 || d.total_tokens < 0 || d.h_qk < 1 || d.h_v < 1 || d.d_k < 8 || d.d_v < 8 ||
+      d.d_k % 8 || d.d_v % 8 || d.conv_width < 2 || d.conv_width > 4 || d.num_state_slots < 0)
+    return GDN_ERR_SHAPE;
+  const int64_t Cq = (int64_t)d.h_qk * d.d_k, Cv = (int64_t)d.h_v * d.d_v, C = 2 * Cq + Cv;
+  if (C > (int64_t)1 << 24) return GDN_ERR_SHAPE;
+  if (d.num_seqs == 0 && d.total_tokens > 0) return GDN_ERR_SHAPE;  // rows but no sequence
+  if (conv_state_in && (d.num_state_slots == 0 || (!state_index && d.num_state_slots < d.num_seqs)))
+    return GDN_ERR_SHAPE;
+  if (d.num_seqs == 0) return GDN_OK;
+  const int64_t T = d.total_tokens;
+  const int K = d.conv_width;
+  if (!cu_seqlens) return GDN_ERR_NULL;
+  if (T > 0 && (!x || !conv_w || !q || !k || !v)) return GDN_ERR_NULL;
+  if (a && (!b || !A_log || !dt_bias || !g || !beta)) return GDN_ERR_NULL;
+  const void* v16[] = {x, q, k, v, conv_state_in, conv_state_out};
+  for (const void* ptr : v16)
+    if (!aligned(ptr, 16)) return GDN_ERR_ALIGN;
+  const void* v4[] = {conv_w, conv_bias, cu_seqlens, state_index, A_log, dt_bias, g, beta};
+  for (const void* ptr : v4)
+    if (!aligned(ptr, 4)) return GDN_ERR_ALIGN;
+  if (!aligned(a, 2) || !aligned(b, 2)) return GDN_ERR_ALIGN;
+  // outputs overlap no input and no other output
+  const bool gates = a != nullptr;
+  const size_t gb = gates ? (size_t)T * d.h_v * 4 : 0, ab = gates ? (size_t)T * d.h_v * 2 : 0;
+  struct R { const void* p; size_t n; };
+  const R ins[] = {{x, (size_t)T * C * 2},
+                   {conv_w, (size_t)C * K * 4},
+                   {conv_bias, conv_bias ? (size_t)C * 4 : 0},
+                   {cu_seqlens, (size_t)(d.num_seqs + 1) * 4},
+                   {conv_state_in, conv_state_in ? (size_t)d.num_state_slots * (K - 1) * C * 2 : 0},
+                   {state_index, state_index ? (size_t)d.num_seqs * 4 : 0},
+                   {a, ab},
+                   {b, ab},
+                   {A_log, gates ? (size_t)d.h_v * 4 : 0},
+                   {dt_bias, gates ? (size_t)d.h_v * 4 : 0}};
+  const R outs[] = {{q, (size_t)T * Cq * 2},
+                    {k, (size_t)T * Cq * 2},
+                    {v, (size_t)T * Cv * 2},
+                    {g, gb},
+                    {beta, gb},
+                    {conv_state_out, conv_state_out ? (size_t)d.num_seqs * (K - 1) * C * 2 : 0}};
+  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+    for (const R& r : ins)
+      if (overlaps(outs[i].p, outs[i].n, r.p, r.n)) return GDN_ERR_ALIAS;
+    for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+      if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return GDN_ERR_ALIAS;
+  }
+  const gdn_status arch = check_arch();
+  if (arch != GDN_OK) return arch;
+  InputPrepArgs p;
+  p.x = x;
+  p.conv_w = conv_w;
+  p.conv_bias = conv_bias;
+  p.cu_seqlens = cu_seqlens;
+  p.conv_state_in = conv_state_in;
+  p.state_index = state_index;
+  p.a = a;
+  p.b = b;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.g = g;
+  p.beta = beta;
+  p.conv_state_out = conv_state_out;
+  p.T = T;
+  p.N = d.num_seqs;
+  p.C = (int)C;
+  p.Cq = (int)Cq;
+  p.h_v = d.h_v;
+  p.K = K;
+  p.slots = conv_state_in ? d.num_state_slots : 0;
+  const cudaError_t e = launch_input_prep(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}

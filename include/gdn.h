@@ -263,6 +263,61 @@ gdn_status gdn_get_device_status(const gdn_desc* desc, void* stream);
 gdn_status gdn_gated_rmsnorm(const void* o, const void* z, const float* weight, void* y, int64_t rows,
                              int32_t d_v, gdn_dtype x_dtype, gdn_dtype z_dtype, float eps, void* stream);
 
+/* Sizes of a gdn_input_prep call. */
+typedef struct {
+  int32_t num_seqs;        /* N >= 0 packed sequences */
+  int64_t total_tokens;    /* T >= 0 rows; T must equal cu_seqlens[N]; N == 0 needs T == 0 */
+  int32_t h_qk, h_v;       /* q/k heads and value heads (>= 1) */
+  int32_t d_k, d_v;        /* head sizes, multiples of 8 */
+  int32_t conv_width;      /* K, the convolution's taps: 2, 3 or 4 */
+  int32_t num_state_slots; /* rows of conv_state_in (0 when it is NULL) */
+} gdn_prep_desc;
+
+/*
+ * GDN input prep: the steps in front of gdn_prefill_varlen that the open-jev-fast
+ * README fuses into one "Gated DeltaNet input prep" kernel (Phase 2 item 1):
+ * causal depthwise convolution and SiLU over the packed projection rows, the
+ * q / k / v split and the gate parameters. With C = 2 h_qk d_k + h_v d_v
+ * channels, for each sequence n (rows [cu[n], cu[n+1])) and channel c:
+ *
+ *     u[t, c] = silu(conv_bias[c] + sum_{j<K} conv_w[c, j] x[t - (K-1) + j, c])
+ *     q = u[:, 0 : h_qk d_k],  k = u[:, h_qk d_k : 2 h_qk d_k],  v = u[:, 2 h_qk d_k :]
+ *     g[t, h] = -exp(A_log[h]) ln(1 + exp(a[t, h] + dt_bias[h])),  beta = 1 / (1 + exp(-b))
+ *
+ * where rows before a sequence's first row read its carried window (so that a
+ * continuation sees the prefix's last rows, as the README's prefix tree requires).
+ * The README gives neither the channel layout nor the gate formula: channels are
+ * taken as contiguous q | k | v blocks, and the gates as the decay of "Gated Delta
+ * Networks: Improving Mamba2 with Delta Rule" (the README's reference [5]), which
+ * keeps Mamba2's form. Head expansion and the q/k L2 norm stay in the prefill
+ * (value head h reads q/k head h / (h_v / h_qk); gdn_prefill_varlen normalises).
+ *
+ *  x               [T, C] bf16, the packed projection rows
+ *  conv_w          [C, K] fp32 (tap K-1 multiplies the current row); conv_bias [C]
+ *                  fp32 or NULL
+ *  cu_seqlens      [N+1] int32 (device), as in gdn_prefill_varlen; inconsistent
+ *                  values give unspecified outputs but no access out of bounds
+ *  conv_state_in   [num_state_slots, K-1, C] bf16 or NULL: the K-1 rows that precede
+ *                  each sequence, oldest first, slot state_index[n] (NULL: slot n;
+ *                  a negative or out-of-range index, or NULL conv_state_in: zeros)
+ *  a, b            [T, h_v] bf16, the gate projections, or a = NULL to skip the gates
+ *                  (then b, A_log, dt_bias, g and beta are not used)
+ *  A_log, dt_bias  [h_v] fp32
+ *  q, k            [T, h_qk, d_k] bf16 out; v [T, h_v, d_v] bf16 out
+ *  g, beta         [T, h_v] fp32 out (ready for gdn_prefill_varlen with fp32 gates)
+ *  conv_state_out  [N, K-1, C] bf16 out or NULL: each sequence's last K-1 input rows
+ *                  (reaching into its carried window when it is shorter)
+ *
+ * Arithmetic in fp32; q, k and v are rounded to bf16 once, after SiLU. x, q, k, v
+ * and both conv states must be 16-byte aligned, the fp32 and int32 arrays 4-byte
+ * aligned (GDN_ERR_ALIGN); no output may overlap an input or another output
+ * (GDN_ERR_ALIAS). Asynchronous on `stream` (two launches); no allocation.
+ */
+gdn_status gdn_input_prep(const void* x, const float* conv_w, const float* conv_bias, const int32_t* cu_seqlens,
+                          const void* conv_state_in, const int32_t* state_index, const void* a, const void* b,
+                          const float* A_log, const float* dt_bias, void* q, void* k, void* v, float* g,
+                          float* beta, void* conv_state_out, const gdn_prep_desc* desc, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* gdn_status_string(gdn_status s);
 

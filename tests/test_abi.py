@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_prefill_varlen_noalloc",
         "gdn_tree_workspace_bytes", "gdn_prefill_tree", "gdn_get_device_status",
-        "gdn_status_string", "gdn_gated_rmsnorm"])
+        "gdn_status_string", "gdn_gated_rmsnorm", "gdn_input_prep"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -232,3 +232,60 @@ def test_gated_rmsnorm_host_checks():
     # fp32 o / y are twice as long: y right after a bf16-sized o overlaps an fp32 o
     assert call_norm(y=FAKE + 1000 * 128 * 2, xd=gdn.GDN_F32) == E["GDN_ERR_ALIAS"]
     assert call_norm() in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
+
+
+def test_prep_desc_layout_matches_header():
+    # int32, (pad), int64, int32 x6
+    assert ctypes.sizeof(gdn.GdnPrepDesc) == 40
+    assert gdn.GdnPrepDesc.total_tokens.offset == 8 and gdn.GdnPrepDesc.num_state_slots.offset == 36
+
+
+def prep_desc(**kw):
+    d = gdn.GdnPrepDesc()
+    d.num_seqs, d.total_tokens = 2, 100
+    d.h_qk, d.h_v, d.d_k, d.d_v = 16, 32, 128, 128
+    d.conv_width, d.num_state_slots = 4, 0
+    for k_, v_ in kw.items():
+        setattr(d, k_, v_)
+    return d
+
+
+def call_prep(desc, **ptrs):
+    if torch.cuda.is_available():
+        pytest.skip("fake-pointer validation calls run only without a device")
+    lib = gdn.load_library()
+    MB = 1 << 22  # 4 MiB apart: x (100 x 8192 bf16 = 1.6 MB) and every other array fit
+    base = dict(x=MB, w=2 * MB, bias=None, cu=3 * MB, sin=None, sidx=None, a=4 * MB, b=5 * MB,
+                A=6 * MB, dt=7 * MB, q=8 * MB, k=9 * MB, v=10 * MB, g=11 * MB, beta=12 * MB, sout=13 * MB)
+    base.update(ptrs)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    order = ["x", "w", "bias", "cu", "sin", "sidx", "a", "b", "A", "dt", "q", "k", "v", "g", "beta", "sout"]
+    return lib.gdn_input_prep(*[P(base[n]) for n in order],
+                              ctypes.byref(desc) if desc is not None else None, None)
+
+
+def test_input_prep_host_checks():
+    MB = 1 << 22
+    assert call_prep(None) == E["GDN_ERR_NULL"]
+    for f, val in [("num_seqs", -1), ("total_tokens", -1), ("h_qk", 0), ("d_k", 12), ("d_v", 0),
+                   ("conv_width", 1), ("conv_width", 5), ("num_state_slots", -2)]:
+        assert call_prep(prep_desc(**{f: val})) == E["GDN_ERR_SHAPE"], f
+    assert call_prep(prep_desc(num_seqs=0)) == E["GDN_ERR_SHAPE"]  # rows without a sequence
+    assert call_prep(prep_desc(num_seqs=0, total_tokens=0), x=None, cu=None) == E["GDN_OK"]
+    # a carried window needs slots (one per sequence without state_index)
+    assert call_prep(prep_desc(), sin=14 * MB) == E["GDN_ERR_SHAPE"]
+    assert call_prep(prep_desc(num_state_slots=1), sin=14 * MB) == E["GDN_ERR_SHAPE"]
+    assert call_prep(prep_desc(), x=None) == E["GDN_ERR_NULL"]
+    assert call_prep(prep_desc(), cu=None) == E["GDN_ERR_NULL"]
+    assert call_prep(prep_desc(), v=None) == E["GDN_ERR_NULL"]
+    assert call_prep(prep_desc(), beta=None) == E["GDN_ERR_NULL"]  # gates asked for (a given)
+    assert call_prep(prep_desc(), x=MB + 8) == E["GDN_ERR_ALIGN"]
+    assert call_prep(prep_desc(), sout=13 * MB + 4) == E["GDN_ERR_ALIGN"]
+    assert call_prep(prep_desc(), g=11 * MB + 2) == E["GDN_ERR_ALIGN"]
+    assert call_prep(prep_desc(), a=4 * MB + 1) == E["GDN_ERR_ALIGN"]
+    assert call_prep(prep_desc(), q=MB + 4096) == E["GDN_ERR_ALIAS"]     # q over x
+    assert call_prep(prep_desc(), v=9 * MB + 1024) == E["GDN_ERR_ALIAS"]  # v over k
+    assert call_prep(prep_desc(), g=5 * MB) == E["GDN_ERR_ALIAS"]         # g over b
+    # without gates their pointers are ignored (even overlapping ones)
+    assert call_prep(prep_desc(), a=None, g=MB, beta=MB) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
+    assert call_prep(prep_desc()) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])

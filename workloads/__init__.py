@@ -310,3 +310,32 @@ def norm_inputs(T: int, h_v: int, d_v: int, *, seed: int, z_dtype=torch.bfloat16
     z = torch.from_numpy(_normal(rng, (T, h_v, d_v), sd=2.0)).to(z_dtype)
     w = torch.from_numpy(rng.uniform(0.5, 1.5, d_v).astype(np.float32))
     return z, w
+
+
+def prep_inputs(lengths, *, h_qk: int, d_k: int, h_v: int, d_v: int, K: int = 4, seed: int,
+                slots: int = 0, bias: bool = False):
+    """Seeded inputs of the GDN input prep: the packed projection rows x [T, C]
+    bf16 ~ N(0, 1) (C = 2 h_qk d_k + h_v d_v); depthwise conv taps [C, K] fp32 ~
+    U(-1/sqrt(K), 1/sqrt(K)) (the fan-in scale of a K-tap filter) and, if asked,
+    a bias [C] ~ U(-0.1, 0.1); the gate projections a, b [T, h_v] bf16 ~ N(0, 1);
+    A_log = ln A with A ~ U(1, 16) and dt_bias = ln(e^dt - 1) with dt
+    log-uniform in [1e-3, 1e-1] (Mamba2's initial ranges, so that the gates give
+    decays alpha of about 0.6 to 1); with slots > 0, carried windows [slots, K-1,
+    C] bf16 ~ N(0, 1). Returns a dict of CPU tensors and cu_seqlens."""
+    rng = np.random.default_rng(seed)
+    T = int(sum(lengths))
+    C = 2 * h_qk * d_k + h_v * d_v
+    bound = 1.0 / np.sqrt(K)
+    dt = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), h_v))
+    out = {
+        "x": torch.from_numpy(_normal(rng, (T, C))).to(torch.bfloat16),
+        "conv_w": torch.from_numpy(rng.uniform(-bound, bound, (C, K)).astype(np.float32)),
+        "conv_bias": (torch.from_numpy(rng.uniform(-0.1, 0.1, C).astype(np.float32)) if bias else None),
+        "a": torch.from_numpy(_normal(rng, (T, h_v))).to(torch.bfloat16),
+        "b": torch.from_numpy(_normal(rng, (T, h_v))).to(torch.bfloat16),
+        "A_log": torch.from_numpy(np.log(rng.uniform(1.0, 16.0, h_v)).astype(np.float32)),
+        "dt_bias": torch.from_numpy(np.log(np.expm1(dt)).astype(np.float32)),
+        "conv_state": (torch.from_numpy(_normal(rng, (slots, K - 1, C))).to(torch.bfloat16) if slots else None),
+        "cu_seqlens": _cu(lengths),
+    }
+    return out
