@@ -160,6 +160,25 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
   return cudaSuccess;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+cudaError_t device_sm_count(int* out) {
+  static std::mutex mu;
+  static int cached[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cached[dev] = n > 0 ? n : 1;
+  }
+  *out = cached[dev];
+  return cudaSuccess;
+}
+
 // ---------------------------------------------------------------- host checks
 
 static bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
@@ -480,10 +499,10 @@ extern "C" gdn_status gdn_input_prep(const void* x, const float* conv_w, const f
   if (!cu_seqlens) return GDN_ERR_NULL;
   if (T > 0 && (!x || !conv_w || !q || !k || !v)) return GDN_ERR_NULL;
   if (a && (!b || !A_log || !dt_bias || !g || !beta)) return GDN_ERR_NULL;
-  const void* v16[] = {x, q, k, v, conv_state_in, conv_state_out};
+  const void* v16[] = {x, conv_w, q, k, v, conv_state_in, conv_state_out};
   for (const void* ptr : v16)
     if (!aligned(ptr, 16)) return GDN_ERR_ALIGN;
-  const void* v4[] = {conv_w, conv_bias, cu_seqlens, state_index, A_log, dt_bias, g, beta};
+  const void* v4[] = {conv_bias, cu_seqlens, state_index, A_log, dt_bias, g, beta};
   for (const void* ptr : v4)
     if (!aligned(ptr, 4)) return GDN_ERR_ALIGN;
   if (!aligned(a, 2) || !aligned(b, 2)) return GDN_ERR_ALIGN;

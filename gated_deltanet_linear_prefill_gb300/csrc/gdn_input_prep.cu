@@ -13,11 +13,11 @@
 // before the values are rounded).
 //
 // Both kernels are bound by HBM. The convolution gives each thread 8 consecutive
-// channels (one 16-byte bf16 vector) over a run of kRows rows: the window of the
-// K-1 previous rows stays in registers, rows are loaded kBatch at a time so that
-// several loads are in flight, and a warp's loads and stores cover 512 contiguous
-// bytes of a row. A run that starts inside a sequence re-reads its K-1 halo rows
-// (3 of 32 rows for K = 4).
+// channels (one 16-byte bf16 vector) over a run of kRows rows: partial sums of the
+// open outputs stay in registers, rows are loaded kBatch at a time so that several
+// loads are in flight, and a warp's loads and stores cover 512 contiguous bytes of
+// a row. A run that starts inside a sequence re-reads its K-1 halo rows (3 of 128
+// rows for K = 4). Consecutive blocks take the channel blocks of one run.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -27,18 +27,10 @@ namespace gdn {
 namespace {
 
 constexpr int kConvThreads = 128;
-constexpr int kRows = 32;   // rows per thread
+constexpr int kRows = 128;   // rows per thread
 constexpr int kBatch = 8;   // rows loaded at once
+constexpr int kConvBlocks = 4;  // resident blocks per SM the register budget allows (<= 128 registers)
 constexpr int kAuxThreads = 256;
-
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
 
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   uint32_t w[4];
@@ -87,23 +79,34 @@ struct PrepArgs {
   int N, C, Cq, h_v, slots;
 };
 
-// the carried window's row r (0 = oldest) of sequence n, 8 channels from c8 * 8
-__device__ __forceinline__ void carried_row(const PrepArgs& p, int K, int n, int r, int c8, float (&f)[8]) {
+// the carried window's row r (0 = oldest) of sequence n, 8 channels from c8 * 8,
+// as loaded (packed bf16)
+__device__ __forceinline__ uint4 carried_row(const PrepArgs& p, int K, int n, int r, int c8) {
   int64_t slot = -1;
   if (p.state_in) {
     slot = p.state_index ? (int64_t)p.state_index[n] : (int64_t)n;
     if (slot >= p.slots) slot = -1;
   }
-  if (slot < 0) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = 0.f;
-    return;
-  }
-  unpack8(__ldg(reinterpret_cast<const uint4*>(p.state_in + ((size_t)slot * (K - 1) + r) * p.C) + c8), f);
+  if (slot < 0) return make_uint4(0u, 0u, 0u, 0u);
+  return __ldg(reinterpret_cast<const uint4*>(p.state_in + ((size_t)slot * (K - 1) + r) * p.C) + c8);
 }
 
+// x row r or, before the sequence's first row bos, row r - bos + (K-1) of its
+// carried window (as loaded, packed bf16)
 template <int K>
-__global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(PrepArgs p) {
+__device__ __forceinline__ uint4 row_or_carried(const PrepArgs& p, int64_t r, int64_t bos, int n, int c8) {
+  if (r >= bos) return __ldcs(reinterpret_cast<const uint4*>(p.x + r * p.C) + c8);
+  return carried_row(p, K, n, (K - 1) - (int)(bos - r), c8);
+}
+
+// The convolution runs as a scatter: when row t arrives (unpacked once) it completes
+// output t and adds its term to the K-2 outputs still open after it, whose partial
+// sums acc[0..K-2] (bias first, then the taps in order) stay in registers as channel
+// pairs for the packed fp32 multiply-add. Starting a run (or a sequence) feeds the
+// K-1 rows before it through the same update without emitting anything. A
+// sequence's final window is read again at its last row (once per sequence).
+template <int K, bool BIAS>
+__global__ void __launch_bounds__(kConvThreads, kConvBlocks) conv_silu_kernel(PrepArgs p) {
   const int nvec = p.C / 8;
   const int cblocks = (nvec + kConvThreads - 1) / kConvThreads;
   const int c8 = (int)(blockIdx.x % cblocks) * kConvThreads + threadIdx.x;
@@ -112,12 +115,25 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(PrepArgs p) {
   const int64_t t1 = t0 + kRows < p.T ? t0 + kRows : p.T;
   const int c = 8 * c8;
 
-  float wt[K][8], bs[8];
+  float2 wt[K][4], bs[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
+  for (int e = 0; e < 4; ++e) {
+    float a_[K], b_[K];
+    if constexpr (K == 4) {
+      const float4 wa = __ldg(reinterpret_cast<const float4*>(p.w + (size_t)(c + 2 * e) * 4));
+      const float4 wb = __ldg(reinterpret_cast<const float4*>(p.w + (size_t)(c + 2 * e + 1) * 4));
+      a_[0] = wa.x; a_[1] = wa.y; a_[2] = wa.z; a_[3] = wa.w;
+      b_[0] = wb.x; b_[1] = wb.y; b_[2] = wb.z; b_[3] = wb.w;
+    } else {
 #pragma unroll
-    for (int j = 0; j < K; ++j) wt[j][e] = __ldg(p.w + (size_t)(c + e) * K + j);
-    bs[e] = p.bias ? __ldg(p.bias + c + e) : 0.f;
+      for (int j = 0; j < K; ++j) {
+        a_[j] = __ldg(p.w + (size_t)(c + 2 * e) * K + j);
+        b_[j] = __ldg(p.w + (size_t)(c + 2 * e + 1) * K + j);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j) wt[j][e] = make_float2(a_[j], b_[j]);
+    bs[e] = BIAS ? make_float2(__ldg(p.bias + c + 2 * e), __ldg(p.bias + c + 2 * e + 1)) : make_float2(0.f, 0.f);
   }
   // where this thread's outputs go: q, k or v, and the channel offset inside it
   __nv_bfloat16* dst;
@@ -126,21 +142,36 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(PrepArgs p) {
   else if (c < 2 * p.Cq) { dst = p.k; ldd = p.Cq; cd = c - p.Cq; }
   else { dst = p.v; ldd = p.C - 2 * p.Cq; cd = c - 2 * p.Cq; }
 
+  float2 acc[K - 1][4];
+  // row xr enters: returns nothing, completes output (acc[0] + w_{K-1} x) into `out`
+  auto feed = [&](const uint4& xr, float2 (&out)[4]) {
+    const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 xv = make_float2(__uint_as_float(xw[e] << 16), __uint_as_float(xw[e] & 0xffff0000u));
+      out[e] = __ffma2_rn(wt[K - 1][e], xv, acc[0][e]);
+#pragma unroll
+      for (int j = 0; j < K - 2; ++j) acc[j][e] = __ffma2_rn(wt[K - 2 - j][e], xv, acc[j + 1][e]);
+      acc[K - 2][e] = __ffma2_rn(wt[0][e], xv, bs[e]);
+    }
+  };
+  // the K-1 rows before row t of sequence n (which starts at bos) prime the sums
+  auto prime = [&](int64_t t, int64_t bos, int n) {
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][e] = bs[e];
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) {
+      float2 unused[4];
+      feed(row_or_carried<K>(p, t - (K - 1) + j, bos, n, c8), unused);
+    }
+  };
+
   int n = seq_of(p.cu, p.N, t0);
   int64_t bos = p.cu[n] > 0 ? (int64_t)p.cu[n] : 0;
   int64_t eos = p.cu[n + 1];
-  // the window: rows t0-(K-1) .. t0-1, from x inside the sequence, else carried
-  float win[K - 1][8];
-#pragma unroll
-  for (int j = 0; j < K - 1; ++j) {
-    const int64_t r = t0 - (K - 1) + j;
-    if (r >= bos && r >= 0) unpack8(__ldcs(reinterpret_cast<const uint4*>(p.x + r * p.C) + c8), win[j]);
-    else if (bos - r <= K - 1) carried_row(p, K, n, (K - 1) - (int)(bos - r), c8, win[j]);
-    else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) win[j][e] = 0.f;
-    }
-  }
+  prime(t0, bos > t0 ? t0 : bos, n);
 #pragma unroll 1
   for (int64_t tb = t0; tb < t1; tb += kBatch) {
     uint4 raw[kBatch];
@@ -155,30 +186,22 @@ __global__ void __launch_bounds__(kConvThreads) conv_silu_kernel(PrepArgs p) {
         while (n + 1 < p.N && (int64_t)p.cu[n + 1] <= t) ++n;
         bos = t;
         eos = p.cu[n + 1];
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j) carried_row(p, K, n, j, c8, win[j]);
+        prime(t, bos, n);
       }
-      float xt[8], out[8];
-      unpack8(raw[i], xt);
+      float2 y[4];
+      feed(raw[i], y);
+      float out[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float y = bs[e];
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j) y = fmaf(wt[j][e], win[j][e], y);
-        y = fmaf(wt[K - 1][e], xt[e], y);
-        out[e] = silu(y);
+      for (int e = 0; e < 4; ++e) {
+        out[2 * e] = silu(y[e].x);
+        out[2 * e + 1] = silu(y[e].y);
       }
       __stcs(reinterpret_cast<uint4*>(dst + t * ldd + cd), pack8(out));
-#pragma unroll
-      for (int j = 0; j < K - 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) win[K - 2][e] = xt[e];
       if (t == eos - 1 && p.state_out) {  // the sequence's last row: its final window
 #pragma unroll
         for (int j = 0; j < K - 1; ++j)
-          *(reinterpret_cast<uint4*>(p.state_out + ((size_t)n * (K - 1) + j) * p.C) + c8) = pack8(win[j]);
+          *(reinterpret_cast<uint4*>(p.state_out + ((size_t)n * (K - 1) + j) * p.C) + c8) =
+              row_or_carried<K>(p, t - (K - 2) + j, bos, n, c8);
       }
     }
   }
@@ -206,11 +229,8 @@ __global__ void __launch_bounds__(kAuxThreads) gates_kernel(PrepArgs p) {
     for (int64_t i = id0; i < total; i += stride) {
       const int n = (int)(i / nvec), c8 = (int)(i % nvec);
       if (p.cu[n + 1] != p.cu[n]) continue;
-      for (int j = 0; j < K - 1; ++j) {
-        float f[8];
-        carried_row(p, K, n, j, c8, f);
-        *(reinterpret_cast<uint4*>(p.state_out + ((size_t)n * (K - 1) + j) * p.C) + c8) = pack8(f);
-      }
+      for (int j = 0; j < K - 1; ++j)
+        *(reinterpret_cast<uint4*>(p.state_out + ((size_t)n * (K - 1) + j) * p.C) + c8) = carried_row(p, K, n, j, c8);
     }
   }
 }
@@ -221,7 +241,10 @@ cudaError_t launch_k(const PrepArgs& p, cudaStream_t stream) {
   const int64_t cblocks = (nvec + kConvThreads - 1) / kConvThreads;
   const int64_t tiles = (p.T + kRows - 1) / kRows;
   if (tiles > 0) {
-    conv_silu_kernel<K><<<(unsigned)(tiles * cblocks), kConvThreads, 0, stream>>>(p);
+    if (p.bias)
+      conv_silu_kernel<K, true><<<(unsigned)(tiles * cblocks), kConvThreads, 0, stream>>>(p);
+    else
+      conv_silu_kernel<K, false><<<(unsigned)(tiles * cblocks), kConvThreads, 0, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -108,6 +108,9 @@ __device__ __forceinline__ int64_t state_slot(const Params& p, int n) {
 // that a launch made during stream capture issues no attribute calls.
 cudaError_t set_smem_once(const void* kernel, int bytes);
 
+// Streaming multiprocessors of the current device (cached per device).
+cudaError_t device_sm_count(int* out);
+
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_prep(const Params& p, cudaStream_t stream);
 cudaError_t launch_simt(const Params& p, cudaStream_t stream);

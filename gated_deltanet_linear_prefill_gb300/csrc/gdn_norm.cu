@@ -136,25 +136,24 @@ template <typename TX, typename TZ, int DV>
 cudaError_t launch_dv(const void* o, const void* z, const float* w, void* y, int64_t rows, float eps,
                       cudaStream_t stream) {
   auto kernel = gated_rmsnorm_kernel<TX, TZ, DV>;
-  // SMs and resident blocks per SM of this instantiation, queried once per device
+  // resident blocks per SM of this instantiation, queried once per device
   static std::mutex mu;
-  static int per_sm[64], sms[64];
-  int dev = 0;
+  static int per_sm[64];
+  int dev = 0, cap_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int cap_sm = 0, cap_blocks = 0;
+  e = device_sm_count(&cap_sm);
+  if (e != cudaSuccess) return e;
+  int cap_blocks = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (sms[dev] == 0) {
-      int n = 0, b = 0;
-      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kNormThreads, 0);
+    if (per_sm[dev] == 0) {
+      int b = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kNormThreads, 0);
       if (e != cudaSuccess) return e;
-      sms[dev] = n > 0 ? n : 1;
       per_sm[dev] = b > 0 ? b : 1;
     }
-    cap_sm = sms[dev];
     cap_blocks = per_sm[dev];
   }
   constexpr int RPW = 32 / (DV / 8);

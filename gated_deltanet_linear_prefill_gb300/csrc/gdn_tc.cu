@@ -1241,24 +1241,6 @@ bool encode_out(CUtensorMap* m, void* base, int64_t T, int H, int D, bool f32) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Streaming multiprocessors of the current device (cached per device).
-cudaError_t sm_count(int* out) {
-  static std::mutex mu;
-  static int cached[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cached[dev] == 0) {
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    cached[dev] = n > 0 ? n : 1;
-  }
-  *out = cached[dev];
-  return cudaSuccess;
-}
 
 template <int DK, int DV, bool OF32>
 cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
@@ -1276,7 +1258,7 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   // one resident CTA per SM (the kernel's shared memory and TMEM fill an SM), each
   // taking units until the work list is exhausted
   int sms = 0;
-  e = sm_count(&sms);
+  e = device_sm_count(&sms);
   if (e != cudaSuccess) return e;
   const long long grid = units < sms ? units : sms;
   gdn_tc_kernel<DK, DV, OF32><<<(unsigned)grid, kTcThreads, L::DYN_SMEM, stream>>>(p, tm);

@@ -308,9 +308,9 @@ typedef struct {
  *  conv_state_out  [N, K-1, C] bf16 out or NULL: each sequence's last K-1 input rows
  *                  (reaching into its carried window when it is shorter)
  *
- * Arithmetic in fp32; q, k and v are rounded to bf16 once, after SiLU. x, q, k, v
- * and both conv states must be 16-byte aligned, the fp32 and int32 arrays 4-byte
- * aligned (GDN_ERR_ALIGN); no output may overlap an input or another output
+ * Arithmetic in fp32; q, k and v are rounded to bf16 once, after SiLU. x, conv_w,
+ * q, k, v and both conv states must be 16-byte aligned, the other fp32 and int32
+ * arrays 4-byte aligned (GDN_ERR_ALIGN); no output may overlap an input or another output
  * (GDN_ERR_ALIAS). Asynchronous on `stream` (two launches); no allocation.
  */
 gdn_status gdn_input_prep(const void* x, const float* conv_w, const float* conv_bias, const int32_t* cu_seqlens,

@@ -282,6 +282,7 @@ def test_input_prep_host_checks():
     assert call_prep(prep_desc(), x=MB + 8) == E["GDN_ERR_ALIGN"]
     assert call_prep(prep_desc(), sout=13 * MB + 4) == E["GDN_ERR_ALIGN"]
     assert call_prep(prep_desc(), g=11 * MB + 2) == E["GDN_ERR_ALIGN"]
+    assert call_prep(prep_desc(), w=2 * MB + 4) == E["GDN_ERR_ALIGN"]
     assert call_prep(prep_desc(), a=4 * MB + 1) == E["GDN_ERR_ALIGN"]
     assert call_prep(prep_desc(), q=MB + 4096) == E["GDN_ERR_ALIAS"]     # q over x
     assert call_prep(prep_desc(), v=9 * MB + 1024) == E["GDN_ERR_ALIAS"]  # v over k
