@@ -89,19 +89,30 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def profiled_traffic(kernel_name: str, workload_name: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel source (the summary records the source hash)."""
+# the sources each profiled kernel is compiled from: a committed ncu summary holds
+# for the current build only if their hash matches the one it records
+KERNEL_SOURCES = {
+    "gdn_tc_kernel": ["gdn_tc.cu", "tc_ptx.cuh", "gdn_internal.cuh"],
+    "gated_rmsnorm_kernel": ["gdn_norm.cu"],
+    "conv_silu_kernel": ["gdn_input_prep.cu"],
+}
+
+
+def kernel_source_hash(kernel_name: str) -> str:
     import hashlib
     src = os.path.join(ROOT, "gated_deltanet_linear_prefill_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(src)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(src, name), "rb") as f:
-                h.update(f.read())
-    digest = h.hexdigest()[:16]
+    for name in KERNEL_SOURCES[kernel_name]:
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_name: str, workload_name: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel source (the summary records the sources' hash)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_name}_{workload_name}.md")
-    if not os.path.exists(path):
+    if kernel_name not in KERNEL_SOURCES or not os.path.exists(path):
         return None
     vals = {}
     with open(path) as f:
@@ -109,7 +120,7 @@ def profiled_traffic(kernel_name: str, workload_name: str):
             if line.startswith("- ") and ":" in line:
                 k_, v_ = line[2:].split(":", 1)
                 vals[k_.strip()] = v_.strip().strip("`")
-    if vals.get("csrc_sha256_16") != digest:
+    if vals.get("kernel_sources_sha256_16") != kernel_source_hash(kernel_name):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -684,8 +695,9 @@ def run_norm_bench(args):
                    "o_z_y": "bf16", "weight": "fp32", "eps": 1e-6,
                    "l2_flush": "none needed: o and z (%.2f GB) exceed the 129 MB L2" % (2 * rows * D * 2 / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": B},
+                     "frac": achieved / hbm_peak,
+                     "traffic": profiled_traffic("gated_rmsnorm_kernel", "gated_rmsnorm_cfg2_output"),
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": B},
         "e2e": e2e_line, "gpu_launches": args.steps, "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -795,9 +807,10 @@ def run_prep_bench(args):
                    "h_qk": h_qk, "h_v": h_v, "d_k": d_k, "d_v": d_v, "x_qkv": "bf16", "gates": "fp32",
                    "l2_flush": "none needed: x (%.2f GB) exceeds the 129 MB L2" % (T * C * 2 / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": B,
-                     "note": "bytes and time of the whole call (conv + SiLU kernel and gate kernel)"},
+                     "frac": achieved / hbm_peak, "traffic": profiled_traffic("conv_silu_kernel", "input_prep_cfg2"),
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": B,
+                     "note": "bytes and time of the whole call (conv + SiLU kernel and gate kernel); "
+                             "traffic: the conv + SiLU kernel's DRAM bytes"},
         "e2e": e2e_line, "gpu_launches": 2 * args.steps, "clocks": clk,
     }
     if not args.no_cpu_baseline:
