@@ -904,7 +904,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int wb = tid - 384;  // == TMEM lane == d_v index
     const uint32_t lane_off = (uint32_t)((wb & ~31) << 16);
     const bool live = wb < DV;
-    bool ok_all = true;
     // A unit's final state S = mu S~, once its last S~ update has finished; in a tree
     // launch the unit's children may then start from it.
     auto store_final = [&](int un, int uh, float umu) {
@@ -957,7 +956,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     int un_c = 0, uh_c = 0;  // the unit of the chunk whose state step ran last,
     float mu_c = 1.f;        // and mu after it
-    int clast = -1;
     constexpr size_t osz = OF32 ? 4 : 2;
     const int pieces = (int)(DV * osz / 16);  // 16-byte pieces of one output row
     const int pshift = __ffs(pieces) - 1;
@@ -969,7 +967,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---- (U' diag(s/lambda))^T -> bf16 hi / lo A operands
         const ChunkScalars& cs = cscal[c % 3];
         bool ok = wait_all(with(with(kNone, B_P1_DONE0 + (c & 1), (c >> 1) & 1), B_UP_DONE, c & 1), 12);
-        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
 #pragma unroll 1
         for (int hb = 0; hb < 2; ++hb) {  // columns j in [32 hb, 32 hb + 32)
@@ -997,22 +995,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         un_c = cs.n;
         uh_c = cs.h;
         mu_c = cs.mu_next;
-        clast = c;
       }
-      if (more) {
-        // ---- S~ -> bf16 A operand for chunk c+1 (first applying its decay when eager)
+      if (more || c >= 0) {
+        // ---- S~ -> bf16 A operand for chunk c+1 (first applying its decay when eager).
+        // After the CTA's last chunk (no chunk c+1) only the final state of its unit is
+        // stored here, once chunk c's S~ update has finished.
         const int cn = c + 1;
         const float* sc = slot_sc(cn);
-        uint64_t wl = with(kNone, B_FULL0 + cn % 3, (cn / 3) & 1);
+        uint64_t wl = more ? with(kNone, B_FULL0 + cn % 3, (cn / 3) & 1) : kNone;
         if (c >= 0) wl = with(wl, B_STATE_DONE, c & 1);
         bool ok = wait_all(wl, 11);
-        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
-        if (sc_int(sc, SC_FLAGS) & F_UFIRST) {
-          // chunk cn starts a unit: the one that ended with chunk c is complete
+        if (!more || (sc_int(sc, SC_FLAGS) & F_UFIRST)) {
+          // chunk cn starts a unit (or there is none): the one that ended with chunk c is complete
           if (c >= 0) store_final(un_c, uh_c, mu_c);
-          if (!load_initial(sc_int(sc, SC_N), sc_int(sc, SC_H))) { ok_all = false; break; }
+          if (more && !load_initial(sc_int(sc, SC_N), sc_int(sc, SC_H))) break;
         }
+      }
+      if (more) {
+        const int cn = c + 1;
+        const float* sc = slot_sc(cn);
         const bool eager = sc_int(sc, SC_FLAGS) & F_EAGER;
         const float rmw = sc[SC_RMW];
 #pragma unroll 1
@@ -1041,7 +1044,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // chunk c+1 runs while the outputs of chunk c are written
         const int cn = c + 1, pn = cn & 1;
         bool ok = wait(B_W_DONE, cn & 1, 15);
-        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
         const uint32_t wt = sbase + L::WT0 + pn * L::SCR_BYTES;
 #pragma unroll 1
@@ -1076,7 +1079,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const ChunkScalars& cs = cscal[c % 3];
         bool ok = wait(B_O_DONE, c & 1, 13);
         if (wb == 0) bulk_wait_read();  // the staging tiles are free again
-        if (named_bar_or(2, 128, !ok || *abort_flag)) { ok_all = false; break; }
+        if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
         const int m = cs.m;
         const long long t0 = cs.t0;
@@ -1181,12 +1184,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!more) break;
     }
     if (wb == 0) bulk_wait_all();
-    // the last unit's final state (every MMA on S~ finished before the last O_DONE); the
-    // decision is taken once for the whole group, which then may meet at a barrier
-    if (!named_bar_or(2, 128, !ok_all || *abort_flag || clast < 0)) {
-      tc_fence_after();
-      store_final(un_c, uh_c, mu_c);
-    }
   }
   tc_fence_before();
   __syncthreads();

@@ -3,9 +3,10 @@
 Bound: the kernel works in fp32 and rounds once to y's type. Its fp32
 arithmetic (about ten operations, the fast exponential and division of the
 SiLU and the reciprocal square root) stays within 2e-6 of the value, relative,
-for the |z| <= 20 these inputs hold; a bf16 y adds at most 2^-9 relative. The
-tests allow 2^-8 (bf16 y) and 1e-5 (fp32 y) relative, plus 1e-30 absolute for
-the values near zero that SiLU produces in the negative tail.
+for the |z| <= 20 these inputs hold; rounding y to bf16 adds up to half an ulp,
+just under 2^-8 relative for values just above a power of two. The tests allow
+2^-8 + 1e-5 (bf16 y) and 1e-5 (fp32 y) relative, plus 1e-30 absolute for the
+values near zero that SiLU produces in the negative tail.
 """
 import numpy as np
 import pytest
@@ -17,7 +18,7 @@ import workloads
 
 pytestmark = pytest.mark.gpu
 
-RTOL = {torch.bfloat16: 2.0 ** -8, torch.float32: 1e-5}
+RTOL = {torch.bfloat16: 2.0 ** -8 + 1e-5, torch.float32: 1e-5}
 
 
 def _check(y, o, z, w, eps, rows=None):
