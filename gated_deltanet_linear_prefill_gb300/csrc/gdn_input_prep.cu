@@ -14,9 +14,9 @@
 //
 // Both kernels are bound by HBM. The convolution gives each thread 8 consecutive
 // channels (one 16-byte bf16 vector) over a run of kRows rows: partial sums of the
-// open outputs stay in registers, rows are loaded kBatch at a time so that several
-// loads are in flight, and a warp's loads and stores cover 512 contiguous bytes of
-// a row. A run that starts inside a sequence re-reads its K-1 halo rows (3 of 128
+// open outputs stay in registers, rows stream through a per-thread ring in shared
+// memory (cp.async) so that many loads are in flight, and a warp's loads and stores
+// cover 512 contiguous bytes of a row. A run that starts inside a sequence re-reads its K-1 halo rows (3 of 128
 // rows for K = 4). Consecutive blocks take the channel blocks of one run.
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -28,8 +28,8 @@ namespace {
 
 constexpr int kConvThreads = 128;
 constexpr int kRows = 128;   // rows per thread
-constexpr int kBatch = 8;   // rows loaded at once
-constexpr int kConvBlocks = 4;  // resident blocks per SM the register budget allows (<= 128 registers)
+constexpr int kStages = 16;  // rows in flight per thread (a ring of 16-byte slots in shared memory)
+constexpr int kConvBlocks = 5;  // resident blocks per SM the register budget allows (<= 102 registers)
 constexpr int kAuxThreads = 256;
 
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
@@ -40,6 +40,16 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     w[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 16 bytes global -> shared without a register (cached in L2 only), and its group
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // silu(y) = y / (1 + e^-y), with e^-y capped at e^80 so that the fast division stays
@@ -172,39 +182,45 @@ __global__ void __launch_bounds__(kConvThreads, kConvBlocks) conv_silu_kernel(Pr
   int64_t bos = p.cu[n] > 0 ? (int64_t)p.cu[n] : 0;
   int64_t eos = p.cu[n + 1];
   prime(t0, bos > t0 ? t0 : bos, n);
+  // Rows stream through a ring of kStages 16-byte slots per thread: the copy of row
+  // t + kStages - 1 is issued before row t is used, so kStages - 1 rows are in flight
+  // without holding registers. A thread reads only its own slots (no block barrier).
+  __shared__ uint4 ring[kStages][kConvThreads];
+  const uint32_t slot0 = (uint32_t)__cvta_generic_to_shared(&ring[0][threadIdx.x]);
+  auto issue = [&](int64_t r) {  // an empty group past the run keeps the group count uniform
+    if (r < t1) cp_async16(slot0 + (uint32_t)((r - t0) & (kStages - 1)) * (kConvThreads * 16u), p.x + r * p.C + 8 * c8);
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int s_ = 0; s_ < kStages - 1; ++s_) issue(t0 + s_);
 #pragma unroll 1
-  for (int64_t tb = t0; tb < t1; tb += kBatch) {
-    uint4 raw[kBatch];
+  for (int64_t t = t0; t < t1; ++t) {
+    issue(t + kStages - 1);
+    cp_async_wait<kStages - 1>();  // row t's group has landed
+    const uint4 xr = ring[(t - t0) & (kStages - 1)][threadIdx.x];
+    if (t >= eos) {  // a new sequence starts at row t (skipping empty ones)
+      while (n + 1 < p.N && (int64_t)p.cu[n + 1] <= t) ++n;
+      bos = t;
+      eos = p.cu[n + 1];
+      prime(t, bos, n);
+    }
+    float2 y[4];
+    feed(xr, y);
+    float out[8];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-      if (tb + i < t1) raw[i] = __ldcs(reinterpret_cast<const uint4*>(p.x + (tb + i) * p.C) + c8);
+    for (int e = 0; e < 4; ++e) {
+      out[2 * e] = silu(y[e].x);
+      out[2 * e + 1] = silu(y[e].y);
+    }
+    __stcs(reinterpret_cast<uint4*>(dst + t * ldd + cd), pack8(out));
+    if (t == eos - 1 && p.state_out) {  // the sequence's last row: its final window
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int64_t t = tb + i;
-      if (t >= t1) break;
-      if (t >= eos) {  // a new sequence starts at row t (skipping empty ones)
-        while (n + 1 < p.N && (int64_t)p.cu[n + 1] <= t) ++n;
-        bos = t;
-        eos = p.cu[n + 1];
-        prime(t, bos, n);
-      }
-      float2 y[4];
-      feed(raw[i], y);
-      float out[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        out[2 * e] = silu(y[e].x);
-        out[2 * e + 1] = silu(y[e].y);
-      }
-      __stcs(reinterpret_cast<uint4*>(dst + t * ldd + cd), pack8(out));
-      if (t == eos - 1 && p.state_out) {  // the sequence's last row: its final window
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j)
-          *(reinterpret_cast<uint4*>(p.state_out + ((size_t)n * (K - 1) + j) * p.C) + c8) =
-              row_or_carried<K>(p, t - (K - 2) + j, bos, n, c8);
-      }
+      for (int j = 0; j < K - 1; ++j)
+        *(reinterpret_cast<uint4*>(p.state_out + ((size_t)n * (K - 1) + j) * p.C) + c8) =
+            row_or_carried<K>(p, t - (K - 2) + j, bos, n, c8);
     }
   }
+  cp_async_wait<0>();  // no copy outlives the thread
 }
 
 // Gate parameters over every (row, value head), and the final windows of empty
