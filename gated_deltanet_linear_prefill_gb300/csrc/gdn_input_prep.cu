@@ -29,6 +29,7 @@ namespace {
 constexpr int kConvThreads = 128;
 constexpr int kRows = 128;   // rows per thread
 constexpr int kStages = 16;  // rows in flight per thread (a ring of 16-byte slots in shared memory)
+static_assert((kStages & (kStages - 1)) == 0, "ring slots are indexed with a mask");
 constexpr int kConvBlocks = 5;  // resident blocks per SM the register budget allows (<= 102 registers)
 constexpr int kAuxThreads = 256;
 
