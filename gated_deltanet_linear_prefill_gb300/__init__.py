@@ -32,6 +32,7 @@ GDN_BF16, GDN_F32 = 0, 1
 GDN_OK = 0
 GDN_FLAG_NO_L2NORM = 0x1
 GDN_FLAG_SIMT = 0x2
+GDN_FLAG_TEST_CHILD_FIRST = 0x4  # tests only: fault injection for the bounded waits (include/gdn.h)
 GDN_NOALLOC_MAX_SEQS = 16384  # include/gdn.h
 STATUS_NAMES = ["GDN_OK", "GDN_ERR_NULL", "GDN_ERR_SHAPE", "GDN_ERR_DTYPE", "GDN_ERR_ALIGN",
                 "GDN_ERR_SEQLENS", "GDN_ERR_STATE_INDEX", "GDN_ERR_ALIAS", "GDN_ERR_WORKSPACE",

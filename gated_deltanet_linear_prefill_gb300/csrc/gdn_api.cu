@@ -341,6 +341,16 @@ extern "C" gdn_status gdn_prefill_varlen(const void* q, const void* k, const voi
 
 namespace gdn {
 
+// GDN_FLAG_TEST_CHILD_FIRST: reverses the work list (one block), so that children
+// precede their parents (fault injection for the bounded waits).
+__global__ void gdn_reverse_order_kernel(int32_t* order, int n) {
+  for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
+    const int32_t a = order[i];
+    order[i] = order[n - 1 - i];
+    order[n - 1 - i] = a;
+  }
+}
+
 // Tree launch with no tokens at all: every sequence ends where it starts, so
 // final_state[n] is its root's starting state (one block per (sequence, head)).
 __global__ void gdn_tree_copy_kernel(Params p) {
@@ -380,6 +390,10 @@ extern "C" gdn_status gdn_prefill_tree(const void* q, const void* k, const void*
   p.ready = (uint32_t*)((char*)desc->workspace + gdn::tree_flags_offset(p.num_seqs));
   cudaStream_t s = (cudaStream_t)stream;
   if (launch_prep(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (desc->flags & GDN_FLAG_TEST_CHILD_FIRST) {
+    gdn::gdn_reverse_order_kernel<<<1, 256, 0, s>>>(const_cast<int32_t*>(p.order), p.num_seqs);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  }
   if (p.total_tokens == 0) {
     const long long units = (long long)p.num_seqs * p.h_v;
     if (units > 0x7fffffffLL) return GDN_ERR_SHAPE;

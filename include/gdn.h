@@ -75,6 +75,12 @@ typedef enum {
 /* Flags. */
 #define GDN_FLAG_NO_L2NORM 0x1u /* use q and k as given (tests of closed forms) */
 #define GDN_FLAG_SIMT 0x2u      /* run the CUDA-core (SIMT) kernel instead of the tensor-core one */
+/* Tests only (fault injection, gdn_prefill_tree): the work list is reversed, so that
+ * children come before their parents. A chain of more sequences than the GPU holds
+ * units at once then stalls on ready flags that no CTA will set; every bounded wait
+ * runs out, the device status becomes GDN_ERR_DEVICE_TIMEOUT and the kernel returns
+ * (outputs unspecified). No fault, trap or hang. Ignored by gdn_prefill_varlen. */
+#define GDN_FLAG_TEST_CHILD_FIRST 0x4u
 
 /*
  * Problem descriptor. Every field is read on the host at call time; the

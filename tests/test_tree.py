@@ -175,3 +175,24 @@ def test_tree_bad_parent_reported_on_device():
     with pytest.raises(gdn.GdnError) as e:
         run_tree(w, np.array([-1, 2, 0], dtype=np.int32))  # parent 2 of sequence 1 is not below it
     assert e.value.code == gdn.STATUS_NAMES.index("GDN_ERR_PARENT")
+
+
+@pytest.mark.gpu
+def test_stalled_ready_flags_time_out_and_the_context_survives():
+    """Fault injection without a fault: with the work list reversed, a chain of 400
+    sequences puts the deepest children in every CTA's hands while their parents wait
+    behind them, so no ready flag is ever set. Every bounded wait runs out (2 s), the
+    launch reports GDN_ERR_DEVICE_TIMEOUT and returns; the context stays usable and
+    the same tree then runs correctly."""
+    N = 400
+    w = workloads.random_workload([2] * N, h_qk=1, h_v=1, d_k=64, d_v=64, seed=21)
+    parent = torch.tensor([-1] + list(range(N - 1)), dtype=torch.int32)
+    d = w.to("cuda")
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.prefill_tree(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, parent.cuda(),
+                         flags=gdn.GDN_FLAG_TEST_CHILD_FIRST, check_device=True)
+    assert e.value.code == gdn.STATUS_NAMES.index("GDN_ERR_DEVICE_TIMEOUT")
+    o, s = gdn.prefill_tree(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, parent.cuda(), check_device=True)
+    torch.cuda.synchronize()
+    o_ref, s_ref = oracle.tree(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, parent)
+    check(errors(o.double().cpu().numpy(), s.double().cpu().numpy(), o_ref, s_ref), "tc", label="tree after stall")
