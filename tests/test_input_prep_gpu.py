@@ -87,6 +87,19 @@ def test_parity_ragged(K, bias):
     np.testing.assert_array_equal(fin.float().cpu().numpy(), fin_ref)
 
 
+def test_unequal_blocks():
+    # q / k blocks of 2 x 64 channels and a v block of 6 x 128: the split at uneven
+    # boundaries (thread vectors never straddle a block: every block is a multiple of 8)
+    lengths = [129, 3, 200]
+    inp = workloads.prep_inputs(lengths, h_qk=2, d_k=64, h_v=6, d_v=128, K=4, seed=12, bias=True)
+    q, k, v, g, beta, fin = run_prep(inp, 2, 64, 6, 128)
+    assert q.shape == (332, 2, 64) and v.shape == (332, 6, 128) and g.shape == (332, 6)
+    u_ref, fin_ref, scale, g_ref, b_ref = reference(inp)
+    check_u(q, k, v, u_ref, scale)
+    check_gates(g, beta, g_ref, b_ref)
+    np.testing.assert_array_equal(fin.float().cpu().numpy(), fin_ref)
+
+
 def test_carried_windows_and_slots():
     lengths = [0, 2, 1, 65, 40]
     inp = workloads.prep_inputs(lengths, h_qk=1, d_k=128, h_v=2, d_v=128, K=4, seed=3, slots=4, bias=True)
