@@ -50,6 +50,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "gdn_internal.cuh"
 #include "tc_ptx.cuh"
@@ -367,9 +368,9 @@ __device__ __noinline__ void drain_loads(uint32_t bars, int kq_issued, int v_iss
 }
 
 // ---------------------------------------------------------------- the kernel
-// OF32: fp32 output (else bf16), a template parameter so that each kernel holds
-// only its own epilogue.
-template <int DK, int DV, bool OF32>
+// OF32: fp32 output (else bf16); GF32: fp32 gates (else bf16). Template parameters,
+// so that each kernel holds only its own epilogue and gate loads.
+template <int DK, int DV, bool OF32, bool GF32>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gdn_tc_kernel(const Params p, const __grid_constant__ Tmaps tm) {
   using L = TcLayout<DK, DV>;
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int64_t avail = len - st;
         const int64_t i0 = (bos + st + lane) * p.h_v + h, i1 = i0 + 32 * (int64_t)p.h_v;
         const bool in0 = lane < avail, in1 = lane + 32 < avail;
-        if (p.gate_f32) {
+        if constexpr (GF32) {
           const float* gg = reinterpret_cast<const float*>(p.g);
           const float* bb = reinterpret_cast<const float*>(p.beta);
           g0 = in0 ? gg[i0] : 0.f;
@@ -1239,7 +1240,7 @@ bool encode_out(CUtensorMap* m, void* base, int64_t T, int H, int D, bool f32) {
 }
 
 
-template <int DK, int DV, bool OF32>
+template <int DK, int DV, bool OF32, bool GF32>
 cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   using L = TcLayout<DK, DV>;
   Tmaps tm;
@@ -1248,7 +1249,7 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
       !encode_rows(&tm.v, p.v, p.total_tokens, p.h_v, DV) ||
       !encode_out(&tm.o, p.out, p.total_tokens, p.h_v, DV, p.out_f32 != 0))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV, OF32>), (int)L::DYN_SMEM);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV, OF32, GF32>), (int)L::DYN_SMEM);
   if (e != cudaSuccess) return e;
   const long long units = (long long)p.num_seqs * p.h_v;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -1258,7 +1259,7 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   e = device_sm_count(&sms);
   if (e != cudaSuccess) return e;
   const long long grid = units < sms ? units : sms;
-  gdn_tc_kernel<DK, DV, OF32><<<(unsigned)grid, kTcThreads, L::DYN_SMEM, stream>>>(p, tm);
+  gdn_tc_kernel<DK, DV, OF32, GF32><<<(unsigned)grid, kTcThreads, L::DYN_SMEM, stream>>>(p, tm);
   return cudaGetLastError();
 }
 
@@ -1267,14 +1268,24 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
 cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
   if (p.total_tokens <= 0) return launch_simt(p, stream);  // only empty sequences: state copy
   if (p.total_tokens > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const bool f = p.out_f32 != 0;
-  if (p.d_k == 128 && p.d_v == 128)
-    return f ? launch_tc_dk<128, 128, true>(p, stream) : launch_tc_dk<128, 128, false>(p, stream);
-  if (p.d_k == 64 && p.d_v == 64)
-    return f ? launch_tc_dk<64, 64, true>(p, stream) : launch_tc_dk<64, 64, false>(p, stream);
-  if (p.d_k == 128 && p.d_v == 64)
-    return f ? launch_tc_dk<128, 64, true>(p, stream) : launch_tc_dk<128, 64, false>(p, stream);
-  return f ? launch_tc_dk<64, 128, true>(p, stream) : launch_tc_dk<64, 128, false>(p, stream);
+  // output and gate storage types are template parameters, so that each kernel carries
+  // only the code of its own types
+  const int t = (p.out_f32 ? 2 : 0) + (p.gate_f32 ? 1 : 0);
+  auto by_types = [&](auto dk, auto dv) {
+    constexpr int K_ = decltype(dk)::value, V_ = decltype(dv)::value;
+    switch (t) {
+      case 0: return launch_tc_dk<K_, V_, false, false>(p, stream);
+      case 1: return launch_tc_dk<K_, V_, false, true>(p, stream);
+      case 2: return launch_tc_dk<K_, V_, true, false>(p, stream);
+      default: return launch_tc_dk<K_, V_, true, true>(p, stream);
+    }
+  };
+  using I64 = std::integral_constant<int, 64>;
+  using I128 = std::integral_constant<int, 128>;
+  if (p.d_k == 128 && p.d_v == 128) return by_types(I128{}, I128{});
+  if (p.d_k == 64 && p.d_v == 64) return by_types(I64{}, I64{});
+  if (p.d_k == 128 && p.d_v == 64) return by_types(I128{}, I64{});
+  return by_types(I64{}, I128{});
 }
 
 }  // namespace gdn
