@@ -294,3 +294,41 @@ def gate_params(a, b, A_log, dt_bias):
     with np.errstate(over="ignore"):
         beta = 1.0 / (1.0 + np.exp(-bb))
     return g, beta
+
+
+def causal_conv_silu_tree(x, conv_w, cu_seqlens, parent, conv_bias=None, conv_state=None, state_index=None):
+    """``causal_conv_silu`` over a prefix tree of packed sequences: sequence n
+    continues sequence parent[n] (parent[n] in [-1, n)), so its window reaches
+    into the last rows of its ancestors' path, and a root's into its carried
+    window (conv_state[state_index[root]], or zeros). Written out as the
+    README's replicated layout (Phase 2 item 2; the prefix-tree item runs each
+    candidate over its whole path so that the convolution window matches): each
+    node's rows are the tail of its full root-to-node path run as one sequence.
+    Returns (u [T, C], final_state [N, K-1, C])."""
+    x = np.asarray(x, dtype=np.float64)
+    cu = _i64(cu_seqlens)
+    par = _i64(parent)
+    N = cu.size - 1
+    if par is None or par.size != N:
+        raise ValueError("parent needs one entry per sequence")
+    K = np.asarray(conv_w).shape[1]
+    u = np.zeros_like(x)
+    final = np.zeros((N, K - 1, x.shape[1]))
+    for n in range(N):
+        path = [n]
+        while int(par[path[-1]]) >= 0:
+            p_ = int(par[path[-1]])
+            if p_ >= path[-1]:
+                raise ValueError(f"parent[{path[-1]}] = {p_} is not below {path[-1]}")
+            path.append(p_)
+        path.reverse()
+        rows = np.concatenate([np.arange(int(cu[m]), int(cu[m + 1])) for m in path]).astype(np.int64)
+        root = path[0]
+        si = None
+        if conv_state is not None:
+            si = [root if state_index is None else int(np.asarray(state_index)[root])]
+        up, fp = causal_conv_silu(x[rows], conv_w, [0, rows.size], conv_bias, conv_state, si)
+        b, e = int(cu[n]), int(cu[n + 1])
+        u[b:e] = up[rows.size - (e - b):]
+        final[n] = fp[0]
+    return u, final

@@ -129,3 +129,45 @@ def test_gate_closed_forms():
     assert np.all(g < 0) and np.all(np.exp(g) > 0) and np.all(np.exp(g) < 1)
     # beta is the logistic function: logit(beta) = b
     np.testing.assert_allclose(np.log(beta / (1 - beta)), b, rtol=1e-9, atol=1e-12)
+
+
+def test_tree_roots_equal_the_plain_batch():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((30, 4))
+    w = rng.standard_normal((4, 4))
+    s0 = rng.standard_normal((2, 3, 4))
+    cu = [0, 10, 30]
+    u, f = oracle.causal_conv_silu(x, w, cu, None, s0, [1, 0])
+    ut, ft = oracle.causal_conv_silu_tree(x, w, cu, [-1, -1], None, s0, [1, 0])
+    np.testing.assert_array_equal(u, ut)
+    np.testing.assert_array_equal(f, ft)
+
+
+def test_tree_chain_equals_one_sequence():
+    # a chain of pieces (one of them empty, one shorter than the window) is one sequence
+    rng = np.random.default_rng(8)
+    lens = [7, 1, 0, 2, 12]
+    x = rng.standard_normal((sum(lens), 5))
+    w = rng.standard_normal((5, 4))
+    b = rng.standard_normal(5)
+    s0 = rng.standard_normal((1, 3, 5))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    u1, f1 = oracle.causal_conv_silu(x, w, [0, sum(lens)], b, s0, [0])
+    ut, ft = oracle.causal_conv_silu_tree(x, w, cu, [-1, 0, 1, 2, 3], b, s0, [0, -1, -1, -1, -1])
+    np.testing.assert_allclose(ut, u1, rtol=1e-14, atol=1e-15)
+    np.testing.assert_array_equal(ft[-1], f1[0])
+    # every node's window is the last three rows of the path up to it
+    np.testing.assert_array_equal(ft[0], x[4:7])
+    np.testing.assert_array_equal(ft[1], x[5:8])
+    np.testing.assert_array_equal(ft[2], ft[1])  # an empty node keeps its parent's window
+
+
+def test_tree_siblings_share_the_parent_window():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((9, 3))
+    w = rng.standard_normal((3, 4))
+    cu = [0, 5, 7, 9]  # a prefix of 5 rows and two 2-row children
+    u, _ = oracle.causal_conv_silu_tree(x, w, cu, [-1, 0, 0])
+    for b in (5, 7):  # each child run alone after the prefix rows
+        ua, _ = oracle.causal_conv_silu(np.concatenate([x[:5], x[b:b + 2]]), w, [0, 7])
+        np.testing.assert_allclose(u[b:b + 2], ua[5:], rtol=1e-14, atol=1e-15)
