@@ -24,7 +24,7 @@ __all__ = [
     "GdnError", "GdnDesc", "GDN_OK", "GDN_BF16", "GDN_F32", "GDN_FLAG_NO_L2NORM", "GDN_FLAG_SIMT",
     "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_get_device_status",
     "gdn_status_string", "make_desc", "prefill_varlen", "library_path", "load_library",
-    "gdn_gated_rmsnorm", "gated_rmsnorm", "GdnPrepDesc", "gdn_input_prep", "input_prep",
+    "gdn_gated_rmsnorm", "gated_rmsnorm", "GdnPrepDesc", "gdn_input_prep", "gdn_input_prep_tree", "input_prep",
 ]
 
 ABI_VERSION = 1
@@ -124,6 +124,8 @@ def load_library(build_if_missing: bool = True):
         lib.gdn_gated_rmsnorm.restype = ctypes.c_int
         lib.gdn_input_prep.argtypes = [P] * 16 + [ctypes.POINTER(GdnPrepDesc), P]
         lib.gdn_input_prep.restype = ctypes.c_int
+        lib.gdn_input_prep_tree.argtypes = [P] * 17 + [ctypes.POINTER(GdnPrepDesc), P]
+        lib.gdn_input_prep_tree.restype = ctypes.c_int
         lib.gdn_get_device_status.argtypes = [ctypes.POINTER(GdnDesc), P]
         lib.gdn_get_device_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -351,13 +353,25 @@ def gdn_input_prep(x, conv_w, conv_bias, cu_seqlens, conv_state_in, state_index,
                                   ctypes.byref(desc), _stream_handle(stream)))
 
 
+def gdn_input_prep_tree(x, conv_w, conv_bias, cu_seqlens, parent, conv_state_in, state_index, a, b, A_log,
+                        dt_bias, q, k, v, g, beta, conv_state_out, desc: GdnPrepDesc, stream=None) -> int:
+    """The C tree entry point with tensors for pointers; returns the gdn_status code."""
+    lib = load_library()
+    return int(lib.gdn_input_prep_tree(_ptr(x), _ptr(conv_w), _ptr(conv_bias), _ptr(cu_seqlens), _ptr(parent),
+                                       _ptr(conv_state_in), _ptr(state_index), _ptr(a), _ptr(b), _ptr(A_log),
+                                       _ptr(dt_bias), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                       _ptr(conv_state_out), ctypes.byref(desc), _stream_handle(stream)))
+
+
 def input_prep(x, conv_w, cu_seqlens, *, h_qk: int, d_k: int, h_v: int, d_v: int, conv_bias=None,
                conv_state=None, state_index=None, a=None, b=None, A_log=None, dt_bias=None,
-               want_conv_state: bool = True, stream=None):
+               parent=None, want_conv_state: bool = True, stream=None):
     """GDN input prep (see include/gdn.h): causal depthwise conv + SiLU over the
     packed rows x [T, C] bf16 (C = 2 h_qk d_k + h_v d_v), split into q, k [T, h_qk,
     d_k] and v [T, h_v, d_v] bf16, and, when a is given, the gates g, beta
-    [T, h_v] fp32. conv_w [C, K] fp32; conv_state [slots, K-1, C] bf16.
+    [T, h_v] fp32. conv_w [C, K] fp32; conv_state [slots, K-1, C] bf16. With
+    parent (int32 [N], parent[n] in [-1, n)) the sequences form a prefix tree and
+    a child's window comes from its ancestors' rows (gdn_input_prep_tree).
     Returns (q, k, v, g, beta, conv_state_out [N, K-1, C] bf16 or None); g and
     beta are None without a. Raises GdnError on a non-OK status."""
     dev = x.device
@@ -380,8 +394,12 @@ def input_prep(x, conv_w, cu_seqlens, *, h_qk: int, d_k: int, h_v: int, d_v: int
     d.num_state_slots = 0 if conv_state is None else int(conv_state.shape[0])
     if C != 2 * h_qk * d_k + h_v * d_v or tuple(conv_w.shape) != (C, K):
         raise ValueError("x must have 2 h_qk d_k + h_v d_v channels and conv_w must be [C, K]")
-    rc = gdn_input_prep(x, conv_w, conv_bias, cu_seqlens, conv_state, state_index, a, b, A_log, dt_bias,
-                        q, k, v, g, beta, cs, d, stream)
+    if parent is None:
+        rc = gdn_input_prep(x, conv_w, conv_bias, cu_seqlens, conv_state, state_index, a, b, A_log, dt_bias,
+                            q, k, v, g, beta, cs, d, stream)
+    else:
+        rc = gdn_input_prep_tree(x, conv_w, conv_bias, cu_seqlens, parent, conv_state, state_index, a, b, A_log,
+                                 dt_bias, q, k, v, g, beta, cs, d, stream)
     if rc != GDN_OK:
-        raise GdnError(rc, "gdn_input_prep")
+        raise GdnError(rc, "gdn_input_prep" if parent is None else "gdn_input_prep_tree")
     return q, k, v, g, beta, cs

@@ -491,13 +491,13 @@ extern "C" gdn_status gdn_gated_rmsnorm(const void* o, const void* z, const floa
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-extern "C" gdn_status gdn_input_prep(const void* x, const float* conv_w, const float* conv_bias,
-                                     const int32_t* cu_seqlens, const void* conv_state_in,
-                                     const int32_t* state_index, const void* a, const void* b,
-                                     const float* A_log, const float* dt_bias, void* q, void* k, void* v,
-                                     float* g, float* beta, void* conv_state_out, const gdn_prep_desc* desc,
-                                     void* stream) {
+static gdn_status input_prep(const void* x, const float* conv_w, const float* conv_bias,
+                             const int32_t* cu_seqlens, const int32_t* parent, const void* conv_state_in,
+                             const int32_t* state_index, const void* a, const void* b, const float* A_log,
+                             const float* dt_bias, void* q, void* k, void* v, float* g, float* beta,
+                             void* conv_state_out, const gdn_prep_desc* desc, void* stream, bool tree) {
   if (!desc) return GDN_ERR_NULL;
+  if (tree && desc->num_seqs > 0 && !parent) return GDN_ERR_NULL;
   const gdn_prep_desc& d = *desc;
   if (d.num_seqs < 0 || d.total_tokens < 0 || d.h_qk < 1 || d.h_v < 1 || d.d_k < 8 || d.d_v < 8 ||
       d.d_k % 8 || d.d_v % 8 || d.conv_width < 2 || d.conv_width > 4 || d.num_state_slots < 0)
@@ -516,7 +516,7 @@ extern "C" gdn_status gdn_input_prep(const void* x, const float* conv_w, const f
   const void* v16[] = {x, conv_w, q, k, v, conv_state_in, conv_state_out};
   for (const void* ptr : v16)
     if (!aligned(ptr, 16)) return GDN_ERR_ALIGN;
-  const void* v4[] = {conv_bias, cu_seqlens, state_index, A_log, dt_bias, g, beta};
+  const void* v4[] = {conv_bias, cu_seqlens, parent, state_index, A_log, dt_bias, g, beta};
   for (const void* ptr : v4)
     if (!aligned(ptr, 4)) return GDN_ERR_ALIGN;
   if (!aligned(a, 2) || !aligned(b, 2)) return GDN_ERR_ALIGN;
@@ -530,6 +530,7 @@ extern "C" gdn_status gdn_input_prep(const void* x, const float* conv_w, const f
                    {cu_seqlens, (size_t)(d.num_seqs + 1) * 4},
                    {conv_state_in, conv_state_in ? (size_t)d.num_state_slots * (K - 1) * C * 2 : 0},
                    {state_index, state_index ? (size_t)d.num_seqs * 4 : 0},
+                   {parent, tree ? (size_t)d.num_seqs * 4 : 0},
                    {a, ab},
                    {b, ab},
                    {A_log, gates ? (size_t)d.h_v * 4 : 0},
@@ -555,6 +556,7 @@ extern "C" gdn_status gdn_input_prep(const void* x, const float* conv_w, const f
   p.cu_seqlens = cu_seqlens;
   p.conv_state_in = conv_state_in;
   p.state_index = state_index;
+  p.parent = tree ? parent : nullptr;
   p.a = a;
   p.b = b;
   p.A_log = A_log;
@@ -574,4 +576,24 @@ extern "C" gdn_status gdn_input_prep(const void* x, const float* conv_w, const f
   p.slots = conv_state_in ? d.num_state_slots : 0;
   const cudaError_t e = launch_input_prep(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_input_prep(const void* x, const float* conv_w, const float* conv_bias,
+                                     const int32_t* cu_seqlens, const void* conv_state_in,
+                                     const int32_t* state_index, const void* a, const void* b,
+                                     const float* A_log, const float* dt_bias, void* q, void* k, void* v,
+                                     float* g, float* beta, void* conv_state_out, const gdn_prep_desc* desc,
+                                     void* stream) {
+  return input_prep(x, conv_w, conv_bias, cu_seqlens, nullptr, conv_state_in, state_index, a, b, A_log, dt_bias,
+                    q, k, v, g, beta, conv_state_out, desc, stream, false);
+}
+
+extern "C" gdn_status gdn_input_prep_tree(const void* x, const float* conv_w, const float* conv_bias,
+                                          const int32_t* cu_seqlens, const int32_t* parent,
+                                          const void* conv_state_in, const int32_t* state_index, const void* a,
+                                          const void* b, const float* A_log, const float* dt_bias, void* q,
+                                          void* k, void* v, float* g, float* beta, void* conv_state_out,
+                                          const gdn_prep_desc* desc, void* stream) {
+  return input_prep(x, conv_w, conv_bias, cu_seqlens, parent, conv_state_in, state_index, a, b, A_log, dt_bias,
+                    q, k, v, g, beta, conv_state_out, desc, stream, true);
 }

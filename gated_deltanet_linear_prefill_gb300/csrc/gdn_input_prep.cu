@@ -76,6 +76,7 @@ struct PrepArgs {
   const int32_t* cu;
   const __nv_bfloat16* state_in;  // [slots, K-1, C] or null
   const int32_t* state_index;     // [N] or null
+  const int32_t* parent;          // [N] or null: a prefix tree (parent[n] in [-1, n))
   __nv_bfloat16* q;
   __nv_bfloat16* k;
   __nv_bfloat16* v;
@@ -91,8 +92,27 @@ struct PrepArgs {
 };
 
 // the carried window's row r (0 = oldest) of sequence n, 8 channels from c8 * 8,
-// as loaded (packed bf16)
+// as loaded (packed bf16). In a tree the window is the last rows of the ancestors'
+// path: the walk goes up parent by parent (indices fall, so it ends) until the row
+// is inside one, else the root's carried window supplies it. A parent outside
+// [-1, n) counts as none.
 __device__ __forceinline__ uint4 carried_row(const PrepArgs& p, int K, int n, int r, int c8) {
+  if (p.parent) {
+    int64_t need = (K - 1) - r;  // rows before sequence n's first row
+#pragma unroll 1
+    for (int steps = 0; steps < p.N; ++steps) {
+      const int32_t pa = p.parent[n];
+      if (pa < 0 || pa >= n) break;
+      const int64_t pb = p.cu[pa] > 0 ? (int64_t)p.cu[pa] : 0;
+      const int64_t pe = (int64_t)p.cu[pa + 1] < p.T ? (int64_t)p.cu[pa + 1] : p.T;
+      const int64_t len = pe > pb ? pe - pb : 0;
+      if (need <= len)
+        return __ldg(reinterpret_cast<const uint4*>(p.x + (pe - need) * p.C) + c8);
+      need -= len;
+      n = pa;
+    }
+    r = (K - 1) - (int)need;
+  }
   int64_t slot = -1;
   if (p.state_in) {
     slot = p.state_index ? (int64_t)p.state_index[n] : (int64_t)n;
@@ -287,6 +307,7 @@ cudaError_t launch_input_prep(const InputPrepArgs& a, cudaStream_t stream) {
   p.cu = a.cu_seqlens;
   p.state_in = static_cast<const __nv_bfloat16*>(a.conv_state_in);
   p.state_index = a.state_index;
+  p.parent = a.parent;
   p.q = static_cast<__nv_bfloat16*>(a.q);
   p.k = static_cast<__nv_bfloat16*>(a.k);
   p.v = static_cast<__nv_bfloat16*>(a.v);

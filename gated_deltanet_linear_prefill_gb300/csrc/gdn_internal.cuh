@@ -124,6 +124,7 @@ struct InputPrepArgs {
   const int32_t* cu_seqlens;
   const void* conv_state_in;
   const int32_t* state_index;
+  const int32_t* parent;  // null: independent sequences
   const void* a;
   const void* b;
   const float* A_log;

@@ -324,6 +324,23 @@ gdn_status gdn_input_prep(const void* x, const float* conv_w, const float* conv_
                           const float* A_log, const float* dt_bias, void* q, void* k, void* v, float* g,
                           float* beta, void* conv_state_out, const gdn_prep_desc* desc, void* stream);
 
+/*
+ * gdn_input_prep over a prefix tree: sequence n continues sequence parent[n]
+ * (int32 [N], device, parent[n] in [-1, n), as in gdn_prefill_tree), so the rows
+ * before its first row are the last rows of its ancestors' path in x (reaching
+ * into the root's carried window when that path is shorter than K-1); roots read
+ * their carried window as in gdn_input_prep. The window a continuation sees is
+ * then the one the open-jev-fast README's replicated full-path layout gives it
+ * (Phase 2 item 2). A parent outside [-1, n) is taken as -1 (gdn_prefill_tree
+ * reports it). parent may not overlap an output (GDN_ERR_ALIAS) and must be
+ * 4-byte aligned; everything else as in gdn_input_prep.
+ */
+gdn_status gdn_input_prep_tree(const void* x, const float* conv_w, const float* conv_bias, const int32_t* cu_seqlens,
+                               const int32_t* parent, const void* conv_state_in, const int32_t* state_index,
+                               const void* a, const void* b, const float* A_log, const float* dt_bias, void* q,
+                               void* k, void* v, float* g, float* beta, void* conv_state_out,
+                               const gdn_prep_desc* desc, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* gdn_status_string(gdn_status s);
 

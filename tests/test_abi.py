@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_prefill_varlen_noalloc",
         "gdn_tree_workspace_bytes", "gdn_prefill_tree", "gdn_get_device_status",
-        "gdn_status_string", "gdn_gated_rmsnorm", "gdn_input_prep"])
+        "gdn_status_string", "gdn_gated_rmsnorm", "gdn_input_prep", "gdn_input_prep_tree"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -290,3 +290,28 @@ def test_input_prep_host_checks():
     # without gates their pointers are ignored (even overlapping ones)
     assert call_prep(prep_desc(), a=None, g=MB, beta=MB) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
     assert call_prep(prep_desc()) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
+
+
+def call_prep_tree(desc, parent=(1 << 22) * 15, **ptrs):
+    if torch.cuda.is_available():
+        pytest.skip("fake-pointer validation calls run only without a device")
+    lib = gdn.load_library()
+    MB = 1 << 22
+    base = dict(x=MB, w=2 * MB, bias=None, cu=3 * MB, sin=None, sidx=None, a=4 * MB, b=5 * MB,
+                A=6 * MB, dt=7 * MB, q=8 * MB, k=9 * MB, v=10 * MB, g=11 * MB, beta=12 * MB, sout=13 * MB)
+    base.update(ptrs)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    order = ["x", "w", "bias", "cu"]
+    rest = ["sin", "sidx", "a", "b", "A", "dt", "q", "k", "v", "g", "beta", "sout"]
+    return lib.gdn_input_prep_tree(*[P(base[n]) for n in order], P(parent), *[P(base[n]) for n in rest],
+                                   ctypes.byref(desc) if desc is not None else None, None)
+
+
+def test_input_prep_tree_host_checks():
+    MB = 1 << 22
+    assert call_prep_tree(None) == E["GDN_ERR_NULL"]
+    assert call_prep_tree(prep_desc(), parent=None) == E["GDN_ERR_NULL"]
+    assert call_prep_tree(prep_desc(num_seqs=0, total_tokens=0), parent=None, x=None, cu=None) == E["GDN_OK"]
+    assert call_prep_tree(prep_desc(), parent=15 * MB + 2) == E["GDN_ERR_ALIGN"]
+    assert call_prep_tree(prep_desc(), parent=8 * MB + 64) == E["GDN_ERR_ALIAS"]  # parent under q
+    assert call_prep_tree(prep_desc()) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])

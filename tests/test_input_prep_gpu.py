@@ -19,14 +19,14 @@ from tests.parity import check, errors
 pytestmark = pytest.mark.gpu
 
 
-def run_prep(inp, h_qk, d_k, h_v, d_v, state_index=None, gates=True, want_state=True):
+def run_prep(inp, h_qk, d_k, h_v, d_v, state_index=None, gates=True, want_state=True, parent=None):
     dev = "cuda"
     cuda = lambda t: None if t is None else t.to(dev)
     out = gdn.input_prep(cuda(inp["x"]), cuda(inp["conv_w"]), cuda(inp["cu_seqlens"]), h_qk=h_qk, d_k=d_k,
                          h_v=h_v, d_v=d_v, conv_bias=cuda(inp["conv_bias"]), conv_state=cuda(inp["conv_state"]),
                          state_index=cuda(state_index), a=cuda(inp["a"]) if gates else None,
                          b=cuda(inp["b"]), A_log=cuda(inp["A_log"]), dt_bias=cuda(inp["dt_bias"]),
-                         want_conv_state=want_state)
+                         parent=cuda(parent), want_conv_state=want_state)
     torch.cuda.synchronize()
     return out
 
@@ -170,3 +170,62 @@ def test_full_size_sampled_sequences():
         check_u(q[b:e], k[b:e], v[b:e], u_ref, scale)
         check_gates(g[b:e], beta[b:e], g_ref, b_ref)
         np.testing.assert_array_equal(fin[n].float().cpu().numpy(), fin_ref[0])
+
+
+def tree_scale(inp, parent, state_index):
+    """|bias| + sum_j |w_j x_j| over each row's window along its root-to-node path."""
+    x = inp["x"].float().numpy().astype(np.float64)
+    w = inp["conv_w"].numpy().astype(np.float64)
+    K = w.shape[1]
+    st = None if inp["conv_state"] is None else inp["conv_state"].float().numpy()
+    cu = inp["cu_seqlens"].numpy().astype(np.int64)
+    par = parent.numpy()
+    scale = np.zeros_like(x)
+    for n in range(cu.size - 1):
+        path = [n]
+        while par[path[-1]] >= 0:
+            path.append(int(par[path[-1]]))
+        path.reverse()
+        rows = np.concatenate([np.arange(cu[m], cu[m + 1]) for m in path]).astype(np.int64)
+        slot = int(state_index[path[0]]) if st is not None else -1
+        car = st[slot] if slot >= 0 else np.zeros((K - 1, x.shape[1]))
+        seq = np.concatenate([car, x[rows]])
+        b, e = int(cu[n]), int(cu[n + 1])
+        off = rows.size - (e - b)
+        for i in range(e - b):
+            scale[b + i] = np.sum(np.abs(w.T * seq[off + i:off + i + K]), axis=0)
+    if inp["conv_bias"] is not None:
+        scale += np.abs(inp["conv_bias"].numpy())
+    return scale
+
+
+@pytest.mark.parametrize("kind", ["forest", "chain", "wide"])
+def test_tree_windows(kind):
+    # children continue their parents' rows; empty and short nodes pass the window on
+    lengths, parent = {
+        "forest": ([40, 2, 0, 70, 1, 33], [-1, 0, 1, 2, -1, 4]),
+        "chain": ([1, 0, 2, 130, 1, 5], [-1, 0, 1, 2, 3, 4]),
+        "wide": ([100, 3, 0, 64, 7, 1], [-1, 0, 0, 0, 0, 3]),
+    }[kind]
+    parent = torch.tensor(parent, dtype=torch.int32)
+    sidx = torch.tensor([1, -1, -1, -1, 0, -1], dtype=torch.int32)  # roots' carried windows
+    inp = workloads.prep_inputs(lengths, h_qk=1, d_k=64, h_v=2, d_v=64, K=4, seed=len(kind), slots=2, bias=True)
+    q, k, v, g, beta, fin = run_prep(inp, 1, 64, 2, 64, state_index=sidx, parent=parent)
+    u_ref, fin_ref = oracle.causal_conv_silu_tree(inp["x"].float().numpy(), inp["conv_w"].numpy(),
+                                                  inp["cu_seqlens"].numpy(), parent.numpy(),
+                                                  inp["conv_bias"].numpy(), inp["conv_state"].float().numpy(),
+                                                  sidx.numpy())
+    check_u(q, k, v, u_ref, tree_scale(inp, parent, sidx))
+    np.testing.assert_array_equal(fin.float().cpu().numpy(), fin_ref)
+
+
+def test_tree_chain_equals_one_sequence_bitwise():
+    lens = [7, 1, 0, 2, 150]
+    inp = workloads.prep_inputs(lens, h_qk=1, d_k=64, h_v=1, d_v=64, K=4, seed=13, slots=1)
+    chain = run_prep(inp, 1, 64, 1, 64, state_index=torch.tensor([0, -1, -1, -1, -1], dtype=torch.int32),
+                     parent=torch.tensor([-1, 0, 1, 2, 3], dtype=torch.int32), gates=False)
+    one_inp = dict(inp, cu_seqlens=torch.tensor([0, sum(lens)], dtype=torch.int32))
+    one = run_prep(one_inp, 1, 64, 1, 64, state_index=torch.tensor([0], dtype=torch.int32), gates=False)
+    for i in range(3):
+        assert torch.equal(chain[i], one[i])
+    assert torch.equal(chain[5][-1], one[5][0])
