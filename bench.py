@@ -93,8 +93,8 @@ def measured_peaks():
 # for the current build only if their hash matches the one it records
 KERNEL_SOURCES = {
     "gdn_tc_kernel": ["gdn_tc.cu", "tc_ptx.cuh", "gdn_internal.cuh"],
-    "gated_rmsnorm_kernel": ["gdn_norm.cu"],
-    "conv_silu_kernel": ["gdn_input_prep.cu"],
+    "gated_rmsnorm_kernel": ["gdn_norm.cu", "gdn_ops.cuh"],
+    "conv_silu_kernel": ["gdn_input_prep.cu", "gdn_ops.cuh"],
 }
 
 

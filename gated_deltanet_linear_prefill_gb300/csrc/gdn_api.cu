@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "gdn_internal.cuh"
+#include "gdn_ops.cuh"
 
 namespace gdn {
 

@@ -22,6 +22,7 @@
 #include <stdint.h>
 
 #include "gdn_internal.cuh"
+#include "gdn_ops.cuh"
 
 namespace gdn {
 namespace {

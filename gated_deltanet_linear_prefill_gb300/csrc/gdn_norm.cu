@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "gdn_internal.cuh"
+#include "gdn_ops.cuh"
 
 namespace gdn {
 namespace {
