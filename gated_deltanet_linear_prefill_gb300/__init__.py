@@ -379,6 +379,8 @@ def input_prep(x, conv_w, cu_seqlens, *, h_qk: int, d_k: int, h_v: int, d_v: int
     N = int(cu_seqlens.numel()) - 1
     K = int(conv_w.shape[1])
     C = int(x.shape[1])
+    if C != 2 * h_qk * d_k + h_v * d_v or tuple(conv_w.shape) != (C, K):
+        raise ValueError("x must have 2 h_qk d_k + h_v d_v channels and conv_w must be [C, K]")
     q = torch.empty((T, h_qk, d_k), dtype=torch.bfloat16, device=dev)
     k = torch.empty((T, h_qk, d_k), dtype=torch.bfloat16, device=dev)
     v = torch.empty((T, h_v, d_v), dtype=torch.bfloat16, device=dev)
@@ -392,8 +394,6 @@ def input_prep(x, conv_w, cu_seqlens, *, h_qk: int, d_k: int, h_v: int, d_v: int
     d.h_qk, d.h_v, d.d_k, d.d_v = h_qk, h_v, d_k, d_v
     d.conv_width = K
     d.num_state_slots = 0 if conv_state is None else int(conv_state.shape[0])
-    if C != 2 * h_qk * d_k + h_v * d_v or tuple(conv_w.shape) != (C, K):
-        raise ValueError("x must have 2 h_qk d_k + h_v d_v channels and conv_w must be [C, K]")
     if parent is None:
         rc = gdn_input_prep(x, conv_w, conv_bias, cu_seqlens, conv_state, state_index, a, b, A_log, dt_bias,
                             q, k, v, g, beta, cs, d, stream)

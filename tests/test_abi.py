@@ -315,3 +315,22 @@ def test_input_prep_tree_host_checks():
     assert call_prep_tree(prep_desc(), parent=15 * MB + 2) == E["GDN_ERR_ALIGN"]
     assert call_prep_tree(prep_desc(), parent=8 * MB + 64) == E["GDN_ERR_ALIAS"]  # parent under q
     assert call_prep_tree(prep_desc()) in (E["GDN_ERR_CUDA"], E["GDN_ERR_ARCH"])
+
+
+def test_wrappers_reject_bad_shapes_before_any_call():
+    # the binding's own checks run before the library is called (CPU tensors are fine)
+    o = torch.zeros(4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gdn.gated_rmsnorm(o, torch.zeros(4, 64, dtype=torch.bfloat16), torch.zeros(128))
+    with pytest.raises(ValueError):
+        gdn.gated_rmsnorm(o, o.clone(), torch.zeros(64))
+    with pytest.raises(ValueError):
+        gdn.gated_rmsnorm(o, o.clone(), torch.zeros(128, dtype=torch.float64))
+    with pytest.raises(ValueError):
+        gdn.gated_rmsnorm(o, o.clone(), torch.zeros(128), out=torch.zeros(4, 128))
+    x = torch.zeros(10, 2 * 1 * 64 + 2 * 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 10], dtype=torch.int32)
+    with pytest.raises(ValueError):  # channels do not match the split
+        gdn.input_prep(x, torch.zeros(256, 4), cu, h_qk=1, d_k=64, h_v=1, d_v=64)
+    with pytest.raises(ValueError):  # taps of the wrong channel count
+        gdn.input_prep(x, torch.zeros(128, 4), cu, h_qk=1, d_k=64, h_v=2, d_v=64)
