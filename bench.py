@@ -129,6 +129,15 @@ def profiled_traffic(kernel_name: str, workload_name: str):
 
 
 # ---------------------------------------------------------------- clocks
+def clocks_path(name: str) -> str:
+    """Where the raw nvidia-smi samples go (the JSON line carries their summary):
+    $GDN_CLOCKS_DIR if set, else the system temporary directory."""
+    import tempfile
+    d = os.environ.get("GDN_CLOCKS_DIR") or tempfile.gettempdir()
+    os.makedirs(d, exist_ok=True)
+    return os.path.join(d, name)
+
+
 class ClockSampler:
     """nvidia-smi sampling during the timed region (200 ms period)."""
 
@@ -309,8 +318,7 @@ def run_gdn(args, world, rank, local):
     # ---- device-resident timing, per-step events on the launching stream. The
     # clock sampler starts one second of untimed steps before the timed region
     # (its 200 ms period needs samples) and stops right after it.
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv"))
+    clocks = ClockSampler(local, clocks_path(f"clocks_rank{rank}.csv"))
     t_soak = time.perf_counter()
     while time.perf_counter() - t_soak < args.soak_s:
         for _ in range(8):
@@ -642,8 +650,7 @@ def run_norm_bench(args):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(device)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(0, os.path.join(ROOT, "gpurun_out", "clocks_norm.csv"))
+    clocks = ClockSampler(0, clocks_path("clocks_norm.csv"))
     t_soak = time.perf_counter()
     while time.perf_counter() - t_soak < args.soak_s:
         for _ in range(32):
@@ -753,8 +760,7 @@ def run_prep_bench(args):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(device)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clocks = ClockSampler(0, os.path.join(ROOT, "gpurun_out", "clocks_prep.csv"))
+    clocks = ClockSampler(0, clocks_path("clocks_prep.csv"))
     t_soak = time.perf_counter()
     while time.perf_counter() - t_soak < args.soak_s:
         for _ in range(32):
