@@ -171,3 +171,19 @@ def test_tree_siblings_share_the_parent_window():
     for b in (5, 7):  # each child run alone after the prefix rows
         ua, _ = oracle.causal_conv_silu(np.concatenate([x[:5], x[b:b + 2]]), w, [0, 7])
         np.testing.assert_allclose(u[b:b + 2], ua[5:], rtol=1e-14, atol=1e-15)
+
+
+def test_recipe_gate_distribution():
+    # the synthetic gate parameters (Mamba2's initial ranges, N(0, 1) projections):
+    # mostly slow decay (median alpha about 0.94), a tenth below about 0.6 and a
+    # tail of strong forgetting, as the input recipe states
+    import workloads
+    inp = workloads.prep_inputs([4000], h_qk=1, d_k=8, h_v=32, d_v=8, seed=3)
+    g, beta = oracle.gate_params(inp["a"].float().numpy(), inp["b"].float().numpy(), inp["A_log"].numpy(),
+                                 inp["dt_bias"].numpy())
+    alpha = np.exp(g)
+    assert 0.0 < alpha.min() and alpha.max() < 1.0
+    assert 0.9 < np.median(alpha) < 0.97
+    assert 0.5 < np.quantile(alpha, 0.1) < 0.7
+    assert alpha.min() < 1e-6
+    assert beta.min() > 0.0 and beta.max() < 1.0

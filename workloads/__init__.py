@@ -319,9 +319,10 @@ def prep_inputs(lengths, *, h_qk: int, d_k: int, h_v: int, d_v: int, K: int = 4,
     U(-1/sqrt(K), 1/sqrt(K)) (the fan-in scale of a K-tap filter) and, if asked,
     a bias [C] ~ U(-0.1, 0.1); the gate projections a, b [T, h_v] bf16 ~ N(0, 1);
     A_log = ln A with A ~ U(1, 16) and dt_bias = ln(e^dt - 1) with dt
-    log-uniform in [1e-3, 1e-1] (Mamba2's initial ranges, so that the gates give
-    decays alpha of about 0.6 to 1); with slots > 0, carried windows [slots, K-1,
-    C] bf16 ~ N(0, 1). Returns a dict of CPU tensors and cu_seqlens."""
+    log-uniform in [1e-3, 1e-1] (Mamba2's initial ranges: the decays alpha have a
+    median near 0.94, a tenth below about 0.6 and a tail of strong forgetting);
+    with slots > 0, carried windows [slots, K-1, C] bf16 ~ N(0, 1). Returns a
+    dict of CPU tensors and cu_seqlens."""
     rng = np.random.default_rng(seed)
     T = int(sum(lengths))
     C = 2 * h_qk * d_k + h_v * d_v
