@@ -334,3 +334,16 @@ def test_wrappers_reject_bad_shapes_before_any_call():
         gdn.input_prep(x, torch.zeros(256, 4), cu, h_qk=1, d_k=64, h_v=1, d_v=64)
     with pytest.raises(ValueError):  # taps of the wrong channel count
         gdn.input_prep(x, torch.zeros(128, 4), cu, h_qk=1, d_k=64, h_v=2, d_v=64)
+
+
+def test_header_is_plain_c_and_cpp():
+    # the boundary is a C ABI: the header must compile as C99 and as C++
+    import shutil
+    import subprocess
+    for cc, lang in (("gcc", "c"), ("g++", "c++")):
+        if not shutil.which(cc):
+            pytest.skip(f"{cc} not found")
+        r = subprocess.run([cc, "-fsyntax-only", "-Wall", "-Wextra", "-Werror", "-x", lang,
+                            *(["-std=c99", "-pedantic"] if lang == "c" else ["-std=c++17"]), HEADER],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
