@@ -270,7 +270,9 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": workloads.CONFIG_NAMES[CONFIG_INDEX], "num_seqs": w.num_seqs,
-                   "total_tokens": w.total_tokens, "h_qk": w.h_qk, "h_v": w.h_v, "d": w.d_k},
+                   "total_tokens": w.total_tokens, "max_seqlen": w.max_seqlen, "h_qk": w.h_qk,
+                   "h_v": w.h_v, "d_k": w.d_k, "d_v": w.d_v, "chunk": 64, "gates": "fp32", "out": "bf16",
+                   "state": "fp32", "parallelism": f"host cores x{threads}"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
