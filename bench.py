@@ -162,25 +162,37 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for name, val in zip(REASON_COLS, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+            return summarize_clock_samples(f)
+
+
+def summarize_clock_samples(lines) -> dict:
+    """The clocks summary of a bench line from nvidia-smi CSV rows (CLOCK_QUERY,
+    no header, no units): the median SM clock over the loaded samples (those at
+    least half the highest), the maximum SM clock, every throttle reason seen
+    Active, and a note when the SM clock stayed below 90% of its maximum with no
+    reason (a clock lock left by someone else)."""
+    sm, mx, reasons = [], [], set()
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for name, val in zip(REASON_COLS, parts[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    loaded = [x for x in sm if x >= 0.5 * max(sm)] or sm
+    out = {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+           "samples": len(sm)}
+    if not reasons and out["sm_mhz"] < 0.9 * out["sm_max_mhz"]:
+        out["note"] = "SM clock below 90% of its maximum with no throttle reason"
+    return out
 
 
 # ---------------------------------------------------------------- oracle timing (CPU)
