@@ -11,6 +11,7 @@ no flush is needed between timed steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
                   [--kernel tc|simt] [--no-cpu-baseline]
+  python bench.py --long | --tree | --latency | --gated-rmsnorm | --input-prep
 
 Prints one JSON line (rank 0). Under torchrun every rank runs its own replica
 batch (seed offset by rank; no collective on the data path) and the line
@@ -411,6 +412,7 @@ def run_gdn(args, world, rank, local):
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": B, "tensor_flops_per_launch": F,
                      "tensor_tflops_achieved": F / step_s / 1e12,
+                     "frac_nominal_8tbs": achieved / 8000.0,
                      "frac_of_roofline_time": roofline_time / step_s},
         "e2e": e2e_line,
         "gpu_launches": launches_per_step * args.steps,
@@ -855,6 +857,181 @@ def run_prep_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def device_layer_inputs(layer: int, device, T=16384, h_qk=16, h_v=32, d=128):
+    """One input set of the 16,384-token workload drawn on the device, with the same
+    distributions as workloads.config(4) (q, k unit rows in bf16; v ~ N(0, 1) bf16;
+    alpha ~ U(0.95, 1), g = log alpha, beta = sigmoid(N(0, 1)), both bf16; initial
+    state ~ N(0, 0.02) fp32), from a torch generator seeded 4 * 1000 + layer. The
+    48-call loop needs 48 distinct sets (about 20 GB); drawing them on the host
+    would take minutes."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(4 * 1000 + int(layer))
+
+    def unit_rows(h):
+        x = torch.randn((T, h, d), generator=gen, device=device, dtype=torch.float32)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    q, k = unit_rows(h_qk), unit_rows(h_qk)
+    v = torch.randn((T, h_v, d), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    alpha = 0.95 + 0.05 * torch.rand((T, h_v), generator=gen, device=device, dtype=torch.float64)
+    g = torch.log(alpha).to(torch.bfloat16)
+    beta = torch.sigmoid(torch.randn((T, h_v), generator=gen, device=device, dtype=torch.float64)).to(torch.bfloat16)
+    init = 0.02 * torch.randn((1, h_v, d, d), generator=gen, device=device, dtype=torch.float32)
+    return q, k, v, g, beta, init
+
+
+def run_long_bench(args):
+    """The long-prompt workload: one 16,384-token prompt, 16 q/k and 32 v heads, head
+    dim 128, bf16 inputs and output, fp32 initial and final state. Times one call
+    (layer 0's inputs, resident) and 48 back-to-back calls, one per linear-attention
+    layer, each on its own input set. One JSON line; value = tokens/s of one call."""
+    import gated_deltanet_linear_prefill_gb300 as gdn
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --long needs a CUDA device")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    gdn.load_library()
+    n_layers = 48
+    w = workloads.config(4, layer=0)
+    T = w.total_tokens
+    stream = torch.cuda.current_stream(device)
+    cu = w.cu_seqlens.to(device)
+    sidx = w.state_index.to(device)
+    layers = [tuple(getattr(w, n).to(device) for n in ("q", "k", "v", "g", "beta", "initial_state"))]
+    for layer in range(1, n_layers):
+        layers.append(device_layer_inputs(layer, device))
+    out = torch.empty((T, w.h_v, w.d_v), dtype=torch.bfloat16, device=device)
+    fs = torch.empty((1, w.h_v, w.d_k, w.d_v), dtype=torch.float32, device=device)
+    q0, _, v0, g0, _, init0 = layers[0]
+    desc = gdn.make_desc(q0, v0, g0, cu, initial_state=init0, out_dtype=torch.bfloat16,
+                         max_seqlen=w.max_seqlen)
+    ws = torch.empty(max(256, gdn.gdn_workspace_bytes(desc)), dtype=torch.uint8, device=device)
+    desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
+
+    def call(i):
+        q, k, v, g, beta, init = layers[i]
+        rc = gdn.gdn_prefill_varlen(q, k, v, g, beta, cu, init, sidx, out, fs, desc, stream)
+        if rc != gdn.GDN_OK:
+            raise gdn.GdnError(rc, "gdn_prefill_varlen")
+
+    for i in range(n_layers):
+        call(i)
+    for _ in range(max(3, args.warmup)):
+        call(0)
+    rc = gdn.gdn_get_device_status(desc, stream)
+    if rc != gdn.GDN_OK:
+        raise gdn.GdnError(rc, "device status")
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(0, clocks_path("clocks_long.csv"))
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        for i in range(n_layers):
+            call(i)
+        torch.cuda.synchronize(device)
+    # one call, layer 0 (inputs 0.27 GB, larger than the L2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        call(0)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    t_one = [a.elapsed_time(b) for a, b in ev]
+    # 48 back-to-back calls, each on its own layer's inputs
+    passes = max(3, args.steps // 4)
+    ev48 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(passes)]
+    for a, b in ev48:
+        a.record(stream)
+        for i in range(n_layers):
+            call(i)
+        b.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    t48 = [a.elapsed_time(b) for a, b in ev48]
+    ms_one = statistics.median(t_one)
+    ms_48 = statistics.median(t48)
+
+    e2e_line = None
+    if not args.no_e2e:
+        names = ("q", "k", "v", "g", "beta", "initial_state", "state_index", "cu_seqlens")
+        host_in = {n: getattr(w, n).pin_memory() for n in names}
+        dev_in = {n: torch.empty_like(t, device=device) for n, t in host_in.items()}
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        host_fs = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = host_out.numel() * host_out.element_size() + host_fs.numel() * host_fs.element_size()
+
+        def e2e_call():
+            for n, t in host_in.items():
+                dev_in[n].copy_(t, non_blocking=True)
+            rc = gdn.gdn_prefill_varlen(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"],
+                                        dev_in["cu_seqlens"], dev_in["initial_state"], dev_in["state_index"],
+                                        out, fs, desc, stream)
+            if rc != gdn.GDN_OK:
+                raise gdn.GdnError(rc, "gdn_prefill_varlen")
+            host_out.copy_(out, non_blocking=True)
+            host_fs.copy_(fs, non_blocking=True)
+
+        for _ in range(2):
+            e2e_call()
+        torch.cuda.synchronize(device)
+        n_e2e = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_call()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_line = {"value": T * n_e2e / (e0.elapsed_time(e1) / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
+    B = algorithmic_bytes(w)
+    F = chunked_tensor_flops(w)
+    s_one = ms_one / 1e3
+    achieved = B / s_one / 1e9
+    roofline_time = max(B / (hbm_peak * 1e9), F / (tc_peak * 1e12))
+    line = {
+        "metric": METRIC, "value": T / s_one, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_one, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "cfg4_long_T16384", "num_seqs": 1, "total_tokens": T, "h_qk": w.h_qk,
+                   "h_v": w.h_v, "d_k": w.d_k, "d_v": w.d_v, "chunk": 64, "gates": "bf16", "out": "bf16",
+                   "state": "fp32 (initial state gathered)", "kernel": "tc",
+                   "l2_flush": "none needed: one call's inputs (%.2f GB) exceed the 129 MB L2" % (
+                       (B - 2 * w.h_v * w.d_k * w.d_v * 4) / 1e9),
+                   "layers": n_layers,
+                   "layer_inputs": "layer 0 drawn on the host (the parity case); layers 1-47 drawn on "
+                                   "the device with the same distributions"},
+        "layers48": {"ms_per_48_calls": ms_48, "ms_per_call": ms_48 / n_layers,
+                     "tokens_per_s": n_layers * T / (ms_48 / 1e3), "passes": passes},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "frac_nominal_8tbs": achieved / 8000.0,
+                     "algorithmic_bytes_per_launch": B, "tensor_flops_per_launch": F,
+                     "tensor_tflops_achieved": F / s_one / 1e12,
+                     "frac_of_roofline_time": roofline_time / s_one,
+                     "note": "32 (sequence, value head) chains on 152 SMs: bound by the chain "
+                             "length (256 chunks), not by bandwidth"},
+        "e2e": e2e_line,
+        "gpu_launches": 2 * (args.steps + passes * n_layers),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.default_threads()
+        t0 = time.perf_counter()
+        oracle.run_workload(w, n_threads=threads)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {
+            "value": T / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"one call (layer 0: {T} tokens, all {w.h_v} heads), fp64 recurrence, {dt:.1f} s",
+            "s_per_48_calls": 48 * dt, "s_per_48_calls_kind": "the one-call time x 48"}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -876,7 +1053,12 @@ def main(argv=None):
                     help="time the gated RMSNorm on the 74-prompt batch's output shape")
     ap.add_argument("--input-prep", action="store_true",
                     help="time the GDN input prep (conv + SiLU + split, gates) on the 74-prompt batch")
+    ap.add_argument("--long", action="store_true",
+                    help="time one 16,384-token prompt: one call and 48 back-to-back calls (48 layers)")
     args = ap.parse_args(argv)
+    if args.long:
+        run_long_bench(args)
+        return
     if args.input_prep:
         run_prep_bench(args)
         return

@@ -81,16 +81,16 @@ constexpr uint32_t kTmemCols = 512;
 enum {
   B_FULL0 = 0, B_FULL1, B_FULL2,  // chunk K/Q tiles + gate scalars landed (slot c % 3)
   B_VFULL0, B_VFULL1,             // chunk V tile landed (slot c % 2)
-  B_KQE0, B_KQE1, B_KQE2,         // K/Q slot released (chunk c's last MMA done)
+  B_KQE0, B_KQE1, B_KQE2,         // K/Q slot released (chunk c's output staged out)
   B_VE0, B_VE1,                   // V slot released (slot c % 2)
   B_RQ0, B_RQ1, B_RQ2,            // q norms of slot c % 3 written
   B_KQ_DONE, B_KQ_FREE, B_W_DONE, B_R_FREE, B_W_FREE,
   B_WCONV0, B_WCONV1,             // W'^T of chunk c converted to bf16 (c % 2)
   B_P1_DONE0, B_P1_DONE1,         // chunk prepared (c % 2)
   B_T_READY0, B_T_READY1,         // T_b / T_w of chunk c written (c % 2)
-  B_U_DONE, B_S_READY, B_UP_DONE, B_WFREE0, B_WFREE1, B_UOPS_READY, B_STATE_DONE, B_O_DONE, B_EPI_DONE,
+  B_U_DONE, B_S_READY, B_UP_DONE, B_UOPS_READY, B_STATE_DONE, B_O_DONE, B_EPI_DONE,
   B_MFREE0, B_MFREE1, B_CSF0, B_CSF1, B_CSF2,
-  B_DRAIN1, B_DRAIN2, kNumBars
+  B_DRAIN1, B_DRAIN2, B_DRAIN3, kNumBars
 };
 static_assert(kNumBars <= 127, "barrier indices fit the seven bits of a wait-list entry");
 
@@ -118,7 +118,7 @@ constexpr int F_SLAST = 8;     // last chunk this CTA processes
 
 // Per-chunk values WG-A hands to WG-B (three buffers, chunk % 3).
 struct ChunkScalars {
-  float co[64];  // scale r^q_i e^{G_i - G_m} lambda: output weight of row i (0 past m)
+  float co[64];  // scale e^{G_i - G_m} lambda: output weight of row i without r^q_i (0 past m)
   long long t0;  // first row of the chunk
   float mu_next; // mu after the chunk
   int m;         // rows
@@ -147,22 +147,26 @@ struct TcLayout {
   static constexpr uint32_t SLOT_BYTES = KQ_BYTES + SCAL_BYTES;
   static constexpr uint32_t V_BYTES = NVA * 8192u;
   static constexpr uint32_t SCR_BYTES = 17408u;           // 64 x 68 fp32, 1024-aligned size
-  static constexpr uint32_t RING0 = 0;                     // K/Q slots x3
+  static constexpr uint32_t WP_BYTES = DK * 64u * 4u;      // W' fp32 [64 rows j][DK], K-major
+  // K/Q slots x3; once a chunk's products have read its K/Q tiles, the first 16 KB of
+  // its slot stage that chunk's output tiles
+  static constexpr uint32_t RING0 = 0;
   static constexpr uint32_t V0 = 3 * SLOT_BYTES;           // V slots x2
   static constexpr uint32_t M0 = V0 + 2 * V_BYTES;         // M (bf16 64x64) x2
-  static constexpr uint32_t STG = M0 + 2 * 8192u;          // output staging, two tiles
-  static constexpr uint32_t TB = STG + 2 * 8192u;          // fp32 T, then T_b hi / lo
+  static constexpr uint32_t TB = M0 + 2 * 8192u;           // fp32 T, then T_b hi / lo
   static constexpr uint32_t TW = TB + SCR_BYTES;           // T_w bf16
-  static constexpr uint32_t WT0 = TW + 8192u;              // fp32 A, then W'^T bf16, x2
+  static constexpr uint32_t AS = TW + 8192u;               // fp32 A (WG-A's own chunk only)
+  static constexpr uint32_t WP = AS + SCR_BYTES;           // W' fp32 (one chunk at a time)
   static constexpr bool NEED_ZERO = (DK == 64) || (DV == 64);
-  static constexpr uint32_t ZERO = WT0 + 2 * SCR_BYTES;   // 8 KB of zeros (M padding)
+  static constexpr uint32_t ZERO = WP + WP_BYTES;          // 8 KB of zeros (M padding)
   static constexpr uint32_t CS0 = ZERO + (NEED_ZERO ? 8192u : 0u);
   static constexpr uint32_t PS = CS0 + 3 * (uint32_t)sizeof(ChunkScalars);
   static constexpr uint32_t BARS = PS + (uint32_t)sizeof(PrepScalars);
   static constexpr uint32_t MISC = BARS + kNumBars * 8u;  // tmem base, abort flag
   static constexpr uint32_t TOTAL = MISC + 64u;
   static constexpr uint32_t DYN_SMEM = TOTAL + 1024u;     // alignment slack
-  static_assert(SLOT_BYTES % 1024 == 0, "slot alignment");
+  static_assert(SLOT_BYTES % 1024 == 0 && WP_BYTES % 1024 == 0, "slot alignment");
+  static_assert(KQ_BYTES >= 16384u, "a K/Q slot holds a chunk's output staging tiles");
   static_assert(sizeof(ChunkScalars) % 16 == 0, "chunk scalars alignment");
   static_assert(DYN_SMEM <= 232448u, "shared memory budget");
 };
@@ -592,34 +596,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) drain_loads(sbase + L::BARS, kq_issued, v_issued, sbase + L::MISC);
   } else if (warp == 1) {
     // ================================================================ state-independent MMAs
-    // [K;Q] K^T of chunk c+1 as soon as its tiles are in and WG-A has read chunk c's;
-    // then W'^T = K^T T_w^T and U^T = V^T T_b^T of chunk c once WG-A has written T_b / T_w.
+    // W'^T = K^T T_w^T and U^T = V^T T_b^T of chunk c once WG-A has written T_b / T_w
+    // (warp 3 issues the chunks' [K;Q] K^T, so these never wait for later tiles).
     if (lane == 0 && any) {
-      constexpr uint32_t id_kq = idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
-      auto issue_kq = [&](int c) {
-        const uint64_t dkq = sdesc(slot_kq(c), 16, 1024);
 #pragma unroll 1
-        for (int kk = 0; kk < 4 * L::NKA; ++kk) {
-          const uint64_t d = sdesc_add(dkq, (kk >> 2) * 16384u + (kk & 3) * 32u);
-          mma_ss(tmem + TM_KQ, d, d, id_kq, kk != 0);
-        }
-        mma_commit(&bars[B_KQ_DONE]);
-      };
-      bool run = wait(B_FULL0, 0, 2);
-      if (run) {
-        tc_fence_after();
-        issue_kq(0);
-      }
-#pragma unroll 1
-      for (int c = 0; run; ++c) {
+      for (int c = 0;; ++c) {
         const int par = c & 1;
-        const bool last = sc_int(slot_sc(c), SC_FLAGS) & F_SLAST;
-        if (!last) {
-          if (!wait_all(with(with(kNone, B_FULL0 + (c + 1) % 3, ((c + 1) / 3) & 1), B_KQ_FREE, c & 1), 2)) break;
-          tc_fence_after();
-          issue_kq(c + 1);
-        }
         // R and the W' accumulator were read by WG-B for chunk c-1
         uint64_t wl = with(kNone, B_T_READY0 + par, (c >> 1) & 1);
         if (c >= 1) wl = with(with(wl, B_R_FREE, (c - 1) & 1), B_W_FREE, (c - 1) & 1);
@@ -642,7 +625,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  id_w, kk != 0);
         mma_commit(&bars[B_U_DONE]);
         mma_commit(&bars[B_VE0 + par]);
-        if (last) break;
+        if (sc_int(slot_sc(c), SC_FLAGS) & F_SLAST) break;
       }
       mma_commit(&bars[B_DRAIN1]);  // every MMA this thread issued has finished before exit
       wait(B_DRAIN1, 0, kDrainWait);
@@ -650,31 +633,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 2) {
     // ================================================================ state-dependent MMAs
     if (lane == 0 && any) {
-      constexpr uint32_t id_sw = idesc_bf16(128, 64, 0, 1);
+      constexpr uint32_t id_sw = idesc_tf32(128, 64);
       constexpr uint32_t id_qs = idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t id_st = idesc_bf16(128, DK, 0, 1);
       constexpr uint32_t id_pu = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
       for (int c = 0;; ++c) {
         const int par = c & 1;
-        if (!wait_all(with(with(with(with(kNone, B_P1_DONE0 + par, (c >> 1) & 1), B_WCONV0 + par, (c >> 1) & 1),
-                                 B_U_DONE, c & 1), B_S_READY, c & 1), 4)) {
+        if (!wait_all(with(with(with(kNone, B_P1_DONE0 + par, (c >> 1) & 1), B_WCONV0 + par, (c >> 1) & 1),
+                           B_U_DONE, c & 1), 4)) {
           break;
         }
+        // U' reads the fp32 state itself: it needs chunk c-1's state update, or, when the
+        // state starts over or is rescaled before this chunk, WG-B's write of it
+        const int fl = sc_int(slot_sc(c), SC_FLAGS);
+        const bool s_written = (fl & (F_UFIRST | F_EAGER)) != 0;
+        if (!(s_written ? wait(B_S_READY, c & 1, 4) : wait(B_STATE_DONE, (c - 1) & 1, 4))) break;
         tc_fence_after();
         const bool last = cscal[c % 3].slast;  // read now: the buffer is reused after this chunk
         const uint32_t kq = slot_kq(c);
-        // U'^T += S~^T W'^T : A = S~^T (bf16, TMEM), B = W'^T MN-major [d_k][j]
-        const uint64_t dwt = sdesc(sbase + L::WT0 + par * L::SCR_BYTES, 16, 1024);
+        // U'^T += S~^T W'^T in tf32: A = S~^T (fp32, TMEM), B = W' fp32 K-major [j][d_k]
+        const uint64_t dwt = sdesc(sbase + L::WP, 16, 1024);
 #pragma unroll 1
-        for (int kk = 0; kk < 4 * L::NKA; ++kk)
-          mma_ts(tmem + TM_R, tmem + TM_SB + kk * 8u, sdesc_add(dwt, kk * 2048u), id_sw, 1);
+        for (int kk = 0; kk < DK / 8; ++kk)
+          mma_ts_tf32(tmem + TM_R, tmem + TM_S + kk * 8u, sdesc_add(dwt, (kk >> 2) * 8192u + (kk & 3) * 32u), id_sw, 1);
         mma_commit(&bars[B_UP_DONE]);
-        mma_commit(&bars[B_WFREE0 + par]);
-        // O^T = S~^T Q^T (raw q tile, K-major), once the last epilogue has read O
-        if (c >= 1 && !wait(B_EPI_DONE, (c - 1) & 1, 4)) {
-          break;
-        }
+        // O^T = S~^T Q^T (raw q tile, K-major) from the bf16 copy of the state, once the
+        // last epilogue has read O
+        uint64_t ol = with(kNone, B_S_READY, c & 1);
+        if (c >= 1) ol = with(ol, B_EPI_DONE, (c - 1) & 1);
+        if (!wait_all(ol, 4)) break;
         tc_fence_after();
         const uint64_t dq = sdesc(kq + 8192u, 16, 1024);
 #pragma unroll 1
@@ -698,7 +686,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kk = 0; kk < 4; ++kk)
           mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, kk * 32u), id_pu, 1);
         mma_commit(&bars[B_O_DONE]);
-        mma_commit(&bars[B_KQE0 + c % 3]);
         mma_commit(&bars[B_MFREE0 + par]);
         if (last) break;
       }
@@ -707,17 +694,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 3) {
     // ================================================================ q norms
-    // r^q_i from the diagonal of Q Q^T, 16 rows at a time on the warp-level tensor
-    // cores (bf16 products are exact in fp32), straight from the swizzled tile and
-    // off the path of the chunk preparation (r^q only weights the output rows).
+    // Lane 0 issues [K;Q] K^T of each chunk (tcgen05) as soon as its tiles are in and
+    // WG-A has read the previous chunk's. Then r^q_i from the diagonal of Q Q^T, 16 rows
+    // at a time on the warp-level tensor cores (bf16 products are exact in fp32), straight
+    // from the swizzled tile and off the path of the chunk preparation (r^q only weights
+    // the output rows).
     if (any) {
       const int g = lane >> 2, t = lane & 3;
       // ldmatrix rows: matrices 0 / 1 are rows 0-7 / 8-15 of k 0-7, 2 / 3 the same of k 8-15
       const uint32_t lr = (uint32_t)((lane & 7) + 8 * ((lane >> 3) & 1)), lk = (uint32_t)(lane >> 4);
+      constexpr uint32_t id_kq = idesc_bf16(128, 64, 0, 0);
 #pragma unroll 1
       for (int c = 0;; ++c) {
         bool ok = true;
-        if (lane == 0) ok = wait(B_FULL0 + c % 3, (c / 3) & 1, 14);
+        if (lane == 0) {
+          ok = wait(B_FULL0 + c % 3, (c / 3) & 1, 14) && (c == 0 || wait(B_KQ_FREE, (c - 1) & 1, 14));
+          if (ok) {
+            tc_fence_after();
+            const uint64_t dkq = sdesc(slot_kq(c), 16, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < 4 * L::NKA; ++kk) {
+              const uint64_t d = sdesc_add(dkq, (kk >> 2) * 16384u + (kk & 3) * 32u);
+              mma_ss(tmem + TM_KQ, d, d, id_kq, kk != 0);
+            }
+            mma_commit(&bars[B_KQ_DONE]);
+          }
+        }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         float* sc = slot_sc(c);
@@ -743,6 +745,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) mbar_arrive(&bars[B_RQ0 + c % 3]);
         if (sc_int(sc, SC_FLAGS) & F_SLAST) break;
       }
+      if (lane == 0) {  // every MMA this thread issued has finished before exit
+        mma_commit(&bars[B_DRAIN3]);
+        wait(B_DRAIN3, 0, kDrainWait);
+      }
     }
   } else if (warp < 12) {
     // ================================================================ WG-A: chunk preparation
@@ -756,11 +762,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
       for (int c = 0;; ++c) {
         const int par = c & 1;
-        // the chunk's tiles, q norms and [K;Q] K^T; M, W'^T / A and the chunk scalars of this
-        // parity released by chunk c-2 / c-3
-        uint64_t wl = with(with(with(kNone, B_FULL0 + c % 3, (c / 3) & 1), B_RQ0 + c % 3, (c / 3) & 1),
-                           B_KQ_DONE, c & 1);
-        if (c >= 2) wl = with(with(wl, B_MFREE0 + par, ((c >> 1) + 1) & 1), B_WFREE0 + par, ((c >> 1) + 1) & 1);
+        // the chunk's tiles and [K;Q] K^T; M, W'^T / A and the chunk scalars of this parity
+        // released by chunk c-2 / c-3 (the q norms only weight the output rows: the
+        // epilogue applies them)
+        uint64_t wl = with(with(kNone, B_FULL0 + c % 3, (c / 3) & 1), B_KQ_DONE, c & 1);
+        if (c >= 2) wl = with(wl, B_MFREE0 + par, ((c >> 1) + 1) & 1);
         if (c >= 3) wl = with(wl, B_CSF0 + c % 3, ((c / 3) + 1) & 1);
         bool ok = wait_all(wl, 8);
         if (named_bar_or(1, 256, !ok || *abort_flag)) break;
@@ -775,7 +781,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld32(tmem + lane_off + TM_KQ + 32 * hf, v);
         tmem_ld_wait();
         tc_fence_before();
-        float* Abuf = reinterpret_cast<float*>(sm + L::WT0 + par * L::SCR_BYTES);
+        float* Abuf = reinterpret_cast<float*>(sm + L::AS);
         float* Tbuf = reinterpret_cast<float*>(sm + L::TB);
         if (krow && (i >> 5) == hf) {
           // r^k_i from the diagonal of K K^T (fp32 sum of exact bf16 products), then the
@@ -794,7 +800,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ps->s[i] = live ? ri * exp2f((Gm - Gi - lamlog) * kLog2e) : 0.f;
         } else if (!krow && hf == 0) {
           // output weights
-          cs.co[i] = i < m ? p.scale * sc[SC_RQ + i] * exp2f((Gi - Gm + lamlog) * kLog2e) : 0.f;
+          cs.co[i] = i < m ? p.scale * exp2f((Gi - Gm + lamlog) * kLog2e) : 0.f;
           if (i == 0) {
             cs.t0 = *reinterpret_cast<const long long*>(&sc[SC_T0]);
             cs.mu_next = sc[SC_MUNEXT];
@@ -961,12 +967,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int pieces = (int)(DV * osz / 16);  // 16-byte pieces of one output row
     const int pshift = __ffs(pieces) - 1;
     uint32_t npass = 0;  // epilogue passes so far (selects the staging tile)
+    // The K/Q slot whose staged output tiles a tensor store may still be reading (thread
+    // 0 of the group issued the store): it goes back to the producer at the next wait
+    // for a U' product, where the group waits anyway.
+    int slot_pending = -1;
+    auto release_slot = [&]() {
+      if (wb == 0 && slot_pending >= 0) {
+        bulk_wait_read();
+        mbar_arrive(&bars[B_KQE0 + slot_pending % 3]);
+      }
+      slot_pending = -1;
+    };
 #pragma unroll 1
     for (int c = -1;; ++c) {
       bool more = any && c < 0;
       if (c >= 0) {
         // ---- (U' diag(s/lambda))^T -> bf16 hi / lo A operands
         const ChunkScalars& cs = cscal[c % 3];
+        release_slot();
         bool ok = wait_all(with(with(kNone, B_P1_DONE0 + (c & 1), (c >> 1) & 1), B_UP_DONE, c & 1), 12);
         if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
@@ -996,6 +1014,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         un_c = cs.n;
         uh_c = cs.h;
         mu_c = cs.mu_next;
+      }
+      if (more) {
+        // ---- W'^T of chunk c+1: TMEM -> fp32 K-major [j][d_k] with the 128-byte swizzle
+        // (32 fp32 per row of an atom), the B operand of warp 2's tf32 U' product. Right
+        // after the split: it does not depend on the state, and the U' product of chunk
+        // c+1 needs it as soon as chunk c's state update is done. Thread d_k writes column
+        // d_k of every row j: a warp fills one 128-byte atom row per store, in 32 banks.
+        const int cn = c + 1, pn = cn & 1;
+        bool ok = wait(B_W_DONE, cn & 1, 15);
+        if (named_bar_or(2, 128, !ok || *abort_flag)) break;
+        tc_fence_after();
+        // (chunk c's U' product, the buffer's last reader, finished before the split above)
+        const uint32_t wcol = sbase + L::WP + (uint32_t)(wb >> 5) * 8192u + (uint32_t)(wb & 3) * 4u;
+        const uint32_t wch = (uint32_t)((wb >> 2) & 7);  // 16-byte chunk of the row before the swizzle
+#pragma unroll 1
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t w[32];
+          tmem_ld32(tmem + lane_off + TM_W + 32 * hb, w);
+          tmem_ld_wait();
+          if (wb < DK) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              asm volatile("st.shared.b32 [%0], %1;" ::"r"(wcol + (uint32_t)(32 * hb + x) * 128u +
+                                                            ((wch ^ (uint32_t)(x & 7)) << 4)),
+                           "r"(w[x])
+                           : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(2, 128);
+        if (wb == 0) {
+          mbar_arrive(&bars[B_W_FREE]);
+          mbar_arrive(&bars[B_WCONV0 + pn]);
+        }
       }
       if (more || c >= 0) {
         // ---- S~ -> bf16 A operand for chunk c+1 (first applying its decay when eager).
@@ -1039,57 +1092,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_bar_sync(2, 128);
         if (wb == 0) mbar_arrive(&bars[B_S_READY]);
       }
-      if (more) {
-        // ---- W'^T of chunk c+1: TMEM -> bf16 MN-major [d_k][j] (over its A scratch), for
-        // warp 2's U' product, ahead of chunk c's epilogue so that the U' product of
-        // chunk c+1 runs while the outputs of chunk c are written
-        const int cn = c + 1, pn = cn & 1;
-        bool ok = wait(B_W_DONE, cn & 1, 15);
-        if (named_bar_or(2, 128, !ok || *abort_flag)) break;
-        tc_fence_after();
-        const uint32_t wt = sbase + L::WT0 + pn * L::SCR_BYTES;
-#pragma unroll 1
-        for (int hb = 0; hb < 2; ++hb) {
-          uint32_t w[32];
-          tmem_ld32(tmem + lane_off + TM_W + 32 * hb, w);
-          tmem_ld_wait();
-          if (wb < DK) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_shared_v4(wt + sw128(wb, 4 * hb + q),
-                           pack_bf16(__uint_as_float(w[8 * q + 0]), __uint_as_float(w[8 * q + 1])),
-                           pack_bf16(__uint_as_float(w[8 * q + 2]), __uint_as_float(w[8 * q + 3])),
-                           pack_bf16(__uint_as_float(w[8 * q + 4]), __uint_as_float(w[8 * q + 5])),
-                           pack_bf16(__uint_as_float(w[8 * q + 6]), __uint_as_float(w[8 * q + 7])));
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(2, 128);
-        if (wb == 0) {
-          mbar_arrive(&bars[B_W_FREE]);
-          mbar_arrive(&bars[B_WCONV0 + pn]);
-        }
-      }
       if (c >= 0) {
         // ---- epilogue: out_i = co_i O^T_i, staged in shared memory and written by tensor
         // stores. bf16: the whole chunk at once, as two 64-column tiles of 64 rows (128-byte
         // swizzle), one store each; fp32: passes of 16 rows alternating between two tiles.
         // A chunk (or pass) shorter than the tile is copied out row by row instead, since a
-        // store of the full tile would run into the next sequence's rows.
+        // store of the full tile would run into the next sequence's rows. The tiles sit in
+        // the chunk's own K/Q slot: once O is complete, every product that reads the chunk's
+        // K and Q tiles has finished; the slot goes back to the producer when the stores
+        // have read the tiles.
+        // The q norms of the chunk (warp 3) complete the row weights here; once they are
+        // written, warp 3 has also finished reading the chunk's Q tile.
         const ChunkScalars& cs = cscal[c % 3];
-        bool ok = wait(B_O_DONE, c & 1, 13);
-        if (wb == 0) bulk_wait_read();  // the staging tiles are free again
+        bool ok = wait_all(with(with(kNone, B_O_DONE, c & 1), B_RQ0 + c % 3, (c / 3) & 1), 13);
         if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
         const int m = cs.m;
         const long long t0 = cs.t0;
+        const uint32_t stg = slot_kq(c);
+        const float* rq = slot_sc(c) + SC_RQ;
         if constexpr (!OF32) {
           // each thread takes consecutive row pairs of its 16-lane blocks (16 x 256b loads)
           // and writes 8x8 blocks transposed into the row-major tiles (the eight rows of a
           // block hit distinct banks under the swizzle); a tile row is 32 half + lane
           const int qd = wb >> 5, t = lane & 3;
-          const uint32_t tile = sbase + L::STG + (uint32_t)(qd >> 1) * 8192u;
+          const uint32_t tile = stg + (uint32_t)(qd >> 1) * 8192u;
 #pragma unroll 1
           for (int half = 0; half < 2 && 32 * half < m; ++half) {
             const int p0 = 32 * half;
@@ -1100,7 +1127,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (32 * qd < DV) {
               float2 co2[4];
 #pragma unroll
-              for (int r = 0; r < 4; ++r) co2[r] = *reinterpret_cast<const float2*>(&cs.co[p0 + 8 * r + 2 * t]);
+              for (int r = 0; r < 4; ++r)
+                co2[r] = __fmul2_rn(*reinterpret_cast<const float2*>(&cs.co[p0 + 8 * r + 2 * t]),
+                                    *reinterpret_cast<const float2*>(&rq[p0 + 8 * r + 2 * t]));
 #pragma unroll
               for (int hs = 0; hs < 4; ++hs) {  // lane half (hs >> 1) and 8-lane block (hs & 1)
                 const uint32_t* x = (hs >> 1) ? b : a;
@@ -1126,22 +1155,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (wb == 0) {
 #pragma unroll
               for (int tl = 0; tl < DV / 64; ++tl)
-                tma_store_3d(&tm.o, sm + L::STG + tl * 8192, 64 * tl, cs.h, (int)t0);
+                tma_store_3d(&tm.o, sm + (stg - sbase) + tl * 8192, 64 * tl, cs.h, (int)t0);
               bulk_commit();
             }
+            slot_pending = c;
           } else {
             for (int idx = wb; idx < (m << pshift); idx += 128) {
               const int r = idx >> pshift, pc = idx & (pieces - 1);
               const uint4 x = *reinterpret_cast<const uint4*>(
-                  sm + L::STG + (pc >> 3) * 8192 + sw128((uint32_t)r, (uint32_t)(pc & 7)));
+                  sm + (stg - sbase) + (pc >> 3) * 8192 + sw128((uint32_t)r, (uint32_t)(pc & 7)));
               char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + r) * p.h_v + cs.h) * DV) * osz;
               *reinterpret_cast<uint4*>(dst + pc * 16) = x;
             }
+            named_bar_sync(2, 128);  // every thread has read the tiles
+            if (wb == 0) mbar_arrive(&bars[B_KQE0 + c % 3]);
           }
         } else {
 #pragma unroll 1
           for (int p0 = 0; p0 < m; p0 += 16, ++npass) {
-            uint8_t* stage = sm + L::STG + (npass & 1) * 8192u;
+            uint8_t* stage = sm + (stg - sbase) + (npass & 1) * 8192u;
             // the store that last used this tile has read it (one store group per pass)
             if (wb == 0) bulk_wait_read_1();
             named_bar_sync(2, 128);
@@ -1151,7 +1183,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (live) {
 #pragma unroll
               for (int t4 = 0; t4 < 4; ++t4) {
-                const float4 c4 = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
+                const float4 c4w = *reinterpret_cast<const float4*>(&cs.co[p0 + 4 * t4]);
+                const float4 r4 = *reinterpret_cast<const float4*>(&rq[p0 + 4 * t4]);
+                const float4 c4 = make_float4(c4w.x * r4.x, c4w.y * r4.y, c4w.z * r4.z, c4w.w * r4.w);
                 float* st = reinterpret_cast<float*>(stage) + (4 * t4) * DV + wb;
                 st[0] = c4.x * __uint_as_float(oa[4 * t4]);
                 st[DV] = c4.y * __uint_as_float(oa[4 * t4 + 1]);
@@ -1180,10 +1214,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(&bars[B_EPI_DONE]);
             mbar_arrive(&bars[B_CSF0 + c % 3]);
           }
+          slot_pending = c;  // released once the stores have read the tiles
         }
       }
       if (!more) break;
     }
+    release_slot();
     if (wb == 0) bulk_wait_all();
   }
   tc_fence_before();

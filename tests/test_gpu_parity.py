@@ -1,9 +1,9 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle.
 
-Small cases are compared element by element over every output; the
-full-size workloads (74 packed prompts; one 16,384-token prompt) run on the
-GPU exactly as the bench launches them and are compared on a sample of
-sequences / heads that the oracle computes one by one.
+Every case is compared element by element over every output, the full-size
+workloads (74 packed prompts; one 16,384-token prompt) included: they run on
+the GPU exactly as the bench launches them, and the oracle computes the whole
+batch (a few seconds on the host cores).
 """
 import numpy as np
 import pytest
@@ -35,28 +35,24 @@ def test_config1_single_prompt(kernel):
     check(errors(o, s, o_ref, s_ref), kernel, label="cfg1")
 
 
-def _sample_seqs(w, k=6, seed=0):
-    lens = w.lengths
-    order = np.argsort(-lens, kind="stable")
-    rng = np.random.default_rng(seed)
-    pick = {int(order[0]), int(order[-1])}
-    pick.update(int(x) for x in rng.choice(len(lens), size=k, replace=False))
-    return sorted(pick)[:k + 2]
+_ORACLE_CACHE = {}
+
+
+def _oracle_whole(key, w):
+    """The oracle over a whole workload, computed once per test session."""
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = oracle.run_workload(w)
+    return _ORACLE_CACHE[key]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_config2_varlen_full_size_sampled(kernel):
-    """74 packed prompts at full size; the oracle checks a sample of sequences
-    (the longest, the shortest and random ones) over every head."""
+def test_config2_varlen_full_size_every_sequence(kernel):
+    """74 packed prompts at full size, every output element and final state
+    against the oracle (all 74 sequences x 32 heads)."""
     w = workloads.config(2)
     o, s = run_lib(w, kernel)
-    seqs = _sample_seqs(w)
-    sub = workloads.subset_sequences(w, seqs)
-    o_ref, s_ref = oracle.run_workload(sub)
-    cu = w.cu_seqlens.numpy()
-    rows = np.concatenate([np.arange(cu[n], cu[n + 1]) for n in seqs])
-    check(errors(o[rows], s[seqs], o_ref, s_ref), kernel, label="cfg2")
-    assert not np.isnan(o).any() and not np.isnan(s).any()
+    o_ref, s_ref = _oracle_whole("cfg2", w)
+    check(errors(o, s, o_ref, s_ref), kernel, label="cfg2")
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -91,18 +87,13 @@ def test_config3_prefix_tree_fork(kernel):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("layer", [0, 47])
-def test_config4_long_prompt_sampled_heads(kernel, layer):
+def test_config4_long_prompt_every_head(kernel, layer):
     """One 16,384-token prompt with a non-zero initial state (layers 0 and 47
-    of the 48 input sets); the oracle checks 4 of the 32 value heads."""
+    of the 48 input sets), every head against the oracle."""
     w = workloads.config(4, layer=layer)
     o, s = run_lib(w, kernel)
-    heads = [0, 9, 22, 31]
-    mask = np.zeros((1, 32), np.uint8)
-    mask[0, heads] = 1
-    o_ref, s_ref = oracle.run_workload(w, unit_mask=mask)
-    check(errors(o[:, heads], s[:, heads], o_ref[:, heads], s_ref[:, heads]), kernel,
-          label=f"cfg4 layer {layer}")
-    assert not np.isnan(o).any() and not np.isnan(s).any()
+    o_ref, s_ref = _oracle_whole(f"cfg4-{layer}", w)
+    check(errors(o, s, o_ref, s_ref), kernel, label=f"cfg4 layer {layer}")
 
 
 EDGE_LENGTHS = [0, 1, 63, 64, 65, 127, 128, 129, 0, 200, 2]
