@@ -345,13 +345,8 @@ __device__ __noinline__ float3 span_fit(float s0, float s1, int m, int lane) {
 #pragma unroll 1
   for (;;) {
     m = (m + 1) >> 1;
-    float wmax = fmaxf(lane < m ? s0 : -3.0e38f, lane + 32 < m ? s1 : -3.0e38f);
-    float wmin = fminf(lane < m ? s0 : 3.0e38f, lane + 32 < m ? s1 : 3.0e38f);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-      wmin = fminf(wmin, __shfl_xor_sync(0xffffffffu, wmin, o));
-    }
+    const float wmax = warp_max(fmaxf(lane < m ? s0 : -3.0e38f, lane + 32 < m ? s1 : -3.0e38f));
+    const float wmin = warp_min(fminf(lane < m ? s0 : 3.0e38f, lane + 32 < m ? s1 : 3.0e38f));
     if (m <= 1 || fmaxf(wmax, 0.f) - fminf(wmin, 0.f) <= kMaxSpan) return make_float3(__int_as_float(m), wmax, wmin);
   }
 }
@@ -472,30 +467,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int64_t len = eos - bos;  // 0: one chunk of no rows carries the unit's state through
       int64_t start = 0;
       float logmu = 0.f;
-      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-      auto load_gates = [&](int64_t st) {
-        const int64_t avail = len - st;
-        const int64_t i0 = (bos + st + lane) * p.h_v + h, i1 = i0 + 32 * (int64_t)p.h_v;
-        const bool in0 = lane < avail, in1 = lane + 32 < avail;
-        if constexpr (GF32) {
-          const float* gg = reinterpret_cast<const float*>(p.g);
-          const float* bb = reinterpret_cast<const float*>(p.beta);
-          g0 = in0 ? gg[i0] : 0.f;
-          b0 = in0 ? bb[i0] : 0.f;
-          g1 = in1 ? gg[i1] : 0.f;
-          b1 = in1 ? bb[i1] : 0.f;
-        } else {
-          const __nv_bfloat16* gg = reinterpret_cast<const __nv_bfloat16*>(p.g);
-          const __nv_bfloat16* bb = reinterpret_cast<const __nv_bfloat16*>(p.beta);
-          g0 = in0 ? __bfloat162float(gg[i0]) : 0.f;
-          b0 = in0 ? __bfloat162float(bb[i0]) : 0.f;
-          g1 = in1 ? __bfloat162float(gg[i1]) : 0.f;
-          b1 = in1 ? __bfloat162float(bb[i1]) : 0.f;
-        }
-      };
-      load_gates(0);
 #pragma unroll 1
       for (int cu = 0;; ++cu, ++g) {
+        // the gates of the chunk's rows (0 past the sequence)
+        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+        {
+          const int64_t avail = len - start;
+          const int64_t i0 = (bos + start + lane) * p.h_v + h, i1 = i0 + 32 * (int64_t)p.h_v;
+          const bool in0 = lane < avail, in1 = lane + 32 < avail;
+          if constexpr (GF32) {
+            const float* gg = reinterpret_cast<const float*>(p.g);
+            const float* bb = reinterpret_cast<const float*>(p.beta);
+            if (in0) { g0 = gg[i0]; b0 = bb[i0]; }
+            if (in1) { g1 = gg[i1]; b1 = bb[i1]; }
+          } else {
+            const __nv_bfloat16* gg = reinterpret_cast<const __nv_bfloat16*>(p.g);
+            const __nv_bfloat16* bb = reinterpret_cast<const __nv_bfloat16*>(p.beta);
+            if (in0) { g0 = __bfloat162float(gg[i0]); b0 = __bfloat162float(bb[i0]); }
+            if (in1) { g1 = __bfloat162float(gg[i1]); b1 = __bfloat162float(bb[i1]); }
+          }
+        }
         const int mv = (int)(len - start < kChunk ? len - start : kChunk);
         // inclusive prefix sums and prefix max / min (the chunk start, 0, included)
         float s0 = g0, s1 = g1;
@@ -508,13 +499,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // rows of the chunk: the window, halved (out of line, only for decays far outside
         // the usual range) while the span of {0, G_0 .. G_{m-1}} passes kMaxSpan
         int m = mv;
-        float gmax = fmaxf(lane < m ? s0 : -3.0e38f, lane + 32 < m ? s1 : -3.0e38f);
-        float gmin = fminf(lane < m ? s0 : 3.0e38f, lane + 32 < m ? s1 : 3.0e38f);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
-          gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
-        }
+        float gmax = warp_max(fmaxf(lane < m ? s0 : -3.0e38f, lane + 32 < m ? s1 : -3.0e38f));
+        float gmin = warp_min(fminf(lane < m ? s0 : 3.0e38f, lane + 32 < m ? s1 : 3.0e38f));
         if (m > 1 && fmaxf(gmax, 0.f) - fminf(gmin, 0.f) > kMaxSpan) {
           const float3 f = span_fit(s0, s1, m, lane);
           m = __float_as_int(f.x);
@@ -530,7 +516,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool ulast = start + m >= len;
         const bool slast = ulast && nxt >= total_units;
         const float b0c = b0, b1c = b1;
-        if (!ulast) load_gates(start + m);  // the next chunk's gates, in flight while this one waits
         // the K / Q ring slot of chunk g-3 was released
         if (g >= 3) ok = wait(B_KQE0 + g % 3, ((g / 3) + 1) & 1, 0);
         if (!ok) break;
@@ -547,8 +532,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           sc[SC_GM] = Gm;
           sc[SC_LAMLOG] = eager ? 0.f : loglam;
           sc[SC_NULOG] = eager ? -Gm : logmu;
-          sc[SC_RMW] = eager ? exp2f(loglam * kLog2e) : 1.f;
-          sc[SC_MUNEXT] = eager ? 1.f : exp2f(loglam * kLog2e);
+          const float lam = exp2f(loglam * kLog2e);
+          sc[SC_RMW] = eager ? lam : 1.f;
+          sc[SC_MUNEXT] = eager ? 1.f : lam;
           sc[SC_M] = __int_as_float(m);
           sc[SC_FLAGS] = __int_as_float((ulast ? F_ULAST : 0) | (eager ? F_EAGER : 0) |
                                         (cu == 0 ? F_UFIRST : 0) | (slast ? F_SLAST : 0));

@@ -368,6 +368,19 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Maximum / minimum of a float over the 32 lanes of a full warp (one warp-wide
+// reduction instruction; the operands here are never NaN).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float warp_min(float v) {
+  float r;
+  asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128-byte-swizzled region whose base is 1024-byte aligned.
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
