@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gdn_internal.cuh"
@@ -29,6 +30,9 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_
   __shared__ int n_roots;
   const int tid = threadIdx.x;
   const bool tree = p.parent != nullptr;
+  // The chunk kernel, launched as a programmatic dependent of this one, may start its
+  // set-up now; it waits for this grid to complete before it reads anything written here.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     p.status->code = 0u;
     p.status->detail = 0u;
@@ -429,20 +433,24 @@ static_assert(kNoallocBytes % 256 == 0, "the work list ends on a 256-byte bounda
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoallocBytes];
 
 // The device address of g_noalloc_workspace on the current device, looked up
-// once per device and kept.
+// once per device and kept. Calls after the first on a device read the kept
+// address without taking the lock.
 static gdn_status noalloc_workspace(void** addr) {
   static std::mutex mu;
-  static void* cached[64];
+  static std::atomic<void*> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
   if (dev < 0 || dev >= 64) return GDN_ERR_ARCH;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cached[dev]) {
-    void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_noalloc_workspace) != cudaSuccess || !a) return GDN_ERR_CUDA;
-    cached[dev] = a;
+  void* a = cached[dev].load(std::memory_order_acquire);
+  if (!a) {
+    std::lock_guard<std::mutex> lock(mu);
+    a = cached[dev].load(std::memory_order_relaxed);
+    if (!a) {
+      if (cudaGetSymbolAddress(&a, g_noalloc_workspace) != cudaSuccess || !a) return GDN_ERR_CUDA;
+      cached[dev].store(a, std::memory_order_release);
+    }
   }
-  *addr = cached[dev];
+  *addr = a;
   return GDN_OK;
 }
 

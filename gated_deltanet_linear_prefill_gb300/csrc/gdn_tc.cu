@@ -390,7 +390,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // units. Thread 0 takes the first unit here; the producer takes the rest.
   const int total_units = p.num_seqs * p.h_v;
   int* first_unit = reinterpret_cast<int*>(sm + L::MISC + MISC_WORK);
-  if (tid == 0) *first_unit = (int)atomicAdd(&p.status->next_unit, 1u);
 
   // ---- setup
   if (tid == 0) {
@@ -411,6 +410,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&tm.o);
   }
   if (warp == 1) tmem_alloc(tmem_base_ptr, kTmemCols);
+  // The launch may overlap the prep kernel (programmatic dependent launch): everything
+  // above touches only this CTA's own memory; the status block, the work counter and the
+  // work list are read only after the prep grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0) *first_unit = (int)atomicAdd(&p.status->next_unit, 1u);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1281,7 +1285,19 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   e = device_sm_count(&sms);
   if (e != cudaSuccess) return e;
   const long long grid = units < sms ? units : sms;
-  gdn_tc_kernel<DK, DV, OF32, GF32><<<(unsigned)grid, kTcThreads, L::DYN_SMEM, stream>>>(p, tm);
+  // launched as a programmatic dependent of the prep kernel, so that its set-up overlaps it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = L::DYN_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gdn_tc_kernel<DK, DV, OF32, GF32>, p, tm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -86,6 +86,27 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 @pytest.mark.gpu
+def test_noalloc_call_allocates_no_device_memory():
+    # After one warm-up call (which loads the kernels and looks the static
+    # workspace up), further calls leave the device's free memory unchanged.
+    w = workloads.random_workload([300, 5, 70], h_qk=2, h_v=4, d_k=128, d_v=128, seed=13)
+    d = w.to("cuda")
+    out = torch.empty(d.v.shape, dtype=d.out_dtype, device="cuda")
+    fs = torch.empty((d.num_seqs, d.h_v, d.d_k, d.d_v), dtype=torch.float32, device="cuda")
+    desc = gdn.make_desc(d.q, d.v, d.g, d.cu_seqlens, out_dtype=out.dtype, max_seqlen=w.max_seqlen)
+    call = lambda: gdn.gdn_prefill_varlen_noalloc(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, None, None,
+                                                  out, fs, desc)
+    assert call() == gdn.GDN_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        assert call() == gdn.GDN_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+
+
+@pytest.mark.gpu
 def test_noalloc_too_many_sequences_writes_nothing():
     n = gdn.GDN_NOALLOC_MAX_SEQS + 1
     cu = torch.arange(n + 1, dtype=torch.int32, device="cuda")
