@@ -115,6 +115,8 @@ constexpr int F_ULAST = 1;     // last chunk of its (sequence, head) unit
 constexpr int F_EAGER = 2;     // the stored state is rescaled before this chunk
 constexpr int F_UFIRST = 4;    // first chunk of its unit: the state starts over
 constexpr int F_SLAST = 8;     // last chunk this CTA processes
+constexpr int F_ZFIRST = 16;   // first chunk of a unit whose starting state is zero: the
+                               // state-dependent products (W' S~, S~^T Q^T) vanish
 
 // Per-chunk values WG-A hands to WG-B (three buffers, chunk % 3).
 struct ChunkScalars {
@@ -466,6 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         n = 0;
       }
       const int h = cur % p.h_v, hq = h / (p.h_v / p.h_qk);
+      const bool zstart = tree_parent(p, n) < 0 && state_slot(p, n) < 0;
       int64_t bos, eos;
       seq_bounds(p, n, bos, eos);
       const int64_t len = eos - bos;  // 0: one chunk of no rows carries the unit's state through
@@ -541,7 +544,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           sc[SC_MUNEXT] = eager ? 1.f : lam;
           sc[SC_M] = __int_as_float(m);
           sc[SC_FLAGS] = __int_as_float((ulast ? F_ULAST : 0) | (eager ? F_EAGER : 0) |
-                                        (cu == 0 ? F_UFIRST : 0) | (slast ? F_SLAST : 0));
+                                        (cu == 0 ? F_UFIRST : 0) | (slast ? F_SLAST : 0) |
+                                        (cu == 0 && zstart ? F_ZFIRST : 0));
           *reinterpret_cast<long long*>(&sc[SC_T0]) = (long long)(bos + start);
           sc[SC_N] = __int_as_float(n);
           sc[SC_H] = __int_as_float(h);
@@ -601,9 +605,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t kq = slot_kq(c), vv = slot_v(c);
         const uint32_t lbo_k = (L::NKA == 2) ? 16384u : (sbase + L::ZERO - kq);
         const uint64_t dka = sdesc(kq, lbo_k, 1024), dtw = sdesc(sbase + L::TW, 16, 1024);
+        const int fl = sc_int(slot_sc(c), SC_FLAGS);
+        if (!(fl & F_ZFIRST)) {  // W' only meets a nonzero state
 #pragma unroll 1
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tmem + TM_W, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + TM_W, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
+        }
         mma_commit(&bars[B_W_DONE]);  // W'^T may be converted while U is still running
         if (!wait(B_VFULL0 + par, (c >> 1) & 1, 10)) break;
         tc_fence_after();
@@ -615,7 +622,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  id_w, kk != 0);
         mma_commit(&bars[B_U_DONE]);
         mma_commit(&bars[B_VE0 + par]);
-        if (sc_int(slot_sc(c), SC_FLAGS) & F_SLAST) break;
+        if (fl & F_SLAST) break;
       }
       mma_commit(&bars[B_DRAIN1]);  // every MMA this thread issued has finished before exit
       wait(B_DRAIN1, 0, kDrainWait);
@@ -642,11 +649,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const bool last = cscal[c % 3].slast;  // read now: the buffer is reused after this chunk
         const uint32_t kq = slot_kq(c);
-        // U'^T += S~^T W'^T in tf32: A = S~^T (fp32, TMEM), B = W' fp32 K-major [j][d_k]
-        const uint64_t dwt = sdesc(sbase + L::WP, 16, 1024);
+        // a zero starting state: U' = U, no S~^T Q^T term, and the state update and the
+        // output product start their accumulators afresh
+        const uint32_t zf = (fl & F_ZFIRST) ? 0u : 1u;
+        if (zf) {
+          // U'^T += S~^T W'^T in tf32: A = S~^T (fp32, TMEM), B = W' fp32 K-major [j][d_k]
+          const uint64_t dwt = sdesc(sbase + L::WP, 16, 1024);
 #pragma unroll 1
-        for (int kk = 0; kk < DK / 8; ++kk)
-          mma_ts_tf32(tmem + TM_R, tmem + TM_S + kk * 8u, sdesc_add(dwt, (kk >> 2) * 8192u + (kk & 3) * 32u), id_sw, 1);
+          for (int kk = 0; kk < DK / 8; ++kk)
+            mma_ts_tf32(tmem + TM_R, tmem + TM_S + kk * 8u, sdesc_add(dwt, (kk >> 2) * 8192u + (kk & 3) * 32u), id_sw,
+                        1);
+        }
         mma_commit(&bars[B_UP_DONE]);
         // O^T = S~^T Q^T (raw q tile, K-major) from the bf16 copy of the state, once the
         // last epilogue has read O
@@ -654,11 +667,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (c >= 1) ol = with(ol, B_EPI_DONE, (c - 1) & 1);
         if (!wait_all(ol, 4)) break;
         tc_fence_after();
-        const uint64_t dq = sdesc(kq + 8192u, 16, 1024);
+        if (zf) {
+          const uint64_t dq = sdesc(kq + 8192u, 16, 1024);
 #pragma unroll 1
-        for (int kk = 0; kk < 4 * L::NKA; ++kk)
-          mma_ts(tmem + TM_O, tmem + TM_SB + kk * 8u, sdesc_add(dq, (kk >> 2) * 16384u + (kk & 3) * 32u),
-                 id_qs, kk != 0);
+          for (int kk = 0; kk < 4 * L::NKA; ++kk)
+            mma_ts(tmem + TM_O, tmem + TM_SB + kk * 8u, sdesc_add(dq, (kk >> 2) * 16384u + (kk & 3) * 32u),
+                   id_qs, kk != 0);
+        }
         if (!wait(B_UOPS_READY, c & 1, 7)) {
           break;
         }
@@ -667,14 +682,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint64_t dkn = sdesc(kq, (L::NKA == 2) ? 16384u : 16u, 1024);
 #pragma unroll 1
         for (int kk = 0; kk < 8; ++kk)  // hi (kk < 4), then lo
-          mma_ts(tmem + TM_S, tmem + TM_UH + kk * 8u, sdesc_add(dkn, (kk & 3) * 2048u), id_st, 1);
+          mma_ts(tmem + TM_S, tmem + TM_UH + kk * 8u, sdesc_add(dkn, (kk & 3) * 2048u), id_st, kk != 0 || zf);
         mma_commit(&bars[B_STATE_DONE]);
         // O^T += (U' s)^T M^T : B = M K-major [i][j]; the hi part of U' s only, since
         // this term reaches the output alone (M itself is bf16)
         const uint64_t dm = sdesc(sbase + L::M0 + par * 8192u, 16, 1024);
 #pragma unroll 1
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, kk * 32u), id_pu, 1);
+          mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, kk * 32u), id_pu, kk != 0 || zf);
         mma_commit(&bars[B_O_DONE]);
         mma_commit(&bars[B_MFREE0 + par]);
         if (last) break;
@@ -940,6 +955,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int64_t slot = state_slot(p, un);
       const float* s0 = par >= 0 ? p.final_state + ((size_t)par * p.h_v + uh) * DK * DV
                                  : (slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + uh) * DK * DV : nullptr);
+      if (!s0) return true;  // a zero state: the first state update overwrites S~ outright
 #pragma unroll 1
       for (int xb = 0; xb < DK / 32; ++xb) {
         uint32_t v[32];
@@ -1018,8 +1034,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // (chunk c's U' product, the buffer's last reader, finished before the split above)
         const uint32_t wcol = sbase + L::WP + (uint32_t)(wb >> 5) * 8192u + (uint32_t)(wb & 3) * 4u;
         const uint32_t wch = (uint32_t)((wb >> 2) & 7);  // 16-byte chunk of the row before the swizzle
+        const bool wz = sc_int(slot_sc(cn), SC_FLAGS) & F_ZFIRST;  // no U' product reads it
 #pragma unroll 1
-        for (int hb = 0; hb < 2; ++hb) {
+        for (int hb = 0; hb < (wz ? 0 : 2); ++hb) {
           uint32_t w[32];
           tmem_ld32(tmem + lane_off + TM_W + 32 * hb, w);
           tmem_ld_wait();
@@ -1062,8 +1079,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float* sc = slot_sc(cn);
         const bool eager = sc_int(sc, SC_FLAGS) & F_EAGER;
         const float rmw = sc[SC_RMW];
+        const bool sz = sc_int(sc, SC_FLAGS) & F_ZFIRST;  // no S~^T Q^T product reads it
 #pragma unroll 1
-        for (int xb = 0; xb < DK / 32; ++xb) {
+        for (int xb = 0; xb < (sz ? 0 : DK / 32); ++xb) {
           uint32_t va[32];
           tmem_ld32(tmem + lane_off + TM_S + xb * 32, va);
           tmem_ld_wait();
