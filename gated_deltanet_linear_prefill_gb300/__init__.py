@@ -21,7 +21,7 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = [
-    "GdnError", "GdnDesc", "GDN_OK", "GDN_BF16", "GDN_F32", "GDN_FLAG_NO_L2NORM", "GDN_FLAG_SIMT",
+    "GdnError", "GdnDesc", "GDN_OK", "GDN_BF16", "GDN_F32", "GDN_FLAG_NO_L2NORM", "GDN_FLAG_SIMT", "GDN_FLAG_NO_SEGMENT",
     "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_get_device_status",
     "gdn_status_string", "make_desc", "prefill_varlen", "library_path", "load_library",
     "gdn_gated_rmsnorm", "gated_rmsnorm", "GdnPrepDesc", "gdn_input_prep", "gdn_input_prep_tree", "input_prep",
@@ -33,6 +33,7 @@ GDN_OK = 0
 GDN_FLAG_NO_L2NORM = 0x1
 GDN_FLAG_SIMT = 0x2
 GDN_FLAG_TEST_CHILD_FIRST = 0x4  # tests only: fault injection for the bounded waits (include/gdn.h)
+GDN_FLAG_NO_SEGMENT = 0x8  # one sequence in one launch even when the segment scan applies
 GDN_NOALLOC_MAX_SEQS = 16384  # include/gdn.h
 STATUS_NAMES = ["GDN_OK", "GDN_ERR_NULL", "GDN_ERR_SHAPE", "GDN_ERR_DTYPE", "GDN_ERR_ALIGN",
                 "GDN_ERR_SEQLENS", "GDN_ERR_STATE_INDEX", "GDN_ERR_ALIAS", "GDN_ERR_WORKSPACE",

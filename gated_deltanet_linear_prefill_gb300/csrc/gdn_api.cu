@@ -34,8 +34,10 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_
   // set-up now; it waits for this grid to complete before it reads anything written here.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
-    p.status->code = 0u;
-    p.status->detail = 0u;
+    if (!p.keep_status) {
+      p.status->code = 0u;
+      p.status->detail = 0u;
+    }
     p.status->units_done = 0u;
     p.status->next_unit = 0u;
     n_roots = 0;
@@ -47,10 +49,12 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_
 
   const int N = p.num_seqs;
   for (int n = tid; n < N; n += kPrepThreads) {
-    const int64_t b = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
-    if ((n == 0 && b != 0) || e < b || (n == N - 1 && e != p.total_tokens) ||
-        (p.max_seqlen > 0 && e - b > p.max_seqlen))
-      report(p.status, GDN_ERR_SEQLENS, (uint32_t)n);
+    if (!p.seq_rows) {  // (a segment launch's rows were checked by its set-up kernel)
+      const int64_t b = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
+      if ((n == 0 && b != 0) || e < b || (n == N - 1 && e != p.total_tokens) ||
+          (p.max_seqlen > 0 && e - b > p.max_seqlen))
+        report(p.status, GDN_ERR_SEQLENS, (uint32_t)n);
+    }
     if (p.initial_state && p.state_index) {
       const int32_t s = p.state_index[n];
       if (s < -1 || s >= p.num_state_slots) report(p.status, GDN_ERR_STATE_INDEX, (uint32_t)n);
@@ -220,7 +224,10 @@ extern "C" int gdn_abi_version(void) { return GDN_ABI_VERSION; }
 
 extern "C" size_t gdn_workspace_bytes(const gdn_desc* desc) {
   if (!desc || desc->num_seqs < 0) return 0;
-  return gdn::workspace_bytes(desc->num_seqs);
+  const size_t base = gdn::workspace_bytes(desc->num_seqs);
+  if (!gdn::seg_eligible(desc)) return base;
+  const size_t seg = gdn::seg_layout(desc->h_v, desc->d_k, desc->d_v).end;
+  return seg > base ? seg : base;
 }
 
 extern "C" size_t gdn_tree_workspace_bytes(const gdn_desc* desc) {
@@ -324,8 +331,54 @@ static gdn_status validate(const void* q, const void* k, const void* v, const vo
   p.out_f32 = d->out_dtype == GDN_F32;
   p.l2norm = (d->flags & GDN_FLAG_NO_L2NORM) ? 0 : 1;
   p.scale = d->scale != 0.0f ? d->scale : 1.0f / sqrtf((float)d->d_k);
+  p.vzero_from = N;
+  p.out_upto = N;
   return GDN_OK;
 }
+
+namespace gdn {
+
+// The segment scan of one sequence (the plan has G >= 3): set-up, launch A, the
+// composition, launch C, and the final state copied out of the workspace. Every step
+// is stream-ordered; the status word collects the first error of any of them.
+static gdn_status run_segmented(const Params& p0, const SegPlan& plan, char* ws, cudaStream_t s) {
+  const SegLayout L = seg_layout(p0.h_v, p0.d_k, p0.d_v);
+  const int G = plan.G;
+  const size_t sb = (size_t)p0.h_v * p0.d_k * p0.d_v * 4;
+  if (launch_seg_setup(p0, plan, L, ws, s) != cudaSuccess) return GDN_ERR_CUDA;
+  Params pa = p0;
+  pa.num_seqs = 2 * G - 3;
+  pa.max_seqlen = 0;
+  pa.seq_rows = reinterpret_cast<const int64_t*>(ws + L.rows_a);
+  pa.initial_state = reinterpret_cast<const float*>(ws + L.slots);
+  pa.num_state_slots = 2;
+  pa.state_index = reinterpret_cast<const int32_t*>(ws + L.sidx_a);
+  pa.final_state = reinterpret_cast<float*>(ws + L.fin_a);
+  pa.vzero_from = G - 1;
+  pa.out_upto = 1;
+  pa.keep_status = 1;
+  if (launch_prep(pa, s) != cudaSuccess || launch_tc(pa, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (launch_seg_combine(p0, plan, L, ws, s) != cudaSuccess) return GDN_ERR_CUDA;
+  Params pc = p0;
+  pc.num_seqs = G - 1;
+  pc.max_seqlen = 0;
+  pc.seq_rows = reinterpret_cast<const int64_t*>(ws + L.rows_c);
+  pc.initial_state = reinterpret_cast<const float*>(ws + L.s_c);
+  pc.num_state_slots = G - 1;
+  pc.state_index = nullptr;                              // segment n starts from S_{n+1}
+  pc.final_state = reinterpret_cast<float*>(ws + L.fin_a);  // launch A's states are spent
+  pc.vzero_from = G - 1;
+  pc.out_upto = G - 1;
+  pc.keep_status = 1;
+  if (launch_prep(pc, s) != cudaSuccess || launch_tc(pc, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (p0.final_state &&
+      cudaMemcpyAsync(p0.final_state, ws + L.fin_a + (size_t)(G - 2) * sb, sb, cudaMemcpyDeviceToDevice, s) !=
+          cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+}  // namespace gdn
 
 extern "C" gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v,
                                          const void* g, const void* beta,
@@ -338,6 +391,13 @@ extern "C" gdn_status gdn_prefill_varlen(const void* q, const void* k, const voi
   if (st != GDN_OK) return st;
   if (p.num_seqs == 0) return GDN_OK;
   cudaStream_t s = (cudaStream_t)stream;
+  if (gdn::seg_eligible(desc) &&
+      desc->workspace_bytes >= gdn::seg_layout(desc->h_v, desc->d_k, desc->d_v).end) {
+    int sms = 0;
+    if (gdn::device_sm_count(&sms) != cudaSuccess) return GDN_ERR_CUDA;
+    const gdn::SegPlan plan = gdn::seg_plan(p.total_tokens, p.h_v, sms);
+    if (plan.G >= 3) return gdn::run_segmented(p, plan, (char*)desc->workspace, s);
+  }
   if (launch_prep(p, s) != cudaSuccess) return GDN_ERR_CUDA;
   const cudaError_t e = (desc->flags & GDN_FLAG_SIMT) ? launch_simt(p, s) : launch_tc(p, s);
   if (e != cudaSuccess) return GDN_ERR_CUDA;

@@ -58,6 +58,14 @@ struct Params {
   const int32_t* order;  // sequences, longest first (tree launches: parents before children)
   const int32_t* parent; // tree launches only (else NULL): parent[n] in [-1, n)
   uint32_t* ready;       // tree launches only: ready flag per (sequence, value head)
+  // Segment launches of one long sequence (else NULL / num_seqs / num_seqs / 0): the rows
+  // of virtual sequence n are [seq_rows[2n], seq_rows[2n+1]) (sequences may share rows);
+  // sequences n >= vzero_from read V as zero; only sequences n < out_upto write out;
+  // keep_status leaves the status word to the launch that set it up.
+  const int64_t* seq_rows;
+  int vzero_from;
+  int out_upto;
+  int keep_status;
   int64_t total_tokens;
   int num_seqs;
   int max_seqlen;
@@ -81,7 +89,8 @@ __device__ __forceinline__ float load_gate(const void* p, int64_t idx, int is_f3
 // Rows [bos, eos) of sequence n, clamped into [0, T] so that a malformed
 // cu_seqlens (reported by the prep kernel) can never send a load out of bounds.
 __device__ __forceinline__ void seq_bounds(const Params& p, int n, int64_t& bos, int64_t& eos) {
-  int64_t b = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
+  int64_t b = p.seq_rows ? p.seq_rows[2 * n] : p.cu_seqlens[n];
+  int64_t e = p.seq_rows ? p.seq_rows[2 * n + 1] : p.cu_seqlens[n + 1];
   b = b < 0 ? 0 : (b > p.total_tokens ? p.total_tokens : b);
   e = e < b ? b : (e > p.total_tokens ? p.total_tokens : e);
   bos = b;
@@ -115,5 +124,59 @@ cudaError_t device_sm_count(int* out);
 cudaError_t launch_prep(const Params& p, cudaStream_t stream);
 cudaError_t launch_simt(const Params& p, cudaStream_t stream);
 cudaError_t launch_tc(const Params& p, cudaStream_t stream);
+
+// ---- segment scan of one long sequence
+//
+// A single sequence of T rows leaves most SMs idle (one chain of chunks per value
+// head). The state after each segment is an affine map of the state before it,
+// S -> Phi_j S + Delta_j, so the sequence is cut into G segments (segment 0 of a rows,
+// the others of b rows, the last possibly shorter) and run in two chunk-kernel launches:
+//   A: segment 0 from the true starting state (its outputs are final), Delta_j (segments
+//      1 .. G-2 from a zero state) and Phi_j (the same segments with V = 0 from S = I);
+//   combine: S_1 = state after segment 0, S_{j+1} = Phi_j S_j + Delta_j;
+//   C: segments 1 .. G-1 from S_1 .. S_{G-1}: their outputs and the final state.
+struct SegPlan {
+  int G;       // segments (0: run the sequence in one launch)
+  int64_t a;   // rows of segment 0
+  int64_t b;   // rows of every later segment but the last
+};
+constexpr int kSegMaxG = 8;
+constexpr int64_t kSegMinTokens = 4096;
+
+// Byte offsets of the segment buffers after the work list (256-byte aligned), sized for
+// kSegMaxG segments: two state slots (the gathered starting state, the identity), the
+// launch-A final states, the states S_1 .. S_{G-1}, and the row / slot tables.
+struct SegLayout {
+  size_t slots, fin_a, s_c, rows_a, rows_c, sidx_a, end;
+};
+inline SegLayout seg_layout(int h_v, int d_k, int d_v) {
+  const size_t sb = (size_t)h_v * d_k * d_v * 4;
+  SegLayout L;
+  L.slots = workspace_bytes(1);
+  L.fin_a = L.slots + 2 * sb;
+  L.s_c = L.fin_a + (size_t)(2 * kSegMaxG - 3) * sb;
+  L.rows_a = L.s_c + (size_t)(kSegMaxG - 1) * sb;
+  L.rows_c = L.rows_a + round_up(sizeof(int64_t) * 2 * (2 * kSegMaxG - 3), 256);
+  L.sidx_a = L.rows_c + round_up(sizeof(int64_t) * 2 * (kSegMaxG - 1), 256);
+  L.end = L.sidx_a + round_up(sizeof(int32_t) * (2 * kSegMaxG - 3), 256);
+  return L;
+}
+// Whether a descriptor of one sequence may take the segment scan (the workspace size
+// then includes SegLayout): the tensor-core kernel, square states, a long sequence.
+inline bool seg_eligible(const gdn_desc* d) {
+  return d && d->num_seqs == 1 && !(d->flags & (GDN_FLAG_SIMT | GDN_FLAG_NO_SEGMENT)) && d->d_k == d->d_v &&
+         d->total_tokens >= kSegMinTokens && d->h_v >= 1;
+}
+// The plan for one sequence of T rows on `sms` SMs: the segment count and lengths that
+// minimise the two launches' makespan (longest-first list scheduling of whole units,
+// in chunk periods), or G = 0 when one launch is as fast.
+SegPlan seg_plan(int64_t T, int h_v, int sms);
+// Launch set-up (one kernel): status reset, checks of the caller's cu_seqlens and
+// state_index, the slot states, the row tables and slot table of both launches.
+cudaError_t launch_seg_setup(const Params& p, const SegPlan& plan, const SegLayout& L, char* ws,
+                             cudaStream_t stream);
+// S_1 = fin_a[0]; S_{j+1} = Phi_j S_j + Delta_j for j = 1 .. G-2, into s_c[0 .. G-2].
+cudaError_t launch_seg_combine(const Params& p, const SegPlan& plan, const SegLayout& L, char* ws,
+                               cudaStream_t stream);
 
 }  // namespace gdn

@@ -117,6 +117,10 @@ constexpr int F_UFIRST = 4;    // first chunk of its unit: the state starts over
 constexpr int F_SLAST = 8;     // last chunk this CTA processes
 constexpr int F_ZFIRST = 16;   // first chunk of a unit whose starting state is zero: the
                                // state-dependent products (W' S~, S~^T Q^T) vanish
+constexpr int F_VZERO = 32;    // the unit reads V as zero (a segment's state map Phi)
+constexpr int F_NOOUT = 64;    // the unit writes no output (only its final state is used)
+// (the last two occur only in a segment launch, the kernel's SEG instance: every test of
+// them is written SEG && ..., so that the other instances carry none of their code)
 
 // Per-chunk values WG-A hands to WG-B (three buffers, chunk % 3).
 struct ChunkScalars {
@@ -371,7 +375,7 @@ __device__ __noinline__ void drain_loads(uint32_t bars, int kq_issued, int v_iss
 // ---------------------------------------------------------------- the kernel
 // OF32: fp32 output (else bf16); GF32: fp32 gates (else bf16). Template parameters,
 // so that each kernel holds only its own epilogue and gate loads.
-template <int DK, int DV, bool OF32, bool GF32>
+template <int DK, int DV, bool OF32, bool GF32, bool SEG>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gdn_tc_kernel(const Params p, const __grid_constant__ Tmaps tm) {
   using L = TcLayout<DK, DV>;
@@ -452,13 +456,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t kq_bytes = (uint32_t)(2 * L::NKA) * 8192u, v_bytes = (uint32_t)L::NVA * 8192u;
     int kq_issued = 0, v_issued = 0;  // chunks whose K / Q and V loads were requested
     int cur = *first_unit, g = 0;     // the unit in hand; chunks emitted so far
-    // the next unit is taken one unit ahead, so that a chunk knows whether it is the CTA's last
+    // the next unit is taken when the last chunk of the current one is emitted (so that
+    // this chunk knows whether it is the CTA's last), not earlier: a CTA then holds a
+    // second unit only briefly, and the work list keeps its longest-first order
     auto take_unit = [&]() {
       int u = 0;
       if (lane == 0) u = (int)atomicAdd(&p.status->next_unit, 1u);
       return __shfl_sync(0xffffffffu, u, 0);
     };
-    int nxt = cur < total_units ? take_unit() : total_units;
+    int nxt = -1;
     bool ok = true;
 #pragma unroll 1
     while (ok && cur < total_units) {
@@ -468,7 +474,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         n = 0;
       }
       const int h = cur % p.h_v, hq = h / (p.h_v / p.h_qk);
-      const bool zstart = tree_parent(p, n) < 0 && state_slot(p, n) < 0;
+      const bool vzero = SEG && n >= p.vzero_from, noout = SEG && n >= p.out_upto;
+      const bool zstart = tree_parent(p, n) < 0 && state_slot(p, n) < 0 && !vzero;
       int64_t bos, eos;
       seq_bounds(p, n, bos, eos);
       const int64_t len = eos - bos;  // 0: one chunk of no rows carries the unit's state through
@@ -521,6 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float loglam = logmu + Gm;
         const bool eager = fabsf(loglam) > kMaxLogScale;
         const bool ulast = start + m >= len;
+        if (ulast && nxt < 0) nxt = take_unit();
         const bool slast = ulast && nxt >= total_units;
         const float b0c = b0, b1c = b1;
         // the K / Q ring slot of chunk g-3 was released
@@ -545,7 +553,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           sc[SC_M] = __int_as_float(m);
           sc[SC_FLAGS] = __int_as_float((ulast ? F_ULAST : 0) | (eager ? F_EAGER : 0) |
                                         (cu == 0 ? F_UFIRST : 0) | (slast ? F_SLAST : 0) |
-                                        (cu == 0 && zstart ? F_ZFIRST : 0));
+                                        (cu == 0 && zstart ? F_ZFIRST : 0) | (vzero ? F_VZERO : 0) |
+                                        (noout ? F_NOOUT : 0));
           *reinterpret_cast<long long*>(&sc[SC_T0]) = (long long)(bos + start);
           sc[SC_N] = __int_as_float(n);
           sc[SC_H] = __int_as_float(h);
@@ -567,10 +576,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         if (lane == 0) {
           uint64_t* vfull = &bars[B_VFULL0 + (g & 1)];
-          mbar_arrive_expect_tx(vfull, v_bytes);
-          const uint32_t vv = slot_v(g);
+          if (vzero) {
+            mbar_arrive(vfull);  // no tile: the U product is skipped
+          } else {
+            mbar_arrive_expect_tx(vfull, v_bytes);
+            const uint32_t vv = slot_v(g);
 #pragma unroll 1
-          for (int a = 0; a < L::NVA; ++a) tma_load_3d(sm + (vv - sbase) + a * 8192, &tm.v, vfull, 64 * a, h, row);
+            for (int a = 0; a < L::NVA; ++a) tma_load_3d(sm + (vv - sbase) + a * 8192, &tm.v, vfull, 64 * a, h, row);
+          }
         }
         __syncwarp();
         v_issued = g + 1;
@@ -583,7 +596,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (nxt >= total_units) break;
       cur = nxt;
-      nxt = take_unit();
+      nxt = -1;
     }
     // let every requested tile land before the CTA can exit (on the normal path
     // they were all consumed and these return at once)
@@ -616,10 +629,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
         const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(sbase + L::TB, 16, 1024);
+        if (!(SEG && (fl & F_VZERO))) {  // V = 0: U = 0, and U' starts from -W' S~
 #pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)  // T_b hi, then lo
-          mma_ss(tmem + TM_R, sdesc_add(dva, (kk & 3) * 2048u), sdesc_add(dtb, (kk >> 2) * 8192u + (kk & 3) * 32u),
-                 id_w, kk != 0);
+          for (int kk = 0; kk < 8; ++kk)  // T_b hi, then lo
+            mma_ss(tmem + TM_R, sdesc_add(dva, (kk & 3) * 2048u), sdesc_add(dtb, (kk >> 2) * 8192u + (kk & 3) * 32u),
+                   id_w, kk != 0);
+        }
         mma_commit(&bars[B_U_DONE]);
         mma_commit(&bars[B_VE0 + par]);
         if (fl & F_SLAST) break;
@@ -652,13 +667,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // a zero starting state: U' = U, no S~^T Q^T term, and the state update and the
         // output product start their accumulators afresh
         const uint32_t zf = (fl & F_ZFIRST) ? 0u : 1u;
+        const uint32_t vz = (SEG && (fl & F_VZERO)) ? 1u : 0u;  // R holds no U: the first product overwrites it
+        const bool want_o = !(SEG && (fl & F_NOOUT));           // no output: no output products
         if (zf) {
           // U'^T += S~^T W'^T in tf32: A = S~^T (fp32, TMEM), B = W' fp32 K-major [j][d_k]
           const uint64_t dwt = sdesc(sbase + L::WP, 16, 1024);
 #pragma unroll 1
           for (int kk = 0; kk < DK / 8; ++kk)
             mma_ts_tf32(tmem + TM_R, tmem + TM_S + kk * 8u, sdesc_add(dwt, (kk >> 2) * 8192u + (kk & 3) * 32u), id_sw,
-                        1);
+                        kk != 0 || !vz);
         }
         mma_commit(&bars[B_UP_DONE]);
         // O^T = S~^T Q^T (raw q tile, K-major) from the bf16 copy of the state, once the
@@ -667,7 +684,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (c >= 1) ol = with(ol, B_EPI_DONE, (c - 1) & 1);
         if (!wait_all(ol, 4)) break;
         tc_fence_after();
-        if (zf) {
+        if (zf && want_o) {
           const uint64_t dq = sdesc(kq + 8192u, 16, 1024);
 #pragma unroll 1
           for (int kk = 0; kk < 4 * L::NKA; ++kk)
@@ -687,9 +704,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // O^T += (U' s)^T M^T : B = M K-major [i][j]; the hi part of U' s only, since
         // this term reaches the output alone (M itself is bf16)
         const uint64_t dm = sdesc(sbase + L::M0 + par * 8192u, 16, 1024);
+        if (want_o) {
 #pragma unroll 1
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, kk * 32u), id_pu, kk != 0 || zf);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + TM_O, tmem + TM_UH + kk * 8u, sdesc_add(dm, kk * 32u), id_pu, kk != 0 || zf);
+        }
         mma_commit(&bars[B_O_DONE]);
         mma_commit(&bars[B_MFREE0 + par]);
         if (last) break;
@@ -729,8 +748,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         float* sc = slot_sc(c);
         const uint32_t qa = slot_kq(c) + 8192u;  // Q atom 0 (atom a at + 16384 a)
+        const int nrb = (SEG && (sc_int(sc, SC_FLAGS) & F_NOOUT)) ? 0 : 4;  // r^q only weights outputs
 #pragma unroll 1
-        for (int rb = 0; rb < 4; ++rb) {
+        for (int rb = 0; rb < nrb; ++rb) {
           const uint32_t r = 16u * rb + lr;
           float d0[4] = {}, d1[4] = {};  // columns 0-7 and 8-15 of the 16 x 16 block
 #pragma unroll
@@ -836,7 +856,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                           make_float2(d4.z, d4.w));
             *reinterpret_cast<float4*>(&Abuf[i * LDF + j0]) = make_float4(a01.x, a01.y, a23.x, a23.y);
           }
-        } else if (!krow && !upper) {
+        } else if (!krow && !upper && !(SEG && (sc_int(sc, SC_FLAGS) & F_NOOUT))) {
           // M_ij = q_i.k_j  (j <= i), bf16 K-major [i][j]
           const uint32_t mrow = sbase + L::M0 + par * 8192u;
 #pragma unroll
@@ -1079,9 +1099,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float* sc = slot_sc(cn);
         const bool eager = sc_int(sc, SC_FLAGS) & F_EAGER;
         const float rmw = sc[SC_RMW];
-        const bool sz = sc_int(sc, SC_FLAGS) & F_ZFIRST;  // no S~^T Q^T product reads it
+        // the bf16 copy only feeds S~^T Q^T, which a zero state or a unit without output skips;
+        // the decay of an eager chunk is applied all the same
+        const bool sb = !(sc_int(sc, SC_FLAGS) & (F_ZFIRST | (SEG ? F_NOOUT : 0)));
 #pragma unroll 1
-        for (int xb = 0; xb < (sz ? 0 : DK / 32); ++xb) {
+        for (int xb = 0; xb < (sb || eager ? DK / 32 : 0); ++xb) {
           uint32_t va[32];
           tmem_ld32(tmem + lane_off + TM_S + xb * 32, va);
           tmem_ld_wait();
@@ -1090,10 +1112,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int x = 0; x < 32; ++x) va[x] = __float_as_uint(__uint_as_float(va[x]) * rmw);
             tmem_st32(tmem + lane_off + TM_S + xb * 32, va);
           }
-          uint32_t pk[16];
+          if (sb) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x) pk[x] = pack_bf16(__uint_as_float(va[2 * x]), __uint_as_float(va[2 * x + 1]));
-          tmem_st16(tmem + lane_off + TM_SB + xb * 16, pk);
+            for (int x = 0; x < 16; ++x) pk[x] = pack_bf16(__uint_as_float(va[2 * x]), __uint_as_float(va[2 * x + 1]));
+            tmem_st16(tmem + lane_off + TM_SB + xb * 16, pk);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -1119,7 +1143,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const long long t0 = cs.t0;
         const uint32_t stg = slot_kq(c);
         const float* rq = slot_sc(c) + SC_RQ;
-        if constexpr (!OF32) {
+        if (SEG && (sc_int(slot_sc(c), SC_FLAGS) & F_NOOUT)) {
+          // nothing to write: the chunk's buffers go straight back
+          if (wb == 0) {
+            mbar_arrive(&bars[B_EPI_DONE]);
+            mbar_arrive(&bars[B_CSF0 + c % 3]);
+            mbar_arrive(&bars[B_KQE0 + c % 3]);
+          }
+        } else if constexpr (!OF32) {
           // each thread takes consecutive row pairs of its 16-lane blocks (16 x 256b loads)
           // and writes 8x8 blocks transposed into the row-major tiles (the eight rows of a
           // block hit distinct banks under the swizzle); a tile row is 32 half + lane
@@ -1284,7 +1315,7 @@ bool encode_out(CUtensorMap* m, void* base, int64_t T, int H, int D, bool f32) {
 }
 
 
-template <int DK, int DV, bool OF32, bool GF32>
+template <int DK, int DV, bool OF32, bool GF32, bool SEG>
 cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   using L = TcLayout<DK, DV>;
   Tmaps tm;
@@ -1293,7 +1324,7 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
       !encode_rows(&tm.v, p.v, p.total_tokens, p.h_v, DV) ||
       !encode_out(&tm.o, p.out, p.total_tokens, p.h_v, DV, p.out_f32 != 0))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV, OF32, GF32>), (int)L::DYN_SMEM);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV, OF32, GF32, SEG>), (int)L::DYN_SMEM);
   if (e != cudaSuccess) return e;
   const long long units = (long long)p.num_seqs * p.h_v;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -1314,7 +1345,7 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gdn_tc_kernel<DK, DV, OF32, GF32>, p, tm);
+  e = cudaLaunchKernelEx(&cfg, gdn_tc_kernel<DK, DV, OF32, GF32, SEG>, p, tm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1329,11 +1360,21 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
   const int t = (p.out_f32 ? 2 : 0) + (p.gate_f32 ? 1 : 0);
   auto by_types = [&](auto dk, auto dv) {
     constexpr int K_ = decltype(dk)::value, V_ = decltype(dv)::value;
+    // segment launches (square states only) take the SEG instance
+    constexpr bool SQ = K_ == V_;
+    if (SQ && p.seq_rows) {
+      switch (t) {
+        case 0: return launch_tc_dk<K_, V_, false, false, SQ>(p, stream);
+        case 1: return launch_tc_dk<K_, V_, false, true, SQ>(p, stream);
+        case 2: return launch_tc_dk<K_, V_, true, false, SQ>(p, stream);
+        default: return launch_tc_dk<K_, V_, true, true, SQ>(p, stream);
+      }
+    }
     switch (t) {
-      case 0: return launch_tc_dk<K_, V_, false, false>(p, stream);
-      case 1: return launch_tc_dk<K_, V_, false, true>(p, stream);
-      case 2: return launch_tc_dk<K_, V_, true, false>(p, stream);
-      default: return launch_tc_dk<K_, V_, true, true>(p, stream);
+      case 0: return launch_tc_dk<K_, V_, false, false, false>(p, stream);
+      case 1: return launch_tc_dk<K_, V_, false, true, false>(p, stream);
+      case 2: return launch_tc_dk<K_, V_, true, false, false>(p, stream);
+      default: return launch_tc_dk<K_, V_, true, true, false>(p, stream);
     }
   };
   using I64 = std::integral_constant<int, 64>;

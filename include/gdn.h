@@ -81,6 +81,9 @@ typedef enum {
  * runs out, the device status becomes GDN_ERR_DEVICE_TIMEOUT and the kernel returns
  * (outputs unspecified). No fault, trap or hang. Ignored by gdn_prefill_varlen. */
 #define GDN_FLAG_TEST_CHILD_FIRST 0x4u
+/* Run a single long sequence in one chunk-kernel launch even when the segment scan
+ * (see gdn_prefill_varlen) would apply. */
+#define GDN_FLAG_NO_SEGMENT 0x8u
 
 /*
  * Problem descriptor. Every field is read on the host at call time; the
@@ -107,10 +110,14 @@ int gdn_abi_version(void);
 
 /*
  * Bytes of device workspace gdn_prefill_varlen needs for this descriptor
- * (depends on num_seqs and the head counts only; 0 for a NULL desc). The
+ * (depends on the descriptor's sizes and flags only; 0 for a NULL desc). The
  * workspace holds the device status word and the work list. Its contents need
  * no initialisation and are rewritten by every call; size it once for the
  * largest batch and reuse it (one call at a time per workspace).
+ *
+ * A descriptor of one sequence of at least 4096 rows with d_k == d_v (tensor-core
+ * kernel, no GDN_FLAG_NO_SEGMENT) also gets room for the segment scan: about
+ * (3 * 8 - 1) fp32 states of h_v x d_k x d_v (46 MiB at h_v = 32, d = 128).
  */
 size_t gdn_workspace_bytes(const gdn_desc* desc);
 
@@ -136,6 +143,14 @@ size_t gdn_workspace_bytes(const gdn_desc* desc);
  * not overlap initial_state (one slot can feed many sequences). Asynchronous on
  * `stream`; safe to capture in a CUDA graph (fixed launch shapes for a fixed
  * descriptor, no allocation, no host synchronisation).
+ *
+ * Segment scan. The chunks of one (sequence, value head) pair form a chain, so a
+ * single sequence keeps only h_v SMs busy. When the descriptor qualifies (see
+ * gdn_workspace_bytes) and its workspace holds the larger size, a single sequence
+ * is cut into segments whose state maps S -> Phi S + Delta (linear in the starting
+ * state) are computed side by side and then composed; the segments are then rerun
+ * from their true starting states. Results agree with the single-launch path
+ * within rounding. A smaller workspace, or GDN_FLAG_NO_SEGMENT, keeps one launch.
  */
 gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const void* g,
                               const void* beta, const int32_t* cu_seqlens,
