@@ -907,6 +907,11 @@ def run_long_bench(args):
                          max_seqlen=w.max_seqlen)
     ws = torch.empty(max(256, gdn.gdn_workspace_bytes(desc)), dtype=torch.uint8, device=device)
     desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    n_seg, rows0, rows = gdn.gdn_segment_plan(desc, sms)
+    # kernels per call: segment scan = set-up, prep + chunk kernel (A), composition,
+    # prep + chunk kernel (C); one launch = prep + chunk kernel
+    launches_per_call = 6 if n_seg else 2
 
     def call(i):
         q, k, v, g, beta, init = layers[i]
@@ -999,6 +1004,9 @@ def run_long_bench(args):
         "config": {"workload": "cfg4_long_T16384", "num_seqs": 1, "total_tokens": T, "h_qk": w.h_qk,
                    "h_v": w.h_v, "d_k": w.d_k, "d_v": w.d_v, "chunk": 64, "gates": "bf16", "out": "bf16",
                    "state": "fp32 (initial state gathered)", "kernel": "tc",
+                   "segment_scan": ({"segments": n_seg, "rows_segment0": rows0, "rows_per_segment": rows,
+                                     "units_launch_a": w.h_v * (2 * n_seg - 3), "units_launch_c": w.h_v * (n_seg - 1)}
+                                    if n_seg else None),
                    "l2_flush": "none needed: one call's inputs (%.2f GB) exceed the 129 MB L2" % (
                        (B - 2 * w.h_v * w.d_k * w.d_v * 4) / 1e9),
                    "layers": n_layers,
@@ -1013,10 +1021,13 @@ def run_long_bench(args):
                      "algorithmic_bytes_per_launch": B, "tensor_flops_per_launch": F,
                      "tensor_tflops_achieved": F / s_one / 1e12,
                      "frac_of_roofline_time": roofline_time / s_one,
-                     "note": "32 (sequence, value head) chains on 152 SMs: bound by the chain "
-                             "length (256 chunks), not by bandwidth"},
+                     "note": ("one prompt: the segment scan runs %d segments' state maps side by side, "
+                              "then the segments from their true states; bound by the chunk chains "
+                              "(one unit per SM), not by bandwidth" % n_seg) if n_seg else
+                             ("%d (sequence, value head) chains on %d SMs: bound by the chain length, "
+                              "not by bandwidth" % (w.h_v, sms))},
         "e2e": e2e_line,
-        "gpu_launches": 2 * (args.steps + passes * n_layers),
+        "gpu_launches": launches_per_call * (args.steps + passes * n_layers),
         "clocks": clk,
     }
     if not args.no_cpu_baseline:

@@ -118,6 +118,9 @@ def load_library(build_if_missing: bool = True):
         lib.gdn_prefill_varlen_noalloc.restype = ctypes.c_int
         lib.gdn_tree_workspace_bytes.argtypes = [ctypes.POINTER(GdnDesc)]
         lib.gdn_tree_workspace_bytes.restype = ctypes.c_size_t
+        lib.gdn_segment_plan.argtypes = [ctypes.POINTER(GdnDesc), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
+        lib.gdn_segment_plan.restype = ctypes.c_int
         lib.gdn_prefill_tree.argtypes = [P] * 11 + [ctypes.POINTER(GdnDesc), P]
         lib.gdn_prefill_tree.restype = ctypes.c_int
         lib.gdn_gated_rmsnorm.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
@@ -198,6 +201,17 @@ def gdn_prefill_varlen_noalloc(q, k, v, g, beta, cu_seqlens, initial_state, stat
 
 def gdn_tree_workspace_bytes(desc: GdnDesc) -> int:
     return int(load_library().gdn_tree_workspace_bytes(ctypes.byref(desc)))
+
+
+def gdn_segment_plan(desc: GdnDesc, sms: int):
+    """(segments, rows of segment 0, rows of each later segment) that gdn_prefill_varlen
+    takes for this descriptor on `sms` SMs; segments == 0 means one launch."""
+    G, a, b = ctypes.c_int32(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = load_library().gdn_segment_plan(ctypes.byref(desc), int(sms), ctypes.byref(G), ctypes.byref(a),
+                                         ctypes.byref(b))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_segment_plan")
+    return int(G.value), int(a.value), int(b.value)
 
 
 def gdn_prefill_tree(q, k, v, g, beta, cu_seqlens, parent, initial_state, state_index, out,

@@ -230,6 +230,24 @@ extern "C" size_t gdn_workspace_bytes(const gdn_desc* desc) {
   return seg > base ? seg : base;
 }
 
+extern "C" gdn_status gdn_segment_plan(const gdn_desc* desc, int32_t sms, int32_t* segments, int64_t* rows0,
+                                       int64_t* rows) {
+  if (!desc || !segments || !rows0 || !rows) return GDN_ERR_NULL;
+  if (sms < 1) return GDN_ERR_VALUE;
+  *segments = 0;
+  *rows0 = desc->total_tokens;
+  *rows = 0;
+  if (!gdn::seg_eligible(desc) || desc->workspace_bytes < gdn::seg_layout(desc->h_v, desc->d_k, desc->d_v).end)
+    return GDN_OK;
+  const gdn::SegPlan plan = gdn::seg_plan(desc->total_tokens, desc->h_v, sms);
+  if (plan.G >= 3) {
+    *segments = plan.G;
+    *rows0 = plan.a;
+    *rows = plan.b;
+  }
+  return GDN_OK;
+}
+
 extern "C" size_t gdn_tree_workspace_bytes(const gdn_desc* desc) {
   if (!desc || desc->num_seqs < 0 || desc->h_v < 1) return 0;
   return gdn::tree_workspace_bytes(desc->num_seqs, desc->h_v);

@@ -117,7 +117,7 @@ int gdn_abi_version(void);
  *
  * A descriptor of one sequence of at least 4096 rows with d_k == d_v (tensor-core
  * kernel, no GDN_FLAG_NO_SEGMENT) also gets room for the segment scan: about
- * (3 * 8 - 1) fp32 states of h_v x d_k x d_v (46 MiB at h_v = 32, d = 128).
+ * 22 fp32 states of h_v x d_k x d_v (44 MiB at h_v = 32, d = 128).
  */
 size_t gdn_workspace_bytes(const gdn_desc* desc);
 
@@ -156,6 +156,19 @@ gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const
                               const void* beta, const int32_t* cu_seqlens,
                               const float* initial_state, const int32_t* state_index, void* out,
                               float* final_state, const gdn_desc* desc, void* stream);
+
+/*
+ * The segment plan gdn_prefill_varlen takes for this descriptor on a device with `sms`
+ * SMs: *segments = G, the number of segments (0: one launch), *rows0 = the rows of
+ * segment 0, *rows = the rows of every later segment but the last, which ends at
+ * total_tokens. G > 0 only when the descriptor qualifies (gdn_workspace_bytes) and
+ * desc->workspace_bytes holds the larger size. The plan minimises the two launches'
+ * makespan in chunk periods (longest-first list scheduling of whole (segment, head)
+ * units) and is used only when it beats one launch by more than 15%. Host only, no
+ * device call; GDN_ERR_NULL for a NULL argument, GDN_ERR_VALUE for sms < 1.
+ */
+gdn_status gdn_segment_plan(const gdn_desc* desc, int32_t sms, int32_t* segments, int64_t* rows0,
+                            int64_t* rows);
 
 /*
  * Largest num_seqs gdn_prefill_varlen_noalloc accepts. Its built-in scratch

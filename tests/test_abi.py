@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "gdn_abi_version", "gdn_workspace_bytes", "gdn_prefill_varlen", "gdn_prefill_varlen_noalloc",
         "gdn_tree_workspace_bytes", "gdn_prefill_tree", "gdn_get_device_status",
-        "gdn_status_string", "gdn_gated_rmsnorm", "gdn_input_prep", "gdn_input_prep_tree"])
+        "gdn_status_string", "gdn_gated_rmsnorm", "gdn_input_prep", "gdn_input_prep_tree",
+        "gdn_segment_plan"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -347,3 +348,51 @@ def test_header_is_plain_c_and_cpp():
                             *(["-std=c99", "-pedantic"] if lang == "c" else ["-std=c++17"]), HEADER],
                            capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def _long_desc(T, h_v=32, d=128, flags=0, big_ws=True):
+    d_ = gdn.GdnDesc()
+    d_.num_seqs, d_.total_tokens, d_.h_qk, d_.h_v, d_.d_k, d_.d_v = 1, T, 16 if h_v >= 16 else 1, h_v, d, d
+    d_.qkv_dtype = d_.gate_dtype = d_.out_dtype = gdn.GDN_BF16
+    d_.flags = flags
+    if big_ws:
+        d_.workspace_bytes = gdn.gdn_workspace_bytes(d_)
+    return d_
+
+
+def _chunks(r):
+    return (r + 63) // 64
+
+
+def test_segment_plan_and_workspace_host_logic():
+    """Host logic of the segment scan (no device): which descriptors qualify, the
+    workspace they then need, and a plan whose segments tile the sequence and whose
+    two-launch makespan (longest-first list scheduling, in chunk periods) beats one
+    launch of the whole sequence."""
+    sms = 152
+    small = gdn.gdn_workspace_bytes(_long_desc(4095))
+    big = gdn.gdn_workspace_bytes(_long_desc(16384))
+    assert small == 512 and big > 22 * 32 * 128 * 128 * 4  # 2 slots + 13 + 7 states, tables
+    assert gdn.gdn_workspace_bytes(_long_desc(16384, flags=gdn.GDN_FLAG_NO_SEGMENT)) == 512
+    assert gdn.gdn_workspace_bytes(_long_desc(16384, flags=gdn.GDN_FLAG_SIMT)) == 512
+    # a workspace of the small size keeps one launch
+    assert gdn.gdn_segment_plan(_long_desc(16384, big_ws=False), sms)[0] == 0
+    assert gdn.gdn_segment_plan(_long_desc(4095), sms)[0] == 0
+    for T, h_v in [(16384, 32), (4096, 32), (5001, 4), (65536, 32), (9000, 8), (4097, 2)]:
+        G, a, b = gdn.gdn_segment_plan(_long_desc(T, h_v), sms)
+        assert 3 <= G <= 8, (T, h_v, G)
+        last = T - a - (G - 2) * b
+        assert a >= 64 and b % 64 == 0 and 1 <= last, (T, G, a, b)
+        # launch A: segment 0 and (Delta_j, Phi_j) for j = 1 .. G-2; launch C: segments 1 .. G-1
+        def makespan(units):
+            import heapq
+            load = [0] * sms
+            for u in sorted(units, reverse=True):
+                heapq.heapreplace(load, load[0] + u)
+            return max(load)
+        ua = [_chunks(a)] * h_v + [_chunks(b)] * (2 * (G - 2) * h_v)
+        uc = [_chunks(b)] * ((G - 2) * h_v) + [_chunks(last)] * h_v
+        assert makespan(ua) + makespan(uc) < 0.85 * _chunks(T), (T, h_v, G, a, b)
+    assert gdn.gdn_segment_plan(_long_desc(16384), sms) == (4, 2176, 4736)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_segment_plan(_long_desc(16384), 0)
