@@ -891,7 +891,7 @@ def run_long_bench(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     gdn.load_library()
-    n_layers = 48
+    n_layers = max(1, min(48, args.layers))
     w = workloads.config(4, layer=0)
     T = w.total_tokens
     stream = torch.cuda.current_stream(device)
@@ -1066,6 +1066,9 @@ def main(argv=None):
                     help="time the GDN input prep (conv + SiLU + split, gates) on the 74-prompt batch")
     ap.add_argument("--long", action="store_true",
                     help="time one 16,384-token prompt: one call and 48 back-to-back calls (48 layers)")
+    ap.add_argument("--layers", type=int, default=48,
+                    help="--long: input sets drawn and timed back to back (48 = every linear-attention "
+                         "layer; fewer only for short profiling runs)")
     args = ap.parse_args(argv)
     if args.long:
         run_long_bench(args)

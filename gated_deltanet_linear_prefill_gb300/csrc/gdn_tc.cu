@@ -56,11 +56,34 @@
 #include "tc_ptx.cuh"
 
 namespace gdn {
+#ifdef GDN_TC_TRACE
+// [16 warps][256 chunks][8 points] clock64 stamps, then {clock, globaltimer} at the
+// traced CTA's start and end (for the clock rate)
+__device__ unsigned long long g_gdn_trace[16 * 2048 + 4];
+__device__ int g_gdn_trace_cta = 0;
+#endif
 namespace {
 
 using namespace ptx;
 
 constexpr int kTcThreads = 512;
+
+// Per-role clock trace, compiled only into the tracing build (-DGDN_TC_TRACE, the
+// separate libgdn_trace.so): lane 0 of warp `role` in CTA g_gdn_trace_cta records
+// clock64() at point `pt` (0-7) of chunk `chunk` (< 256); gdn_trace_* read it back.
+#ifdef GDN_TC_TRACE
+#define GDN_TRACE(role, chunk, pt)                                                                   \
+  do {                                                                                               \
+    const int gt_c = (chunk);                                                                        \
+    if ((int)blockIdx.x == g_gdn_trace_cta && gt_c >= 0 && gt_c < 256 && (threadIdx.x & 31) == 0 &&  \
+        (int)(threadIdx.x >> 5) == (role))                                                           \
+      g_gdn_trace[(role) * 2048 + gt_c * 8 + (pt)] = clock64();                                      \
+  } while (0)
+#else
+#define GDN_TRACE(role, chunk, pt) \
+  do {                             \
+  } while (0)
+#endif
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait: far above any legal wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxSpan = 30.0f;      // largest log-decay span inside one chunk
@@ -390,6 +413,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   PrepScalars* ps = reinterpret_cast<PrepScalars*>(sm + L::PS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#ifdef GDN_TC_TRACE
+  if (tid == 0 && (int)blockIdx.x == g_gdn_trace_cta) {
+    g_gdn_trace[16 * 2048] = clock64();
+    g_gdn_trace[16 * 2048 + 1] = globaltimer();
+  }
+#endif
   // The CTA stays resident and takes (sequence, head) units in order from a counter
   // (the work list is longest first; in a tree launch parents come before children),
   // running their chunks as one stream so that the pipeline does not drain between
@@ -533,6 +562,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float b0c = b0, b1c = b1;
         // the K / Q ring slot of chunk g-3 was released
         if (g >= 3) ok = wait(B_KQE0 + g % 3, ((g / 3) + 1) & 1, 0);
+        GDN_TRACE(0, g, 0);
         if (!ok) break;
         float* sc = slot_sc(g);
         sc[SC_G + lane] = s0;
@@ -570,6 +600,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
         kq_issued = g + 1;
+        GDN_TRACE(0, g, 1);
         // V has its own ring (two slots, released by chunk g-2's U product) and barrier, so
         // the K / Q tiles above never wait for it
         if (g >= 2) ok = wait(B_VE0 + (g & 1), ((g >> 1) + 1) & 1, 0);
@@ -587,6 +618,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
         v_issued = g + 1;
+        GDN_TRACE(0, g, 2);
         if (ulast) {
           ++g;
           break;
@@ -609,11 +641,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t id_w = idesc_bf16(128, 64, 1, 0);
 #pragma unroll 1
       for (int c = 0;; ++c) {
+        GDN_TRACE(1, c, 0);
         const int par = c & 1;
         // R and the W' accumulator were read by WG-B for chunk c-1
         uint64_t wl = with(kNone, B_T_READY0 + par, (c >> 1) & 1);
         if (c >= 1) wl = with(with(wl, B_R_FREE, (c - 1) & 1), B_W_FREE, (c - 1) & 1);
         if (!wait_all(wl, 10)) break;
+        GDN_TRACE(1, c, 1);
         tc_fence_after();
         const uint32_t kq = slot_kq(c), vv = slot_v(c);
         const uint32_t lbo_k = (L::NKA == 2) ? 16384u : (sbase + L::ZERO - kq);
@@ -625,7 +659,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_ss(tmem + TM_W, sdesc_add(dka, k * 2048u), sdesc_add(dtw, k * 32u), id_w, k != 0);
         }
         mma_commit(&bars[B_W_DONE]);  // W'^T may be converted while U is still running
+        GDN_TRACE(1, c, 2);
         if (!wait(B_VFULL0 + par, (c >> 1) & 1, 10)) break;
+        GDN_TRACE(1, c, 3);
         tc_fence_after();
         const uint32_t lbo_v = (L::NVA == 2) ? 8192u : (sbase + L::ZERO - vv);
         const uint64_t dva = sdesc(vv, lbo_v, 1024), dtb = sdesc(sbase + L::TB, 16, 1024);
@@ -637,6 +673,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mma_commit(&bars[B_U_DONE]);
         mma_commit(&bars[B_VE0 + par]);
+        GDN_TRACE(1, c, 4);
         if (fl & F_SLAST) break;
       }
       mma_commit(&bars[B_DRAIN1]);  // every MMA this thread issued has finished before exit
@@ -659,8 +696,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // U' reads the fp32 state itself: it needs chunk c-1's state update, or, when the
         // state starts over or is rescaled before this chunk, WG-B's write of it
         const int fl = sc_int(slot_sc(c), SC_FLAGS);
+        GDN_TRACE(2, c, 0);
         const bool s_written = (fl & (F_UFIRST | F_EAGER)) != 0;
         if (!(s_written ? wait(B_S_READY, c & 1, 4) : wait(B_STATE_DONE, (c - 1) & 1, 4))) break;
+        GDN_TRACE(2, c, 1);
         tc_fence_after();
         const bool last = cscal[c % 3].slast;  // read now: the buffer is reused after this chunk
         const uint32_t kq = slot_kq(c);
@@ -678,11 +717,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         kk != 0 || !vz);
         }
         mma_commit(&bars[B_UP_DONE]);
+        GDN_TRACE(2, c, 2);
         // O^T = S~^T Q^T (raw q tile, K-major) from the bf16 copy of the state, once the
         // last epilogue has read O
         uint64_t ol = with(kNone, B_S_READY, c & 1);
         if (c >= 1) ol = with(ol, B_EPI_DONE, (c - 1) & 1);
         if (!wait_all(ol, 4)) break;
+        GDN_TRACE(2, c, 3);
         tc_fence_after();
         if (zf && want_o) {
           const uint64_t dq = sdesc(kq + 8192u, 16, 1024);
@@ -694,6 +735,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!wait(B_UOPS_READY, c & 1, 7)) {
           break;
         }
+        GDN_TRACE(2, c, 4);
         tc_fence_after();
         // S~^T += (U' s)^T K : A from TMEM (hi, then lo), B = K MN-major (N = d_k)
         const uint64_t dkn = sdesc(kq, (L::NKA == 2) ? 16384u : 16u, 1024);
@@ -701,6 +743,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kk = 0; kk < 8; ++kk)  // hi (kk < 4), then lo
           mma_ts(tmem + TM_S, tmem + TM_UH + kk * 8u, sdesc_add(dkn, (kk & 3) * 2048u), id_st, kk != 0 || zf);
         mma_commit(&bars[B_STATE_DONE]);
+        GDN_TRACE(2, c, 5);
         // O^T += (U' s)^T M^T : B = M K-major [i][j]; the hi part of U' s only, since
         // this term reaches the output alone (M itself is bf16)
         const uint64_t dm = sdesc(sbase + L::M0 + par * 8192u, 16, 1024);
@@ -711,6 +754,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mma_commit(&bars[B_O_DONE]);
         mma_commit(&bars[B_MFREE0 + par]);
+        GDN_TRACE(2, c, 6);
         if (last) break;
       }
       mma_commit(&bars[B_DRAIN2]);
@@ -742,6 +786,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               mma_ss(tmem + TM_KQ, d, d, id_kq, kk != 0);
             }
             mma_commit(&bars[B_KQ_DONE]);
+            GDN_TRACE(3, c, 0);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -768,6 +813,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_RQ0 + c % 3]);
+        GDN_TRACE(3, c, 1);
         if (sc_int(sc, SC_FLAGS) & F_SLAST) break;
       }
       if (lane == 0) {  // every MMA this thread issued has finished before exit
@@ -794,6 +840,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (c >= 2) wl = with(wl, B_MFREE0 + par, ((c >> 1) + 1) & 1);
         if (c >= 3) wl = with(wl, B_CSF0 + c % 3, ((c / 3) + 1) & 1);
         bool ok = wait_all(wl, 8);
+        GDN_TRACE(4, c, 0);
         if (named_bar_or(1, 256, !ok || *abort_flag)) break;
         tc_fence_after();
         const float* sc = slot_sc(c);
@@ -837,6 +884,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_bar_sync(1, 256);
         if (wa == 0) mbar_arrive(&bars[B_KQ_FREE]);  // [K;Q] K^T is in registers
+        GDN_TRACE(4, c, 1);
         // A above the block diagonal (rows 0-31, columns 32-63) is never read, and M there is
         // always zero (cleared once at the start): those two warps have nothing to write
         const bool upper = hf == 1 && (Ln & 63) < 32;
@@ -871,12 +919,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         fence_proxy_async_smem();
+        GDN_TRACE(4, c, 2);
         // T_b / T_w of chunk c-1 have been read by its W and U products (the solve
         // overwrites them); A is complete once every thread passes this barrier
         ok = c < 1 || wait(B_U_DONE, (c - 1) & 1, 9);
         if (named_bar_or(1, 256, !ok || *abort_flag)) break;
+        GDN_TRACE(4, c, 3);
         // ---- T = (I + A)^-1
         solve_unit_lower(Abuf, Tbuf, wa);
+        GDN_TRACE(4, c, 4);
         // ---- T_b = T diag(beta) as bf16 hi + lo; T_w = T diag(tw)
         {
           const int ti = wa & 63, qq = wa >> 6;  // row ti, columns [16 qq, 16 qq + 16)
@@ -927,6 +978,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (wa == 0) {
           mbar_arrive(&bars[B_T_READY0 + par]);
           mbar_arrive(&bars[B_P1_DONE0 + par]);
+          GDN_TRACE(4, c, 5);
         }
         if (last) break;
       }
@@ -1014,6 +1066,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = wait_all(with(with(kNone, B_P1_DONE0 + (c & 1), (c >> 1) & 1), B_UP_DONE, c & 1), 12);
         if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
+        GDN_TRACE(12, c, 0);
 #pragma unroll 1
         for (int hb = 0; hb < 2; ++hb) {  // columns j in [32 hb, 32 hb + 32)
           uint32_t u[32];
@@ -1035,6 +1088,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (wb == 0) {
           mbar_arrive(&bars[B_R_FREE]);
           mbar_arrive(&bars[B_UOPS_READY]);
+          GDN_TRACE(12, c, 1);
         }
         more = !cs.slast;
         un_c = cs.n;
@@ -1051,6 +1105,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = wait(B_W_DONE, cn & 1, 15);
         if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
+        GDN_TRACE(12, c + 1, 2);
         // (chunk c's U' product, the buffer's last reader, finished before the split above)
         const uint32_t wcol = sbase + L::WP + (uint32_t)(wb >> 5) * 8192u + (uint32_t)(wb & 3) * 4u;
         const uint32_t wch = (uint32_t)((wb >> 2) & 7);  // 16-byte chunk of the row before the swizzle
@@ -1075,6 +1130,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (wb == 0) {
           mbar_arrive(&bars[B_W_FREE]);
           mbar_arrive(&bars[B_WCONV0 + pn]);
+          GDN_TRACE(12, c + 1, 3);
         }
       }
       if (more || c >= 0) {
@@ -1088,6 +1144,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = wait_all(wl, 11);
         if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
+        GDN_TRACE(12, c + 1, 4);
         if (!more || (sc_int(sc, SC_FLAGS) & F_UFIRST)) {
           // chunk cn starts a unit (or there is none): the one that ended with chunk c is complete
           if (c >= 0) store_final(un_c, uh_c, mu_c);
@@ -1123,6 +1180,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_before();
         named_bar_sync(2, 128);
         if (wb == 0) mbar_arrive(&bars[B_S_READY]);
+        GDN_TRACE(12, c + 1, 5);
       }
       if (c >= 0) {
         // ---- epilogue: out_i = co_i O^T_i, staged in shared memory and written by tensor
@@ -1139,6 +1197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = wait_all(with(with(kNone, B_O_DONE, c & 1), B_RQ0 + c % 3, (c / 3) & 1), 13);
         if (named_bar_or(2, 128, !ok || *abort_flag)) break;
         tc_fence_after();
+        GDN_TRACE(12, c, 6);
         const int m = cs.m;
         const long long t0 = cs.t0;
         const uint32_t stg = slot_kq(c);
@@ -1190,6 +1249,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(&bars[B_EPI_DONE]);
             mbar_arrive(&bars[B_CSF0 + c % 3]);
           }
+          GDN_TRACE(12, c, 7);
           if (m == 64) {
             if (wb == 0) {
 #pragma unroll
@@ -1267,6 +1327,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+#ifdef GDN_TC_TRACE
+  if (tid == 0 && (int)blockIdx.x == g_gdn_trace_cta) {
+    g_gdn_trace[16 * 2048 + 2] = clock64();
+    g_gdn_trace[16 * 2048 + 3] = globaltimer();
+  }
+#endif
 }
 
 // ---------------------------------------------------------------- host side
@@ -1386,3 +1452,18 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
 }
 
 }  // namespace gdn
+
+#ifdef GDN_TC_TRACE
+// Accessors of the tracing build (declared in include/gdn_trace.h).
+extern "C" int gdn_trace_set_cta(int cta) {
+  return (int)cudaMemcpyToSymbol(gdn::g_gdn_trace_cta, &cta, sizeof(int));
+}
+extern "C" int gdn_trace_clear(void) {
+  static unsigned long long zeros[16 * 2048 + 4];
+  return (int)cudaMemcpyToSymbol(gdn::g_gdn_trace, zeros, sizeof(zeros));
+}
+extern "C" int gdn_trace_read(unsigned long long* host) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  return (int)cudaMemcpyFromSymbol(host, gdn::g_gdn_trace, sizeof(unsigned long long) * (16 * 2048 + 4));
+}
+#endif

@@ -396,3 +396,10 @@ def test_segment_plan_and_workspace_host_logic():
     assert gdn.gdn_segment_plan(_long_desc(16384), sms) == (4, 2176, 4736)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_segment_plan(_long_desc(16384), 0)
+
+
+def test_regular_library_has_no_trace_code():
+    """The per-role clock trace (include/gdn_trace.h) exists only in the tracing build."""
+    lib = gdn.load_library()
+    for name in ("gdn_trace_set_cta", "gdn_trace_clear", "gdn_trace_read"):
+        assert not hasattr(lib, name), name
