@@ -38,7 +38,7 @@ GDN_NOALLOC_MAX_SEQS = 16384  # include/gdn.h
 STATUS_NAMES = ["GDN_OK", "GDN_ERR_NULL", "GDN_ERR_SHAPE", "GDN_ERR_DTYPE", "GDN_ERR_ALIGN",
                 "GDN_ERR_SEQLENS", "GDN_ERR_STATE_INDEX", "GDN_ERR_ALIAS", "GDN_ERR_WORKSPACE",
                 "GDN_ERR_ARCH", "GDN_ERR_CUDA", "GDN_ERR_DEVICE_TIMEOUT", "GDN_ERR_PARENT",
-                "GDN_ERR_VALUE"]
+                "GDN_ERR_VALUE", "GDN_ERR_BOUNDS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()

@@ -5,9 +5,12 @@ then linked into one shared library with the CUDA runtime linked statically
 and no other dependency (the driver entry points the tensor-core kernel needs
 are fetched at run time). Run as a module or call build().
 
-build(trace=True) makes a second library, libgdn_trace.so, from the same sources
-with -DGDN_TC_TRACE: the chunk kernel then records per-role clock stamps
-(include/gdn_trace.h). It is for profiling only; nothing loads it by default.
+Two more libraries come from the same sources for diagnosis only (nothing loads
+them by default): build(trace=True) makes libgdn_trace.so with -DGDN_TC_TRACE (the
+chunk kernel records per-role clock stamps, include/gdn_trace.h), and
+build(checked=True) makes libgdn_checked.so with -DGDN_CHECKED (every global index
+the kernels compute from their inputs is checked against its buffer; a failure
+reports GDN_ERR_BOUNDS and skips the access).
 """
 from __future__ import annotations
 
@@ -23,6 +26,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libgdn.so")
 TRACE_LIB = os.path.join(HERE, "libgdn_trace.so")
+CHECKED_LIB = os.path.join(HERE, "libgdn_checked.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -52,15 +56,17 @@ def up_to_date(lib: str = LIB) -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
-    lib = TRACE_LIB if trace else LIB
+def build(force: bool = False, verbose: bool = False, trace: bool = False, checked: bool = False) -> str:
+    if trace and checked:
+        raise ValueError("one diagnostic build at a time")
+    lib = TRACE_LIB if trace else CHECKED_LIB if checked else LIB
     if not force and up_to_date(lib):
         return lib
     nvcc = _nvcc()
-    bdir = os.path.join(BUILD_DIR, "trace") if trace else BUILD_DIR
+    bdir = os.path.join(BUILD_DIR, "trace" if trace else "checked") if (trace or checked) else BUILD_DIR
     os.makedirs(bdir, exist_ok=True)
     objs = []
-    extra = ["-DGDN_TC_TRACE"] if trace else []
+    extra = ["-DGDN_TC_TRACE"] if trace else ["-DGDN_CHECKED"] if checked else []
 
     def compile_one(src):
         obj = os.path.join(bdir, os.path.basename(src) + ".o")

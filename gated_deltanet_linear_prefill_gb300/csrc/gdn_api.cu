@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_
     int64_t nc = (eos - bos + kChunk - 1) / kChunk;
     const int bin = (int)(nc < kBins - 1 ? nc : kBins - 1);
     const int pos = atomicAdd(&hist[bin], 1);
-    order[pos] = n;
+    if (GDN_IN_BOUNDS(p.status, pos >= 0 && pos < N, 0x201u)) order[pos] = n;
   }
   if (!tree) return;
   // the other sequences after the roots, in index order (a block-wide scan per pass)
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_
       if (w < warp) before += warp_tot[w];
       total += warp_tot[w];
     }
-    if (f) order[base + before + incl - 1] = n;
+    if (f && GDN_IN_BOUNDS(p.status, base + before + incl - 1 < N, 0x202u)) order[base + before + incl - 1] = n;
     base += total;
   }
 }
@@ -269,6 +269,7 @@ extern "C" const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
     case GDN_ERR_PARENT: return "GDN_ERR_PARENT: a parent index outside [-1, n) (device check)";
     case GDN_ERR_VALUE: return "GDN_ERR_VALUE: an argument outside its range";
+    case GDN_ERR_BOUNDS: return "GDN_ERR_BOUNDS: an index outside its buffer (bounds-checked build)";
   }
   return "unknown gdn_status";
 }

@@ -81,6 +81,20 @@ __device__ __forceinline__ void report(Status* st, uint32_t code, uint32_t detai
   if (atomicCAS(&st->code, 0u, code) == 0u) st->detail = detail;
 }
 
+// Bounds checks of the bounds-checked build (-DGDN_CHECKED, libgdn_checked.so, the
+// stand-in for a memory checker): a failed check reports GDN_ERR_BOUNDS with the site
+// as detail, and the access it guards is skipped. The regular build compiles the
+// checks away: there every index is in range by construction (clamped bounds, guards).
+__device__ __forceinline__ bool check_bounds(Status* st, bool ok, uint32_t site) {
+  if (!ok) report(st, GDN_ERR_BOUNDS, site);
+  return ok;
+}
+#ifdef GDN_CHECKED
+#define GDN_IN_BOUNDS(status, cond, site) ::gdn::check_bounds((status), (cond), (site))
+#else
+#define GDN_IN_BOUNDS(status, cond, site) true
+#endif
+
 __device__ __forceinline__ float load_gate(const void* p, int64_t idx, int is_f32) {
   return is_f32 ? reinterpret_cast<const float*>(p)[idx]
                 : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[idx]);

@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
 #pragma unroll 1
     while (ok && cur < total_units) {
-      int n = p.order[cur / p.h_v];
+      int n = GDN_IN_BOUNDS(p.status, cur / p.h_v < p.num_seqs, 0x101u) ? p.order[cur / p.h_v] : 0;
       if (n < 0 || n >= p.num_seqs) {  // never expected: the prep kernel writes a permutation
         if (lane == 0) report(p.status, GDN_ERR_SEQLENS, (uint32_t)cur);
         n = 0;
@@ -517,7 +517,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         {
           const int64_t avail = len - start;
           const int64_t i0 = (bos + start + lane) * p.h_v + h, i1 = i0 + 32 * (int64_t)p.h_v;
-          const bool in0 = lane < avail, in1 = lane + 32 < avail;
+          const bool in0 = lane < avail && GDN_IN_BOUNDS(p.status, bos + start + lane < p.total_tokens, 0x102u);
+          const bool in1 =
+              lane + 32 < avail && GDN_IN_BOUNDS(p.status, bos + start + lane + 32 < p.total_tokens, 0x102u);
           if constexpr (GF32) {
             const float* gg = reinterpret_cast<const float*>(p.g);
             const float* bb = reinterpret_cast<const float*>(p.beta);
@@ -992,6 +994,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // launch the unit's children may then start from it.
     auto store_final = [&](int un, int uh, float umu) {
       if (!p.final_state) return;
+      if (!GDN_IN_BOUNDS(p.status, un >= 0 && un < p.num_seqs && uh >= 0 && uh < p.h_v, 0x103u)) return;
       float* fs = p.final_state + ((size_t)un * p.h_v + uh) * DK * DV;
 #pragma unroll 1
       for (int xb = 0; xb < DK / 32; ++xb) {
@@ -1005,7 +1008,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (p.parent) {
         named_bar_sync(2, 128);  // every thread's stores before the release
-        if (wb == 0) release_flag(&p.ready[(size_t)un * p.h_v + uh]);
+        if (wb == 0) release_flag(&p.ready[(size_t)un * p.h_v + uh]);  // (un, uh checked above)
       }
     };
     // A unit's starting state -> S~^T in TMEM (lane d_v, column d_k), mu = 1: an
@@ -1027,6 +1030,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int64_t slot = state_slot(p, un);
       const float* s0 = par >= 0 ? p.final_state + ((size_t)par * p.h_v + uh) * DK * DV
                                  : (slot >= 0 ? p.initial_state + ((size_t)slot * p.h_v + uh) * DK * DV : nullptr);
+      if (s0 && !GDN_IN_BOUNDS(p.status,
+                               uh >= 0 && uh < p.h_v && (par >= 0 ? par < p.num_seqs : slot < p.num_state_slots),
+                               0x104u))
+        s0 = nullptr;
       if (!s0) return true;  // a zero state: the first state update overwrites S~ outright
 #pragma unroll 1
       for (int xb = 0; xb < DK / 32; ++xb) {
@@ -1264,7 +1271,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const uint4 x = *reinterpret_cast<const uint4*>(
                   sm + (stg - sbase) + (pc >> 3) * 8192 + sw128((uint32_t)r, (uint32_t)(pc & 7)));
               char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + r) * p.h_v + cs.h) * DV) * osz;
-              *reinterpret_cast<uint4*>(dst + pc * 16) = x;
+              if (GDN_IN_BOUNDS(p.status, t0 + r < p.total_tokens && cs.h < p.h_v, 0x105u))
+                *reinterpret_cast<uint4*>(dst + pc * 16) = x;
             }
             named_bar_sync(2, 128);  // every thread has read the tiles
             if (wb == 0) mbar_arrive(&bars[B_KQE0 + c % 3]);
@@ -1302,7 +1310,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int r = idx >> pshift, pc = idx & (pieces - 1);
                 const uint4 x = *reinterpret_cast<const uint4*>(stage + r * DV * 4 + pc * 16);
                 char* dst = reinterpret_cast<char*>(p.out) + (((size_t)(t0 + p0 + r) * p.h_v + cs.h) * DV) * osz;
-                *reinterpret_cast<uint4*>(dst + pc * 16) = x;
+                if (GDN_IN_BOUNDS(p.status, t0 + p0 + r < p.total_tokens && cs.h < p.h_v, 0x106u))
+                  *reinterpret_cast<uint4*>(dst + pc * 16) = x;
               }
             }
             if (wb == 0) bulk_commit();  // empty for a copied pass

@@ -69,7 +69,9 @@ typedef enum {
   GDN_ERR_CUDA = 10,          /* a CUDA runtime call failed (launch, query, copy) */
   GDN_ERR_DEVICE_TIMEOUT = 11, /* device: a bounded wait gave up */
   GDN_ERR_PARENT = 12,         /* device: a parent index outside [-1, n) (gdn_prefill_tree) */
-  GDN_ERR_VALUE = 13           /* an argument outside its range (gdn_gated_rmsnorm: eps) */
+  GDN_ERR_VALUE = 13,          /* an argument outside its range (gdn_gated_rmsnorm: eps) */
+  GDN_ERR_BOUNDS = 14          /* device, bounds-checked build only (libgdn_checked.so): an index
+                                  outside its buffer; the access was skipped */
 } gdn_status;
 
 /* Flags. */

@@ -403,3 +403,8 @@ def test_regular_library_has_no_trace_code():
     lib = gdn.load_library()
     for name in ("gdn_trace_set_cta", "gdn_trace_clear", "gdn_trace_read"):
         assert not hasattr(lib, name), name
+
+
+def test_bounds_status_is_named():
+    assert gdn.STATUS_NAMES[14] == "GDN_ERR_BOUNDS"
+    assert b"GDN_ERR_BOUNDS" in gdn.load_library().gdn_status_string(14)

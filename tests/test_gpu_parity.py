@@ -279,3 +279,16 @@ def test_repeat_runs_bitwise():
     z, wt = workloads.norm_inputs(493, 4, 128, seed=4)
     ys = [gdn.gated_rmsnorm(outs[0][2], z.cuda(), wt.cuda()) for _ in range(2)]
     assert torch.equal(ys[0], ys[1])
+
+
+@pytest.mark.parametrize("lengths", [[65], [80], [96], [65, 72, 80, 88, 91, 94, 96]],
+                         ids=["lone65", "lone80", "lone96", "seven_paths"])
+def test_short_paths_two_chunks(lengths):
+    """Row F4's case: candidate paths of 65-96 tokens (two chunks each), alone and as
+    the seven-path batch `bench.py --latency` times, at the long-prompt workload's
+    shape (16 q/k and 32 value heads, d 128, bf16 gates), against the oracle."""
+    w = workloads.random_workload(lengths, h_qk=16, h_v=32, d_k=128, d_v=128, seed=90 + len(lengths),
+                                  gate_dtype=torch.bfloat16, name=f"short paths {lengths}")
+    o_ref, s_ref = oracle.run_workload(w)
+    o, s = run_lib(w, "tc")
+    check(errors(o, s, o_ref, s_ref), "tc", label=f"short paths {lengths}")
