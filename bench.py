@@ -476,6 +476,20 @@ def run_gdn(args, world, rank, local):
             "value": tot_tok / tot_s, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"the whole batch ({w.num_seqs} sequences, {w.total_tokens} tokens, "
                       f"{w.h_v} heads), fp64 recurrence, {passes} passes in {tot_s:.1f} s"}
+    if rank == 0 and world == 1 and not args.no_long and args.kernel == "tc" and args.subset_seqs == 0:
+        # the long-prompt workload (one 16,384-token prompt as one call and as 48 calls), so
+        # that the default run's record holds it too; `bench.py --long` prints it in full
+        la = argparse.Namespace(**vars(args))
+        la.steps, la.warmup, la.soak_s, la.layers = 10, 3, 0.5, 48
+        la.no_cpu_baseline = True
+        ll = measure_long(la)
+        line["long_prompt"] = {
+            "workload": ll["config"]["workload"], "metric": ll["metric"], "unit": ll["unit"],
+            "value": ll["value"], "ms_per_call": ll["ms_per_step"],
+            "ms_per_call_48_layers": ll["layers48"]["ms_per_call"],
+            "roofline_frac": ll["roofline"]["frac"], "segment_scan": ll["config"]["segment_scan"],
+            "e2e": ll["e2e"], "gpu_launches": ll["gpu_launches"], "clocks": ll["clocks"],
+            "full_line": "python bench.py --long"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -927,10 +941,16 @@ def device_layer_inputs(layer: int, device, T=16384, h_qk=16, h_v=32, d=128):
 
 
 def run_long_bench(args):
+    """`--long`: prints measure_long's JSON line."""
+    print(json.dumps(measure_long(args)), flush=True)
+
+
+def measure_long(args):
     """The long-prompt workload: one 16,384-token prompt, 16 q/k and 32 v heads, head
     dim 128, bf16 inputs and output, fp32 initial and final state. Times one call
     (layer 0's inputs, resident) and 48 back-to-back calls, one per linear-attention
-    layer, each on its own input set. One JSON line; value = tokens/s of one call."""
+    layer, each on its own input set. Returns one JSON-line dict; value = tokens/s of
+    one call."""
     import gated_deltanet_linear_prefill_gb300 as gdn
     if not torch.cuda.is_available():
         raise SystemExit("bench.py --long needs a CUDA device")
@@ -1081,7 +1101,7 @@ def run_long_bench(args):
             "value": T / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"one call (layer 0: {T} tokens, all {w.h_v} heads), fp64 recurrence, {dt:.1f} s",
             "s_per_48_calls": 48 * dt, "s_per_48_calls_kind": "the one-call time x 48"}
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def main(argv=None):
@@ -1107,6 +1127,8 @@ def main(argv=None):
                     help="time the GDN input prep (conv + SiLU + split, gates) on the 74-prompt batch")
     ap.add_argument("--long", action="store_true",
                     help="time one 16,384-token prompt: one call and 48 back-to-back calls (48 layers)")
+    ap.add_argument("--no-long", action="store_true",
+                    help="leave the long-prompt workload out of the default run's line")
     ap.add_argument("--layers", type=int, default=48,
                     help="--long: input sets drawn and timed back to back (48 = every linear-attention "
                          "layer; fewer only for short profiling runs)")
