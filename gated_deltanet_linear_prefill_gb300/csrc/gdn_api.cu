@@ -143,8 +143,52 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(Params p, int32_
   }
 }
 
+// The prep kernel for a batch of at most 32 sequences outside a tree launch: one warp,
+// lane n checks sequence n and places it by rank (more chunks first, then lower index).
+// The same checks and the same kind of order as gdn_prep_kernel, without its 4096-bin
+// histogram and block-wide scans, which set a small batch's latency.
+__global__ void __launch_bounds__(32) gdn_prep_small_kernel(Params p, int32_t* order) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int n = threadIdx.x, N = p.num_seqs;
+  if (n == 0) {
+    if (!p.keep_status) {
+      p.status->code = 0u;
+      p.status->detail = 0u;
+    }
+    p.status->units_done = 0u;
+    p.status->next_unit = 0u;
+  }
+  __syncwarp();
+  int64_t nc = -1;  // lanes past N rank last and write nothing
+  if (n < N) {
+    if (!p.seq_rows) {
+      const int64_t b = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
+      if ((n == 0 && b != 0) || e < b || (n == N - 1 && e != p.total_tokens) ||
+          (p.max_seqlen > 0 && e - b > p.max_seqlen))
+        report(p.status, GDN_ERR_SEQLENS, (uint32_t)n);
+    }
+    if (p.initial_state && p.state_index) {
+      const int32_t si = p.state_index[n];
+      if (si < -1 || si >= p.num_state_slots) report(p.status, GDN_ERR_STATE_INDEX, (uint32_t)n);
+    }
+    int64_t bos, eos;
+    seq_bounds(p, n, bos, eos);
+    nc = (eos - bos + kChunk - 1) / kChunk;
+  }
+  int rank = 0;
+#pragma unroll 1
+  for (int m = 0; m < 32; ++m) {
+    const int64_t o = __shfl_sync(0xffffffffu, nc, m);
+    rank += (o > nc || (o == nc && m < n)) ? 1 : 0;
+  }
+  if (n < N && GDN_IN_BOUNDS(p.status, rank < N, 0x203u)) order[rank] = n;
+}
+
 cudaError_t launch_prep(const Params& p, cudaStream_t stream) {
-  gdn_prep_kernel<<<1, kPrepThreads, 0, stream>>>(p, const_cast<int32_t*>(p.order));
+  if (!p.parent && p.num_seqs <= 32)
+    gdn_prep_small_kernel<<<1, 32, 0, stream>>>(p, const_cast<int32_t*>(p.order));
+  else
+    gdn_prep_kernel<<<1, kPrepThreads, 0, stream>>>(p, const_cast<int32_t*>(p.order));
   return cudaGetLastError();
 }
 
