@@ -143,8 +143,9 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream);
 //
 // A single sequence of T rows leaves most SMs idle (one chain of chunks per value
 // head). The state after each segment is an affine map of the state before it,
-// S -> Phi_j S + Delta_j, so the sequence is cut into G segments (segment 0 of a rows,
-// the others of b rows, the last possibly shorter) and run in two chunk-kernel launches:
+// S -> Phi_j S + Delta_j, so the sequence is cut into G segments (segments 1 .. G-1 of
+// b rows each, segment 0 the a = T - (G-1) b before them) and run in two chunk-kernel
+// launches:
 //   A: segment 0 from the true starting state (its outputs are final), Delta_j (segments
 //      1 .. G-2 from a zero state) and Phi_j (the same segments with V = 0 from S = I);
 //   combine: S_1 = state after segment 0, S_{j+1} = Phi_j S_j + Delta_j;
@@ -152,7 +153,7 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream);
 struct SegPlan {
   int G;       // segments (0: run the sequence in one launch)
   int64_t a;   // rows of segment 0
-  int64_t b;   // rows of every later segment but the last
+  int64_t b;   // rows of every later segment (a + (G-1) b = T)
 };
 constexpr int kSegMaxG = 8;
 constexpr int64_t kSegMinTokens = 4096;

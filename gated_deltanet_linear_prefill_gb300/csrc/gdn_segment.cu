@@ -48,7 +48,7 @@ static SegPlan seg_plan_search(int64_t T, int h_v, int sms) {
   int64_t best_cost = serial * 85 / 100 - kOverhead;
   for (int G = 3; G <= kSegMaxG; ++G) {
     for (int ratio = 2; ratio <= 4; ++ratio) {  // a = b * ratio / 4
-      // a + (G - 1) b = T with b a multiple of the chunk; the last segment takes the rest
+      // a + (G - 1) b = T with b a multiple of the chunk: segment 0 takes the rest
       const double bf = (double)T / ((double)(G - 1) + ratio / 4.0);
       const int64_t b = ((int64_t)bf + kChunk - 1) / kChunk * kChunk;
       const int64_t a = T - (int64_t)(G - 1) * b;
@@ -137,7 +137,7 @@ __global__ void gdn_seg_setup_kernel(Params p, SegPlan plan, float* slots, int64
       rows_a[2 * n + 1] = r1;
       sidx_a[n] = si;
     }
-    // launch C: segments 1 .. G-1 (the last one ends at T)
+    // launch C: segments 1 .. G-1 (b rows each; the last ends at T)
     for (int n = threadIdx.x; n < G - 1; n += blockDim.x) {
       const int64_t r0 = a + (int64_t)n * b;
       rows_c[2 * n] = r0;

@@ -162,8 +162,8 @@ gdn_status gdn_prefill_varlen(const void* q, const void* k, const void* v, const
 /*
  * The segment plan gdn_prefill_varlen takes for this descriptor on a device with `sms`
  * SMs: *segments = G, the number of segments (0: one launch), *rows0 = the rows of
- * segment 0, *rows = the rows of every later segment but the last, which ends at
- * total_tokens. G > 0 only when the descriptor qualifies (gdn_workspace_bytes) and
+ * segment 0, *rows = the rows of each of the G - 1 later segments (rows0 + (G - 1) rows
+ * = total_tokens). G > 0 only when the descriptor qualifies (gdn_workspace_bytes) and
  * desc->workspace_bytes holds the larger size. The plan minimises the two launches'
  * makespan in chunk periods (longest-first list scheduling of whole (segment, head)
  * units) and is used only when it beats one launch by more than 15%. Host only, no
