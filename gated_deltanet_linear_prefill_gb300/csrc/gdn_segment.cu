@@ -182,13 +182,32 @@ __global__ void __launch_bounds__(2 * DK) gdn_seg_combine_kernel(Params p, SegPl
   const size_t sz = (size_t)DK * dv, hs = (size_t)p.h_v * sz;
   const int tid = threadIdx.x, cg = tid % 8, rg = tid / 8;
   const float* s1 = fin_a + (size_t)h * sz;
-  constexpr int NS = DK * 8 / kCombThreads;  // float4 pieces of the slice per thread
+  constexpr int NS = DK * 8 / kCombThreads;      // float4 pieces of the slice per thread
+  constexpr int NP = DK * DK / 4 / kCombThreads;  // float4 pieces of Phi_j per thread
+  // Phi_j and Delta_j of the next step are loaded into registers while the current
+  // step computes (all of a step's loads in flight at once). Piece u of Phi_j holds
+  // Phi_j[r][m .. m+3] with r = i % DK, i = tid + u * threads: a warp covers 32 rows,
+  // so that its transposed stores fill 32 banks.
+  float4 pf[NP], pd[R];
+  auto load_step = [&](int j) {
+    const float* phi = fin_a + (size_t)(G - 2 + j) * hs + (size_t)h * sz;  // Phi_j [DK][DK]
+    const float* del = fin_a + (size_t)j * hs + (size_t)h * sz;             // Delta_j [DK][d_v]
+#pragma unroll
+    for (int u = 0; u < NP; ++u) {
+      const int i = tid + u * kCombThreads;
+      pf[u] = *reinterpret_cast<const float4*>(&phi[(size_t)(i % DK) * DK + 4 * (i / DK)]);
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      pd[i] = *reinterpret_cast<const float4*>(&del[(size_t)(R * rg + i) * dv + c0 + 4 * cg]);
+  };
   float4 xs[NS];
 #pragma unroll
-  for (int u = 0; u < NS; ++u) {  // every load in flight before the first store
+  for (int u = 0; u < NS; ++u) {
     const int i = tid + u * kCombThreads, r = i / 8, q = i % 8;
     xs[u] = *reinterpret_cast<const float4*>(&s1[(size_t)r * dv + c0 + 4 * q]);
   }
+  if (G >= 3) load_step(1);
 #pragma unroll
   for (int u = 0; u < NS; ++u) {
     const int i = tid + u * kCombThreads, r = i / 8, q = i % 8;
@@ -196,40 +215,25 @@ __global__ void __launch_bounds__(2 * DK) gdn_seg_combine_kernel(Params p, SegPl
     *reinterpret_cast<float4*>(&s_c[(size_t)h * sz + (size_t)r * dv + c0 + 4 * q]) = xs[u];
   }
   for (int j = 1; j <= G - 2; ++j) {
-    const float* phi = fin_a + (size_t)(G - 2 + j) * hs + (size_t)h * sz;  // Phi_j [DK][DK]
-    const float* del = fin_a + (size_t)j * hs + (size_t)h * sz;             // Delta_j [DK][d_v]
     __syncthreads();  // the previous Phi is no longer read; S_j is in place
-    // piece i holds Phi_j[r][m .. m+3] with r = i % DK (a warp covers 32 rows, so that
-    // its transposed stores fill 32 banks), eight loads in flight per thread at a time
-    constexpr int NP = DK * DK / 4 / kCombThreads, NB = NP;
-    static_assert(NP % NB == 0, "pieces per thread");
-#pragma unroll 1
-    for (int u0 = 0; u0 < NP; u0 += NB) {
-      float4 f[NB];
 #pragma unroll
-      for (int u = 0; u < NB; ++u) {
-        const int i = tid + (u0 + u) * kCombThreads;
-        f[u] = *reinterpret_cast<const float4*>(&phi[(size_t)(i % DK) * DK + 4 * (i / DK)]);
-      }
-#pragma unroll
-      for (int u = 0; u < NB; ++u) {
-        const int i = tid + (u0 + u) * kCombThreads, r = i % DK, m = 4 * (i / DK);
-        pht[(m + 0) * LDT + r] = f[u].x;
-        pht[(m + 1) * LDT + r] = f[u].y;
-        pht[(m + 2) * LDT + r] = f[u].z;
-        pht[(m + 3) * LDT + r] = f[u].w;
-      }
+    for (int u = 0; u < NP; ++u) {
+      const int i = tid + u * kCombThreads, r = i % DK, m = 4 * (i / DK);
+      pht[(m + 0) * LDT + r] = pf[u].x;
+      pht[(m + 1) * LDT + r] = pf[u].y;
+      pht[(m + 2) * LDT + r] = pf[u].z;
+      pht[(m + 3) * LDT + r] = pf[u].w;
     }
-    __syncthreads();
     float acc[R][4];
 #pragma unroll
     for (int i = 0; i < R; ++i) {
-      const float4 d4 = *reinterpret_cast<const float4*>(&del[(size_t)(R * rg + i) * dv + c0 + 4 * cg]);
-      acc[i][0] = d4.x;
-      acc[i][1] = d4.y;
-      acc[i][2] = d4.z;
-      acc[i][3] = d4.w;
+      acc[i][0] = pd[i].x;
+      acc[i][1] = pd[i].y;
+      acc[i][2] = pd[i].z;
+      acc[i][3] = pd[i].w;
     }
+    __syncthreads();
+    if (j + 1 <= G - 2) load_step(j + 1);
 #pragma unroll 8
     for (int m = 0; m < DK; ++m) {
       const float4 x = *reinterpret_cast<const float4*>(&sj[m * kCombCols + 4 * cg]);
