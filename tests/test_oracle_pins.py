@@ -74,7 +74,7 @@ def test_chunked_equals_recurrence_varlen_gqa_rectangular():
 
 
 # ---------------------------------------------------------------- exact arithmetic
-def test_exact_rational_recurrence_matches_north_star_formula():
+def test_exact_rational_recurrence_matches_the_defining_formula():
     """Three tokens, d_k=3, d_v=2, evaluated exactly with sympy from
     S_t = e^{g_t} (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T, o_t = scale S_t^T q_t.
     The keys are given un-normalised; the L2 normalisation is applied exactly
