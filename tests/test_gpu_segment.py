@@ -126,3 +126,39 @@ def test_segment_scan_dirty_workspace():
     o_ref, s_ref = oracle.run_workload(w)
     check(errors(runs[0][1].double().numpy(), runs[0][2].double().numpy(), o_ref, s_ref), "tc",
           label="segment scan dirty workspace")
+
+
+def test_segment_scan_in_a_cuda_graph():
+    """The segmented call (six kernels and a device copy) captures into a CUDA graph;
+    replaying it on changed inputs gives the same bits as direct calls."""
+    T = 4800
+    w1 = _workload(T, 2, 4, 128, torch.float32, torch.bfloat16, "slot", seed=74)
+    w2 = _workload(T, 2, 4, 128, torch.float32, torch.bfloat16, "slot", seed=75)
+    d1, d2, static = w1.to("cuda"), w2.to("cuda"), w1.to("cuda")
+    out = torch.empty(static.v.shape, dtype=torch.bfloat16, device="cuda")
+    fs = torch.empty((1, 4, 128, 128), dtype=torch.float32, device="cuda")
+    desc = gdn.make_desc(static.q, static.v, static.g, static.cu_seqlens, initial_state=static.initial_state)
+    assert gdn.gdn_segment_plan(desc, torch.cuda.get_device_properties(0).multi_processor_count)[0] == 0
+    ws = torch.empty(gdn.gdn_workspace_bytes(desc), dtype=torch.uint8, device="cuda")
+    desc.workspace, desc.workspace_bytes = ws.data_ptr(), ws.numel()
+    assert gdn.gdn_segment_plan(desc, torch.cuda.get_device_properties(0).multi_processor_count)[0] >= 3
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm up outside capture
+        assert gdn.gdn_prefill_varlen(static.q, static.k, static.v, static.g, static.beta, static.cu_seqlens,
+                                      static.initial_state, None, out, fs, desc, s) == gdn.GDN_OK
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        rc = gdn.gdn_prefill_varlen(static.q, static.k, static.v, static.g, static.beta, static.cu_seqlens,
+                                    static.initial_state, None, out, fs, desc, torch.cuda.current_stream())
+    assert rc == gdn.GDN_OK
+    for d in (d2, d1):
+        for name in ("q", "k", "v", "g", "beta", "initial_state"):
+            getattr(static, name).copy_(getattr(d, name))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref_o, ref_s = gdn.prefill_varlen(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, initial_state=d.initial_state)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_o)
+        assert torch.equal(fs, ref_s)
