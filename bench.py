@@ -656,7 +656,9 @@ def run_latency_bench(args):
     rng = np.random.default_rng(5)
     short = workloads.random_workload([int(x) for x in rng.integers(65, 97, 7)], h_qk=16, h_v=32,
                                       d_k=128, d_v=128, seed=5)
-    cases = {"cfg0_tiny_T128_d64": varlen_case(workloads.config(0)),
+    lone = workloads.random_workload([96], h_qk=1, h_v=1, d_k=128, d_v=128, seed=6)
+    cases = {"lone_unit_T96_1head": varlen_case(lone),
+             "cfg0_tiny_T128_d64": varlen_case(workloads.config(0)),
              "cfg1_single_T539": varlen_case(workloads.config(1)),
              "short_paths_7x65to96": varlen_case(short),
              "cfg3_prefix_tree_one_launch": tree_case()}
@@ -691,10 +693,12 @@ def run_latency_bench(args):
         graph = med(replay)
         res[name] = {"tokens": tokens, "us_per_call": plain, "us_per_graph_replay": graph}
     line = {"metric": "GDN prefill latency of small workloads (per call, one GB300)",
-            "value": res["cfg1_single_T539"]["us_per_graph_replay"], "unit": "us per call",
+            "value": min(res["cfg1_single_T539"]["us_per_call"], res["cfg1_single_T539"]["us_per_graph_replay"]),
+            "unit": "us per call",
             "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "dtype": "bf16", "data": "synthetic", "cases": res,
-            "config": {"workload": "cfg1_single_T539 (value); all cases under 'cases'",
+            "config": {"workload": "cfg1_single_T539 (value: the faster of a plain call and a graph replay); "
+                                   "all cases under 'cases'",
                        "timing": "median of per-call CUDA events, inputs resident"}}
     print(json.dumps(line))
 

@@ -9,6 +9,11 @@ are CUDA-clock cycles converted with the CTA's own clock rate; the stamps cost
 about 10% of the kernel's time, so the absolute period reads a little long.
 
     python -m gated_deltanet_linear_prefill_gb300.trace [--subset-seqs N] [--ctas 0,77]
+    python -m gated_deltanet_linear_prefill_gb300.trace --lengths 96 --heads 1 --ctas 0
+
+The second form traces a random batch of the given lengths (h_qk = h_v = heads,
+d 128) and prints every stamp of the CTA from its start: the latency of a short
+unit rather than a steady-state period.
 """
 from __future__ import annotations
 
@@ -106,7 +111,21 @@ def trace_workload(w, ctas, warmup=3):
         buf = buf.astype(np.int64)
         clk0, gt0, clk1, gt1 = buf[16 * 2048:]
         ghz = (clk1 - clk0) / max(1, gt1 - gt0)
+        trace_workload.start_clock = int(clk0)
         yield cta, buf[:16 * 2048].reshape(16, 256, 8), ghz, (gt1 - gt0) / 1e3
+
+
+def report_raw(T, start_clk, ghz, cta, cta_us, file=sys.stdout):
+    """Every stamp of one CTA in time order, in us from the CTA's start."""
+    print(f"CTA {cta}: {cta_us:.1f} us from start to end, clock {ghz:.3f} GHz", file=file)
+    evs = []
+    for (wp, pt), name in EVENTS.items():
+        for c in range(256):
+            if T[wp, c, pt] > 0:
+                evs.append(((T[wp, c, pt] - start_clk) / ghz / 1e3, f"chunk {c}: {name}"))
+    for t, name in sorted(evs):
+        print(f"    {t:8.2f}  {name}", file=file)
+    return evs
 
 
 def report(T, ghz, cta, cta_us, file=sys.stdout):
@@ -135,13 +154,22 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--subset-seqs", type=int, default=0, help="trace the first N sequences only")
     ap.add_argument("--ctas", default="0,77", help="comma-separated CTAs to trace (one launch each)")
+    ap.add_argument("--lengths", default="", help="comma-separated sequence lengths of a random batch")
+    ap.add_argument("--heads", type=int, default=1, help="q/k and value heads of the random batch")
     args = ap.parse_args(argv)
-    w = workloads.config(2)
-    if args.subset_seqs:
-        w = workloads.subset_sequences(w, list(range(args.subset_seqs)))
+    if args.lengths:
+        w = workloads.random_workload([int(x) for x in args.lengths.split(",")], h_qk=args.heads,
+                                      h_v=args.heads, d_k=128, d_v=128, seed=6, gate_dtype=torch.float32)
+    else:
+        w = workloads.config(2)
+        if args.subset_seqs:
+            w = workloads.subset_sequences(w, list(range(args.subset_seqs)))
     print(f"workload {w.name}: {w.num_seqs} sequences, {w.total_tokens} tokens, h_v {w.h_v}")
     for cta, T, ghz, cta_us in trace_workload(w, [int(x) for x in args.ctas.split(",")]):
-        report(T, ghz, cta, cta_us)
+        if args.lengths:
+            report_raw(T, trace_workload.start_clock, ghz, cta, cta_us)
+        else:
+            report(T, ghz, cta, cta_us)
 
 
 if __name__ == "__main__":

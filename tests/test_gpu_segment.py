@@ -162,3 +162,16 @@ def test_segment_scan_in_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(out, ref_o)
         assert torch.equal(fs, ref_s)
+
+
+def test_segment_scan_without_final_state():
+    """final_state may be NULL: the segmented call still writes every output, the
+    same bits as with it."""
+    w = _workload(4500, 2, 4, 128, torch.float32, torch.bfloat16, "none", seed=76)
+    d = w.to("cuda")
+    o1, s1 = gdn.prefill_varlen(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, check_device=True)
+    o2, s2 = gdn.prefill_varlen(d.q, d.k, d.v, d.g, d.beta, d.cu_seqlens, want_final_state=False,
+                                check_device=True)
+    torch.cuda.synchronize()
+    assert s2 is None
+    assert torch.equal(o1, o2)
