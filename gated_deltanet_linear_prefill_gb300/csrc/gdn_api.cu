@@ -461,6 +461,18 @@ extern "C" gdn_status gdn_prefill_varlen(const void* q, const void* k, const voi
     const gdn::SegPlan plan = gdn::seg_plan(p.total_tokens, p.h_v, sms);
     if (plan.G >= 3) return gdn::run_segmented(p, plan, (char*)desc->workspace, s);
   }
+  if (!(desc->flags & GDN_FLAG_SIMT) && p.total_tokens > 0 && p.num_seqs <= 32 && p.d_k == p.d_v) {
+    // A batch with at most one (sequence, value head) unit per SM needs no work list:
+    // CTA b takes unit b and checks its own sequence, and a memset of the status block
+    // replaces the prep kernel (one launch less on the latency of a small call).
+    int sms = 0;
+    if (gdn::device_sm_count(&sms) != cudaSuccess) return GDN_ERR_CUDA;
+    if ((long long)p.num_seqs * p.h_v <= sms) {
+      if (cudaMemsetAsync(p.status, 0, 4 * sizeof(uint32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+      p.direct = 1;
+      return gdn::launch_tc(p, s) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+  }
   if (launch_prep(p, s) != cudaSuccess) return GDN_ERR_CUDA;
   const cudaError_t e = (desc->flags & GDN_FLAG_SIMT) ? launch_simt(p, s) : launch_tc(p, s);
   if (e != cudaSuccess) return GDN_ERR_CUDA;

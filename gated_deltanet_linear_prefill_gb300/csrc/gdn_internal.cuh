@@ -66,6 +66,10 @@ struct Params {
   int vzero_from;
   int out_upto;
   int keep_status;
+  // Direct launch (a small batch, no prep kernel): CTA b takes unit b (grid = units), the
+  // units in index order, and checks its own sequence's cu_seqlens / state_index entries;
+  // the host has zeroed the status word.
+  int direct;
   int64_t total_tokens;
   int num_seqs;
   int max_seqlen;

@@ -398,9 +398,12 @@ __device__ __noinline__ void drain_loads(uint32_t bars, int kq_issued, int v_iss
 // ---------------------------------------------------------------- the kernel
 // OF32: fp32 output (else bf16); GF32: fp32 gates (else bf16). Template parameters,
 // so that each kernel holds only its own epilogue and gate loads.
-template <int DK, int DV, bool OF32, bool GF32, bool SEG>
+template <int DK, int DV, bool OF32, bool GF32, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gdn_tc_kernel(const Params p, const __grid_constant__ Tmaps tm) {
+  // instance: 0 the regular launch, 1 a segment launch (V-zero and no-output units), 2 a
+  // direct launch of a small batch (CTA b takes unit b, no work list)
+  constexpr bool SEG = MODE == 1, DIRECT = MODE == 2;
   using L = TcLayout<DK, DV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -449,7 +452,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // above touches only this CTA's own memory; the status block, the work counter and the
   // work list are read only after the prep grid has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0) *first_unit = (int)atomicAdd(&p.status->next_unit, 1u);
+  if (tid == 0) *first_unit = DIRECT ? (int)blockIdx.x : (int)atomicAdd(&p.status->next_unit, 1u);
+  if (DIRECT && tid == 32 && (int)blockIdx.x < total_units && blockIdx.x % p.h_v == 0) {
+    // a direct launch checks what the prep kernel would: this CTA's own sequence
+    const int n = (int)blockIdx.x / p.h_v;
+    const int64_t b = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
+    if ((n == 0 && b != 0) || e < b || (n == p.num_seqs - 1 && e != p.total_tokens) ||
+        (p.max_seqlen > 0 && e - b > p.max_seqlen))
+      report(p.status, GDN_ERR_SEQLENS, (uint32_t)n);
+    if (p.initial_state && p.state_index) {
+      const int32_t si = p.state_index[n];
+      if (si < -1 || si >= p.num_state_slots) report(p.status, GDN_ERR_STATE_INDEX, (uint32_t)n);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -489,6 +504,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // this chunk knows whether it is the CTA's last), not earlier: a CTA then holds a
     // second unit only briefly, and the work list keeps its longest-first order
     auto take_unit = [&]() {
+      if (DIRECT) return total_units;  // one unit per CTA
       int u = 0;
       if (lane == 0) u = (int)atomicAdd(&p.status->next_unit, 1u);
       return __shfl_sync(0xffffffffu, u, 0);
@@ -497,7 +513,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
 #pragma unroll 1
     while (ok && cur < total_units) {
-      int n = GDN_IN_BOUNDS(p.status, cur / p.h_v < p.num_seqs, 0x101u) ? p.order[cur / p.h_v] : 0;
+      int n = !GDN_IN_BOUNDS(p.status, cur / p.h_v < p.num_seqs, 0x101u) ? 0
+              : DIRECT ? cur / p.h_v : p.order[cur / p.h_v];
       if (n < 0 || n >= p.num_seqs) {  // never expected: the prep kernel writes a permutation
         if (lane == 0) report(p.status, GDN_ERR_SEQLENS, (uint32_t)cur);
         n = 0;
@@ -1390,7 +1407,7 @@ bool encode_out(CUtensorMap* m, void* base, int64_t T, int H, int D, bool f32) {
 }
 
 
-template <int DK, int DV, bool OF32, bool GF32, bool SEG>
+template <int DK, int DV, bool OF32, bool GF32, int MODE>
 cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   using L = TcLayout<DK, DV>;
   Tmaps tm;
@@ -1399,7 +1416,7 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
       !encode_rows(&tm.v, p.v, p.total_tokens, p.h_v, DV) ||
       !encode_out(&tm.o, p.out, p.total_tokens, p.h_v, DV, p.out_f32 != 0))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV, OF32, GF32, SEG>), (int)L::DYN_SMEM);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(&gdn_tc_kernel<DK, DV, OF32, GF32, MODE>), (int)L::DYN_SMEM);
   if (e != cudaSuccess) return e;
   const long long units = (long long)p.num_seqs * p.h_v;
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -1419,8 +1436,8 @@ cudaError_t launch_tc_dk(const Params& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gdn_tc_kernel<DK, DV, OF32, GF32, SEG>, p, tm);
+  cfg.numAttrs = MODE == 2 ? 0 : 1;  // a direct launch follows a memset, not the prep kernel
+  e = cudaLaunchKernelEx(&cfg, gdn_tc_kernel<DK, DV, OF32, GF32, MODE>, p, tm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1435,21 +1452,30 @@ cudaError_t launch_tc(const Params& p, cudaStream_t stream) {
   const int t = (p.out_f32 ? 2 : 0) + (p.gate_f32 ? 1 : 0);
   auto by_types = [&](auto dk, auto dv) {
     constexpr int K_ = decltype(dk)::value, V_ = decltype(dv)::value;
-    // segment launches (square states only) take the SEG instance
+    // segment and direct launches (square states only) take their own instances
     constexpr bool SQ = K_ == V_;
+    constexpr int SEGM = SQ ? 1 : 0, DIRM = SQ ? 2 : 0;
     if (SQ && p.seq_rows) {
       switch (t) {
-        case 0: return launch_tc_dk<K_, V_, false, false, SQ>(p, stream);
-        case 1: return launch_tc_dk<K_, V_, false, true, SQ>(p, stream);
-        case 2: return launch_tc_dk<K_, V_, true, false, SQ>(p, stream);
-        default: return launch_tc_dk<K_, V_, true, true, SQ>(p, stream);
+        case 0: return launch_tc_dk<K_, V_, false, false, SEGM>(p, stream);
+        case 1: return launch_tc_dk<K_, V_, false, true, SEGM>(p, stream);
+        case 2: return launch_tc_dk<K_, V_, true, false, SEGM>(p, stream);
+        default: return launch_tc_dk<K_, V_, true, true, SEGM>(p, stream);
+      }
+    }
+    if (SQ && p.direct) {
+      switch (t) {
+        case 0: return launch_tc_dk<K_, V_, false, false, DIRM>(p, stream);
+        case 1: return launch_tc_dk<K_, V_, false, true, DIRM>(p, stream);
+        case 2: return launch_tc_dk<K_, V_, true, false, DIRM>(p, stream);
+        default: return launch_tc_dk<K_, V_, true, true, DIRM>(p, stream);
       }
     }
     switch (t) {
-      case 0: return launch_tc_dk<K_, V_, false, false, false>(p, stream);
-      case 1: return launch_tc_dk<K_, V_, false, true, false>(p, stream);
-      case 2: return launch_tc_dk<K_, V_, true, false, false>(p, stream);
-      default: return launch_tc_dk<K_, V_, true, true, false>(p, stream);
+      case 0: return launch_tc_dk<K_, V_, false, false, 0>(p, stream);
+      case 1: return launch_tc_dk<K_, V_, false, true, 0>(p, stream);
+      case 2: return launch_tc_dk<K_, V_, true, false, 0>(p, stream);
+      default: return launch_tc_dk<K_, V_, true, true, 0>(p, stream);
     }
   };
   using I64 = std::integral_constant<int, 64>;
