@@ -223,21 +223,21 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 // c[16 x 8] += X[xr.., xc + k) * Y[yr + k, yc..) over k in [0, 8 nk8), nk8 <= 4, fp32 smem
-// with row stride LDF. Every operand is loaded before the first product.
+// with row stride LDF (xc a multiple of 4). Every operand is loaded before the first
+// product. The A fragments come from one ldmatrix per k step: read as 16-bit pairs, an
+// 8 x 8 b16 matrix is an 8 x 4 block of fp32 words and lane 4 g + t gets word (g, t), so
+// the four blocks (rows 0-7 / 8-15 by columns 0-3 / 4-7 of the step) are a0 .. a3; lane
+// l gives the address of row (l & 7) + 8 ((l >> 3) & 1), columns 4 (l >> 4) on.
 __device__ __forceinline__ void mma_tile(const float* X, int xr, int xc, const float* Y, int yr,
                                          int yc, int nk8, float (&c)[4], int lane) {
   const int g = lane >> 2, t = lane & 3;
-  const float* x0 = X + (xr + g) * LDF + xc + t;
-  const float* x1 = x0 + 8 * LDF;
+  const uint32_t xrow = smem_u32(X + (xr + (lane & 7) + 8 * ((lane >> 3) & 1)) * LDF + xc + 4 * (lane >> 4));
   const float* y0 = Y + (yr + t) * LDF + yc + g;
   uint32_t xa[4][4], yb[4][2];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if (k < nk8) {
-      xa[k][0] = __float_as_uint(x0[8 * k]);
-      xa[k][1] = __float_as_uint(x1[8 * k]);
-      xa[k][2] = __float_as_uint(x0[8 * k + 4]);
-      xa[k][3] = __float_as_uint(x1[8 * k + 4]);
+      ldmatrix_x4(xrow + 32u * k, xa[k][0], xa[k][1], xa[k][2], xa[k][3]);
       yb[k][0] = __float_as_uint(y0[8 * k * LDF]);
       yb[k][1] = __float_as_uint(y0[(8 * k + 4) * LDF]);
     }
